@@ -1,0 +1,225 @@
+/*
+ * moeq.h -- C ABI of the weight-only-quantised fused MoE library (libmoeq.so).
+ *
+ * The operations restate, as plain C, the interface documented on the vLLM API
+ * pages "vllm.model_executor.layers.quantization.experts_int8" (W8A16) and
+ * "vllm.model_executor.layers.quantization.moe_wna16" (W4A16):
+ *
+ *   ExpertsInt8MoEMethod.apply(layer, x, router_logits, top_k, renormalize, ...)
+ *     = select_experts(...)  -> moe_topk_route
+ *     + fused_experts(x, w13, w2, topk_weights, topk_ids, activation="silu",
+ *                     use_int8_w8a16=True, w1_scale, w2_scale)
+ *                            -> moe_align_block + moe_quant_forward
+ *   quantize_in_place_and_get_scales(weight) -> moe_quantize_int8_per_channel
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Every pointer marked (device) is a CUDA device pointer on the current
+ *   device; (host) pointers are ordinary host memory.  The caller owns every
+ *   buffer.  No call allocates or frees device memory.
+ * - All tensors are dense row-major with the shapes given; "bf16" is IEEE
+ *   bfloat16 (uint16 storage), "f16" IEEE half.  Device pointers must be
+ *   16-byte aligned.
+ * - `stream` is a cudaStream_t (NULL = the legacy default stream).  Device
+ *   work is enqueued on it and the call returns without waiting.
+ * - Return value: an mq_status.  Argument errors are detected on the host
+ *   before anything is launched, and leave every output untouched.  Errors
+ *   found on the device (an expert id outside [0, E), a bounded wait that ran
+ *   out) never trap: kernels set bits in a per-device status word, read with
+ *   mq_device_status().
+ * - mq_last_error_message() gives a human-readable reason for the most recent
+ *   failing call on the calling thread.
+ */
+#ifndef MOEQ_H
+#define MOEQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MQ_OK = 0,
+  MQ_ERR_INVALID_ARG = 1,   /* bad pointer, shape, alignment or size          */
+  MQ_ERR_UNSUPPORTED = 2,   /* well-formed but outside what the kernels cover */
+  MQ_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed              */
+  MQ_ERR_WORKSPACE = 4      /* workspace smaller than the query returned      */
+} mq_status;
+
+/* Bits of the device status word (see mq_device_status). */
+#define MQ_DEV_BAD_EXPERT_ID  0x1u  /* a topk id outside [0, E); slot ignored   */
+#define MQ_DEV_WAIT_TIMEOUT   0x2u  /* a pipeline wait gave up; output invalid  */
+
+const char* mq_status_string(int status);
+const char* mq_last_error_message(void);
+
+/*
+ * Waits for `stream`, then returns in *flags the OR of the MQ_DEV_* bits set
+ * by kernels on the current device since the last call, and clears them.
+ */
+int mq_device_status(void* stream, uint32_t* flags);
+
+/*
+ * moe_quantize_int8_per_channel -- experts_int8 page,
+ * quantize_in_place_and_get_scales (used by quantizing_weight_loader).
+ *
+ * For each row r of w (bf16 [rows, cols], device):
+ *   scale[r] = max_c |w[r,c]| / 127           (float32, IEEE division)
+ *   q[r,c]   = clamp(rint(w[r,c] / scale[r]), -127, 127)
+ *              (float32 true division, round half to even)
+ * A row of zeros gets scale 0 and codes 0.
+ * Outputs: q int8 [rows, cols] (device), scale float32 [rows] (device).
+ * For expert tensors pass rows = E * N (w13: N = 2I with the gate rows first,
+ * then the up rows; w2: N = H) and cols = K.
+ * Errors: MQ_ERR_INVALID_ARG for null pointers, rows/cols < 0, cols > 2^31,
+ * misaligned pointers or cols % 8 != 0.
+ */
+int moe_quantize_int8_per_channel(const void* w, int64_t rows, int64_t cols,
+                                  int8_t* q, float* scale, void* stream);
+
+/*
+ * moe_quantize_uint4_group -- produces the moe_wna16 page's W4A16 storage
+ * (MoeWNA16Method.create_weights) from bf16 weights.  The page consumes
+ * GPTQ/AWQ tensors already quantised; this call exists so that callers (and
+ * the benchmark) can build such tensors on the device.
+ *
+ * Per row r and group g of `group_size` consecutive columns:
+ *   lo = min(0, min w_g), hi = max(0, max w_g)
+ *   s  = f16((hi - lo) / 15)      z = clamp(rint(-lo / s), 0, 15)
+ *   q  = clamp(rint(w / s) + z, 0, 15)          (s == 0: z = 0, q = 0)
+ * Outputs (device):
+ *   qweight uint8 [rows, cols/2]   byte j = q[2j] | q[2j+1] << 4
+ *   scales  f16   [rows, cols/group_size]
+ *   qzeros  uint8 [rows/2, cols/group_size]  byte = z[2i] | z[2i+1] << 4
+ * Errors: MQ_ERR_INVALID_ARG for odd rows, group_size not in {32,64,128,256}
+ * or not dividing cols, null or misaligned pointers.
+ */
+int moe_quantize_uint4_group(const void* w, int64_t rows, int64_t cols, int group_size,
+                             uint8_t* qweight, uint16_t* scales, uint8_t* qzeros,
+                             void* stream);
+
+/*
+ * moe_topk_route -- the router of ExpertsInt8MoEMethod.apply
+ * (select_experts with scoring_func="softmax", top_k, renormalize).
+ *
+ * logits float32 [T, E] (device).  For each token: p = softmax(logits[t]);
+ * the k experts with the largest logits (ties -> lower index) fill slots
+ * j = 0..k-1 in decreasing order; topk_w[t,j] = p[id_j], divided by the sum
+ * of the k chosen p when renormalize != 0.
+ * Outputs: topk_w float32 [T, k], topk_ids int32 [T, k] (device).
+ * Limits: 1 <= k <= E <= 1024, k <= 32, T >= 0.
+ */
+int moe_topk_route(const float* logits, int T, int E, int k, int renormalize,
+                   float* topk_w, int32_t* topk_ids, void* stream);
+
+/*
+ * moe_align_capacity -- number of rows moe_align_block may produce:
+ * round_up(T*k + min(E, T*k) * (block_m - 1), block_m).  Returns -1 for bad
+ * arguments.
+ */
+int64_t moe_align_capacity(int T, int k, int E, int block_m);
+
+/*
+ * moe_align_block -- sorts the S = T*k token-slots (slot s = t*k + j) by
+ * expert, stably, and pads every expert's segment to a multiple of block_m
+ * with the sentinel S.  This is the grouping step fused_experts performs
+ * before its grouped GEMMs.
+ *
+ * Inputs: topk_ids int32 [T, k] (device).
+ * Outputs (device):
+ *   sorted_slot_ids int32 [capacity]: entries [0, num_padded) hold expert 0's
+ *       slots in increasing order, then padding, then expert 1's, ...;
+ *       entries past num_padded are unspecified.
+ *   block_expert    int32 [capacity / block_m]: expert of each block.
+ *   expert_offsets  int32 [E + 1]: padded segment starts; [E] = num_padded.
+ *   num_padded      int32 [1].
+ * An expert with no slot gets no block.  A slot whose id is outside [0, E)
+ * is left out and sets MQ_DEV_BAD_EXPERT_ID.
+ * Limits: E <= 1024, 1 <= block_m <= 1024, capacity >= moe_align_capacity().
+ */
+int moe_align_block(const int32_t* topk_ids, int T, int k, int E, int block_m,
+                    int32_t* sorted_slot_ids, int32_t* block_expert,
+                    int32_t* expert_offsets, int32_t* num_padded,
+                    int64_t capacity, void* stream);
+
+/*
+ * Weight formats of moe_quant_forward (bits, group_size, has_zp):
+ *   W8A16 (experts_int8):  bits = 8, group_size = -1, has_zp = 0
+ *     w13 int8 [E, 2I, H], w2 int8 [E, H, I],
+ *     s13 float32 [E, 2I], s2 float32 [E, H]       (dequant = q * s)
+ *   W4A16 (moe_wna16):     bits = 4, group_size in {32, 64, 128, 256}
+ *     w13 uint8 [E, 2I, H/2], w2 uint8 [E, H, I/2]  (two codes per byte,
+ *         even index in the low nibble)
+ *     s13 f16 [E, 2I, H/gs], s2 f16 [E, H, I/gs]
+ *     z13 uint8 [E, I, H/gs], z2 uint8 [E, H/2, I/gs] (zero points packed two
+ *         output rows per byte, even row low) when has_zp = 1; with
+ *         has_zp = 0 the zero point is 8 and z13/z2 must be NULL.
+ *     dequant = (q - z) * s
+ * In both, rows [0, I) of w13 are the gate projection (w1) and rows [I, 2I)
+ * the up projection (w3), as quantizing_weight_loader lays them out.
+ */
+
+/*
+ * moe_quant_forward_workspace -- bytes of device workspace moe_quant_forward
+ * needs for these sizes (0 on bad arguments).
+ */
+size_t moe_quant_forward_workspace(int T, int H, int I, int E, int k,
+                                   int bits, int group_size);
+
+/*
+ * moe_quant_forward -- fused_experts for the formats above:
+ *   for every token t and slot j with e = topk_ids[t,j]:
+ *     h  = dequant(w13[e]) . x[t]             (2I values)
+ *     a  = silu(h[0:I]) * h[I:2I]             silu(u) = u / (1 + exp(-u))
+ *     y  = dequant(w2[e]) . a                 (H values)
+ *     out[t] += topk_w[t,j] * y
+ * x bf16 [T, H] (device), topk_w float32 [T, k], topk_ids int32 [T, k]
+ * (device, e.g. from moe_topk_route), out bf16 [T, H] (device; must not
+ * overlap x).  The block alignment runs inside, in the workspace.
+ * Accumulation is float32; the intermediate a is rounded to bf16.
+ * Limits: H % 128 == 0, I % 128 == 0, E <= 1024, 1 <= k <= min(E, 32).
+ * Errors: MQ_ERR_INVALID_ARG (null/misaligned pointers, bad shapes),
+ * MQ_ERR_UNSUPPORTED (format or sizes outside the limits),
+ * MQ_ERR_WORKSPACE (ws_bytes below the query).
+ */
+int moe_quant_forward(const void* x, int T, int H, int I, int E, int k,
+                      int bits, int group_size, int has_zp,
+                      const void* w13, const void* w2,
+                      const void* s13, const void* s2,
+                      const uint8_t* z13, const uint8_t* z2,
+                      const float* topk_w, const int32_t* topk_ids,
+                      void* workspace, size_t ws_bytes,
+                      void* out, void* stream);
+
+/*
+ * Instrumentation (no counterpart on the pages; used by the benchmark).
+ *
+ * mq_kernel_launch_count: kernels this library has launched in this process.
+ * mq_profile_enable(on): while on, every kernel launch is bracketed by a pair
+ *   of CUDA events recorded on the launch's own stream (costs a few
+ *   microseconds of host time per launch).
+ * mq_profile_read(total_ms, launches, n_slots): waits for the recorded
+ *   events, writes per slot the summed device time in milliseconds and the
+ *   number of timed launches (host arrays of n_slots entries), and resets.
+ *   Slots are the MQ_PROF_* values.
+ */
+#define MQ_PROF_QUANT   0
+#define MQ_PROF_ROUTE   1
+#define MQ_PROF_ALIGN   2
+#define MQ_PROF_GEMM1   3
+#define MQ_PROF_GEMM2   4
+#define MQ_PROF_COMBINE 5
+#define MQ_PROF_GATHER  6
+#define MQ_PROF_SLOTS   8
+
+long long mq_kernel_launch_count(void);
+int mq_profile_enable(int on);
+int mq_profile_read(double* total_ms, long long* launches, int n_slots);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOEQ_H */

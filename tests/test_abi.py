@@ -1,0 +1,76 @@
+"""CPU checks of the C ABI: the library builds, loads, exports every symbol
+that include/moeq.h declares, and rejects bad arguments on the host before
+launching anything (no GPU needed for these paths)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from weight_quantized_moe_gb300 import binding, build
+    build.build()
+    return binding.lib()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "moeq.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(?:int|int64_t|size_t|long long|const char\*)\s+(\w+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    from weight_quantized_moe_gb300 import binding
+    assert binding.mq_status_string(0) == "ok"
+    assert "invalid" in binding.mq_status_string(1)
+
+
+def test_align_capacity(lib):
+    from weight_quantized_moe_gb300 import binding
+    import oracle
+    for args in [(16, 2, 8, 16), (1, 2, 8, 64), (8192, 2, 8, 128), (4096, 8, 128, 64), (0, 2, 8, 16)]:
+        assert binding.moe_align_capacity(*args) == oracle.align_capacity(*args)
+    assert binding.moe_align_capacity(-1, 2, 8, 16) == -1
+
+
+def test_host_side_rejections(lib):
+    vp = ctypes.c_void_p
+    fake = vp(0x1000)  # never dereferenced: every case fails validation first
+    # unsupported format (bits=8 with a group size)
+    assert lib.moe_quant_forward(fake, 4, 128, 128, 8, 2, 8, 128, 0, fake, fake, fake, fake,
+                                 None, None, fake, fake, fake, 1 << 20, fake, None) == 2
+    # H not a multiple of 128
+    assert lib.moe_quant_forward(fake, 4, 100, 128, 8, 2, 8, -1, 0, fake, fake, fake, fake,
+                                 None, None, fake, fake, fake, 1 << 20, fake, None) == 2
+    # k > E
+    assert lib.moe_quant_forward(fake, 4, 128, 128, 2, 3, 8, -1, 0, fake, fake, fake, fake,
+                                 None, None, fake, fake, fake, 1 << 20, fake, None) == 1
+    # workspace too small
+    assert lib.moe_quant_forward(fake, 4, 128, 128, 8, 2, 8, -1, 0, fake, fake, fake, fake,
+                                 None, None, fake, fake, fake, 16, vp(0x9000), None) == 4
+    # out overlapping x
+    assert lib.moe_quant_forward(fake, 4, 128, 128, 8, 2, 8, -1, 0, fake, fake, fake, fake,
+                                 None, None, fake, fake, fake, 1 << 30, vp(0x1100), None) == 1
+    assert b"overlap" in lib.mq_last_error_message()
+    # null pointers, odd rows, bad group size, k > 32
+    assert lib.moe_quantize_int8_per_channel(None, 4, 8, fake, fake, None) == 1
+    assert lib.moe_quantize_int8_per_channel(fake, 4, 12, fake, fake, None) == 1
+    assert lib.moe_quantize_uint4_group(fake, 3, 256, 128, fake, fake, fake, None) == 1
+    assert lib.moe_quantize_uint4_group(fake, 4, 256, 96, fake, fake, fake, None) == 1
+    assert lib.moe_topk_route(fake, 4, 64, 33, 1, fake, fake, None) == 1
+    assert lib.moe_topk_route(fake, 4, 2048, 8, 1, fake, fake, None) == 2
+    assert lib.moe_align_block(fake, 4, 2, 8, 16, fake, fake, fake, fake, 8, None) == 1
+    assert lib.moe_quant_forward_workspace(4, 128, 128, 8, 2, 8, -1) > 0
+    assert lib.moe_quant_forward_workspace(4, 128, 128, 8, 2, 3, -1) == 0

@@ -1,0 +1,121 @@
+"""GPU parity of moe_quant_forward (route + align + expert GEMMs + combine)
+against the oracle, within the forward tolerance of moe_helpers."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from moe_helpers import FWD_TOL, Layer, forward_error, inputs
+from weight_quantized_moe_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+mq = pytest.importorskip("weight_quantized_moe_gb300")
+
+W = synth.WORKLOADS
+
+
+def _run(layer, T, seed=0, tokens=None, out_cols=None, renorm=True):
+    x, lg = inputs(layer.wl, T, seed)
+    tw, tid = mq.moe_topk_route(lg, layer.k, renorm)
+    out = layer.forward(x, tw, tid)
+    torch.cuda.synchronize()
+    assert mq.mq_device_status() == 0
+    ids = tid.cpu().numpy()
+    ow, oid = oracle.topk_route(lg.cpu().numpy(), layer.k, renorm)
+    assert np.array_equal(ids, oid)
+    sel = np.arange(T) if tokens is None else np.asarray(tokens)
+    ex = layer.oracle_experts(np.unique(ids[sel]))
+    ref = oracle.moe_forward(x.float().cpu().numpy(), ex, ow, oid, tokens=sel, out_cols=out_cols)
+    got = out.float().cpu().numpy()[sel]
+    if out_cols is not None:
+        got = got[:, out_cols]
+    return forward_error(got, ref)
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    return Layer(W["tiny"], seed=0)
+
+
+@pytest.mark.parametrize("T", [16, 1, 37, 300])
+def test_forward_tiny(tiny, T):
+    assert _run(tiny, T, seed=T) <= FWD_TOL
+
+
+def test_forward_tiny_no_renormalise(tiny):
+    assert _run(tiny, 16, seed=5, renorm=False) <= FWD_TOL
+
+
+def test_forward_k_equals_e_identical_experts():
+    """Dense-MLP identity on the GPU: k = E, equal logits."""
+    wl = synth.Workload("dense", E=4, k=4, H=128, I=128, Ts=(8,))
+    layer = Layer(wl, seed=3)
+    w13, w2 = layer._bf16
+    w13[1:] = w13[0]
+    w2[1:] = w2[0]
+    layer.q13, layer.s13 = mq.moe_quantize_int8_per_channel(w13)
+    layer.q2, layer.s2 = mq.moe_quantize_int8_per_channel(w2)
+    x = synth.hidden_states(8, 128, seed=1, device="cuda")
+    lg = torch.zeros(8, 4, device="cuda")
+    tw, tid = mq.moe_topk_route(lg, 4, True)
+    out = layer.forward(x, tw, tid).float().cpu().numpy()
+    ex = layer.oracle_experts([0])
+    W13, W2 = ex.deq13(0), ex.deq2(0)
+    h = x.float().cpu().numpy().astype(np.float64) @ W13.T
+    ref = (oracle.silu(h[:, :128]) * h[:, 128:]) @ W2.T
+    assert forward_error(out, ref) <= FWD_TOL
+
+
+def test_forward_zero_input(tiny):
+    x = torch.zeros(4, 128, dtype=torch.bfloat16, device="cuda")
+    tw, tid = mq.moe_topk_route(synth.router_logits(4, 8, 1, device="cuda"), 2, True)
+    assert torch.count_nonzero(tiny.forward(x, tw, tid)).item() == 0
+
+
+def test_forward_invalid_ids_flagged(tiny):
+    x, lg = inputs(tiny.wl, 6, seed=9)
+    tw, tid = mq.moe_topk_route(lg, 2, True)
+    tid[1, 1] = 8
+    tid[4, 0] = -3
+    out = tiny.forward(x, tw, tid)
+    assert mq.mq_device_status() == mq.MQ_DEV_BAD_EXPERT_ID
+    ids = tid.cpu().numpy()
+    ex = tiny.oracle_experts()
+    ref = oracle.moe_forward(x.float().cpu().numpy(), ex, tw.cpu().numpy(), ids)
+    assert forward_error(out.float().cpu().numpy(), ref) <= FWD_TOL
+
+
+def test_forward_empty_batch(tiny):
+    x = torch.zeros(0, 128, dtype=torch.bfloat16, device="cuda")
+    tw = torch.zeros(0, 2, device="cuda")
+    tid = torch.zeros(0, 2, dtype=torch.int32, device="cuda")
+    assert tiny.forward(x, tw, tid).shape == (0, 128)
+
+
+def test_forward_fine_grained_full():
+    """E=128, k=8, H=2048, I=768 with Zipf-skewed routing (zero-token experts)."""
+    layer = Layer(W["fine"], seed=0)
+    assert _run(layer, 64, seed=1) <= FWD_TOL
+
+
+def test_forward_w4a16():
+    wl = synth.Workload("w4a16_small", E=8, k=3, H=256, I=384, Ts=(24,), bits=4, group_size=128,
+                        has_zp=True)
+    layer = Layer(wl, seed=2)
+    assert _run(layer, 24, seed=2) <= FWD_TOL
+
+
+def test_forward_w4a16_full_sampled():
+    """The full W4A16 layer (E=64, k=6, H=2048, I=1408, gs=128) at T=32."""
+    layer = Layer(W["w4a16"], seed=0)
+    assert _run(layer, 32, seed=3, tokens=[0, 7, 31]) <= FWD_TOL
+
+
+def test_forward_mixtral_decode_sampled():
+    """Mixtral-shaped layer at T=64, the benchmarked decode size: two sampled
+    tokens, 512 sampled output columns."""
+    layer = Layer(W["mixtral_decode"], seed=0)
+    cols = np.sort(np.random.default_rng(0).choice(4096, 512, replace=False))
+    assert _run(layer, 64, seed=0, tokens=[5, 40], out_cols=cols) <= FWD_TOL

@@ -1,0 +1,242 @@
+"""ctypes binding of libmoeq.so: same names as the C ABI in include/moeq.h.
+
+Argument marshalling only.  Each function checks dtypes/shapes/devices of
+the torch tensors it is given, allocates missing outputs with torch (the
+caller side of the ABI owns memory), and passes raw device pointers plus the
+current CUDA stream.  All computation happens in the library's kernels; if
+the library is missing, every call raises -- there is no fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoeq.so")
+
+MQ_OK, MQ_ERR_INVALID_ARG, MQ_ERR_UNSUPPORTED, MQ_ERR_CUDA, MQ_ERR_WORKSPACE = range(5)
+MQ_DEV_BAD_EXPERT_ID = 0x1
+MQ_DEV_WAIT_TIMEOUT = 0x2
+
+_vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+_SIGNATURES = {
+    "mq_status_string": (ctypes.c_char_p, [_i32]),
+    "mq_last_error_message": (ctypes.c_char_p, []),
+    "mq_device_status": (_i32, [_vp, ctypes.POINTER(ctypes.c_uint32)]),
+    "moe_quantize_int8_per_channel": (_i32, [_vp, _i64, _i64, _vp, _vp, _vp]),
+    "moe_quantize_uint4_group": (_i32, [_vp, _i64, _i64, _i32, _vp, _vp, _vp, _vp]),
+    "moe_topk_route": (_i32, [_vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp]),
+    "moe_align_capacity": (_i64, [_i32, _i32, _i32, _i32]),
+    "moe_align_block": (_i32, [_vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _i64, _vp]),
+    "moe_quant_forward_workspace": (_sz, [_i32] * 7),
+    "moe_quant_forward": (_i32, [_vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
+                                 _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _vp]),
+    "mq_kernel_launch_count": (ctypes.c_longlong, []),
+    "mq_profile_enable": (_i32, [_i32]),
+    "mq_profile_read": (_i32, [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_longlong), _i32]),
+}
+
+PROF_SLOTS = ("quant", "route", "align", "gemm1", "gemm2", "combine", "gather", "slot7")
+
+_lib = None
+
+
+class MoeqError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"moeq status {status}: {message}")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmoeq.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(status: int) -> None:
+    if status != MQ_OK:
+        msg = lib().mq_last_error_message().decode()
+        raise MoeqError(status, msg)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t, dtype, name, ndim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims")
+
+
+def mq_kernel_launch_count() -> int:
+    """Kernels launched by the library in this process so far."""
+    return int(lib().mq_kernel_launch_count())
+
+
+def mq_profile_enable(on: bool) -> None:
+    _check(lib().mq_profile_enable(int(bool(on))))
+
+
+def mq_profile_read() -> dict:
+    """{slot name: (total device ms, timed launches)} since the last read."""
+    n = len(PROF_SLOTS)
+    ms = (ctypes.c_double * n)()
+    cnt = (ctypes.c_longlong * n)()
+    _check(lib().mq_profile_read(ms, cnt, n))
+    return {PROF_SLOTS[i]: (float(ms[i]), int(cnt[i])) for i in range(n) if cnt[i]}
+
+
+def mq_status_string(status: int) -> str:
+    return lib().mq_status_string(status).decode()
+
+
+def mq_device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status bits."""
+    flags = ctypes.c_uint32(0)
+    _check(lib().mq_device_status(_stream(stream), ctypes.byref(flags)))
+    return int(flags.value)
+
+
+def moe_quantize_int8_per_channel(w, q=None, scale=None, stream=None):
+    """bf16 [rows, cols] -> (int8 [rows, cols], float32 [rows])."""
+    w2d = w.reshape(-1, w.shape[-1])
+    _need(w2d, torch.bfloat16, "w", 2)
+    rows, cols = w2d.shape
+    if q is None:
+        q = torch.empty(w.shape, dtype=torch.int8, device=w.device)
+    if scale is None:
+        scale = torch.empty(w.shape[:-1], dtype=torch.float32, device=w.device)
+    _need(q, torch.int8, "q")
+    _need(scale, torch.float32, "scale")
+    if q.numel() != w.numel() or scale.numel() != rows:
+        raise ValueError("q / scale have the wrong size")
+    _check(lib().moe_quantize_int8_per_channel(_ptr(w2d), rows, cols, _ptr(q), _ptr(scale),
+                                               _stream(stream)))
+    return q, scale
+
+
+def moe_quantize_uint4_group(w, group_size, stream=None):
+    """bf16 [.., N, K] -> (qweight uint8 [.., N, K/2], scales f16 [.., N, K/gs],
+    qzeros uint8 [.., N/2, K/gs])."""
+    w2d = w.reshape(-1, w.shape[-1])
+    _need(w2d, torch.bfloat16, "w", 2)
+    rows, cols = w2d.shape
+    lead = tuple(w.shape[:-2])
+    N = w.shape[-2]
+    G = cols // group_size if group_size > 0 else 0
+    qw = torch.empty(*w.shape[:-1], cols // 2, dtype=torch.uint8, device=w.device)
+    sc = torch.empty(*w.shape[:-1], max(G, 1), dtype=torch.float16, device=w.device)
+    qz = torch.empty(*lead, N // 2, max(G, 1), dtype=torch.uint8, device=w.device)
+    _check(lib().moe_quantize_uint4_group(_ptr(w2d), rows, cols, group_size, _ptr(qw), _ptr(sc),
+                                          _ptr(qz), _stream(stream)))
+    return qw, sc, qz
+
+
+def moe_topk_route(logits, k, renormalize, topk_w=None, topk_ids=None, stream=None):
+    """fp32 [T, E] -> (topk_w fp32 [T, k], topk_ids int32 [T, k])."""
+    _need(logits, torch.float32, "logits", 2)
+    T, E = logits.shape
+    if topk_w is None:
+        topk_w = torch.empty(T, k, dtype=torch.float32, device=logits.device)
+    if topk_ids is None:
+        topk_ids = torch.empty(T, k, dtype=torch.int32, device=logits.device)
+    _need(topk_w, torch.float32, "topk_w")
+    _need(topk_ids, torch.int32, "topk_ids")
+    if topk_w.numel() != T * k or topk_ids.numel() != T * k:
+        raise ValueError("topk_w / topk_ids must hold T * k elements")
+    _check(lib().moe_topk_route(_ptr(logits), T, E, k, int(bool(renormalize)), _ptr(topk_w),
+                                _ptr(topk_ids), _stream(stream)))
+    return topk_w, topk_ids
+
+
+def moe_align_capacity(T, k, E, block_m) -> int:
+    return int(lib().moe_align_capacity(T, k, E, block_m))
+
+
+def moe_align_block(topk_ids, E, block_m, stream=None):
+    """int32 [T, k] -> (sorted_slot_ids [cap], block_expert [cap/bm],
+    expert_offsets [E+1], num_padded [1]); all int32 on the device."""
+    _need(topk_ids, torch.int32, "topk_ids", 2)
+    T, k = topk_ids.shape
+    cap = moe_align_capacity(T, k, E, block_m)
+    if cap < 0:
+        raise ValueError("bad align arguments")
+    dev = topk_ids.device
+    sorted_ids = torch.empty(max(cap, 1), dtype=torch.int32, device=dev)
+    block_expert = torch.empty(max(cap // block_m, 1), dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    num_padded = torch.empty(1, dtype=torch.int32, device=dev)
+    _check(lib().moe_align_block(_ptr(topk_ids), T, k, E, block_m, _ptr(sorted_ids),
+                                 _ptr(block_expert), _ptr(offsets), _ptr(num_padded), cap,
+                                 _stream(stream)))
+    return sorted_ids, block_expert, offsets, num_padded
+
+
+def moe_quant_forward_workspace(T, H, I, E, k, bits=8, group_size=-1) -> int:
+    return int(lib().moe_quant_forward_workspace(T, H, I, E, k, bits, group_size))
+
+
+def moe_quant_forward(x, w13, w2, s13, s2, topk_w, topk_ids, bits=8, group_size=-1,
+                      has_zp=False, z13=None, z2=None, workspace=None, out=None, stream=None):
+    """The fused expert MLP (see moe_quant_forward in include/moeq.h)."""
+    _need(x, torch.bfloat16, "x", 2)
+    T, H = x.shape
+    E = w13.shape[0]
+    I = w13.shape[1] // 2
+    k = topk_ids.shape[-1] if topk_ids.dim() == 2 else 1
+    if bits == 8:
+        _need(w13, torch.int8, "w13", 3)
+        _need(w2, torch.int8, "w2", 3)
+        _need(s13, torch.float32, "s13")
+        _need(s2, torch.float32, "s2")
+    else:
+        _need(w13, torch.uint8, "w13", 3)
+        _need(w2, torch.uint8, "w2", 3)
+        _need(s13, torch.float16, "s13")
+        _need(s2, torch.float16, "s2")
+        if has_zp:
+            _need(z13, torch.uint8, "z13")
+            _need(z2, torch.uint8, "z2")
+    _need(topk_w, torch.float32, "topk_w")
+    _need(topk_ids, torch.int32, "topk_ids")
+    ws_need = moe_quant_forward_workspace(T, H, I, E, k, bits, group_size)
+    if workspace is None:
+        workspace = torch.empty(max(ws_need, 16), dtype=torch.uint8, device=x.device)
+    _need(workspace, torch.uint8, "workspace")
+    if out is None:
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=x.device)
+    _need(out, torch.bfloat16, "out", 2)
+    _check(lib().moe_quant_forward(
+        _ptr(x), T, H, I, E, k, bits, group_size, int(bool(has_zp)),
+        _ptr(w13), _ptr(w2), _ptr(s13), _ptr(s2), _ptr(z13 if has_zp else None),
+        _ptr(z2 if has_zp else None), _ptr(topk_w), _ptr(topk_ids),
+        _ptr(workspace), workspace.numel(), _ptr(out), _stream(stream)))
+    return out

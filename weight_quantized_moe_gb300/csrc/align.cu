@@ -1,0 +1,124 @@
+// Block alignment: stable counting sort of the token-slots by expert, each
+// expert's segment padded to a multiple of block_m (the grouping fused_experts
+// performs before its grouped GEMMs).
+//
+// One CTA of 32 warps.  Warp w owns the contiguous slot range
+// [w * chunk, (w + 1) * chunk).
+//   1. per-warp histograms hist[w][e] (shared-memory atomics);
+//   2. per expert: count, pad, block-wide exclusive scan -> segment starts;
+//      hist[w][e] becomes the first position of warp w's slots of expert e;
+//   3. each warp walks its range again in slot order and places every slot at
+//      hist[w][e] + (rank among equal experts in this 32-slot step), found
+//      with __match_any_sync; the rank order is lane order, i.e. slot order.
+// The result is therefore deterministic and identical to a stable sort.
+#include "common.cuh"
+
+namespace {
+
+constexpr int kWarps = 32;
+constexpr int kThreads = kWarps * 32;
+
+__global__ void __launch_bounds__(kThreads, 1)
+    align_kernel(const int32_t* __restrict__ ids, int S, int E, int bm, int32_t* __restrict__ sorted,
+                 int32_t* __restrict__ block_expert, int32_t* __restrict__ offsets,
+                 int32_t* __restrict__ num_padded, unsigned* status) {
+  extern __shared__ int smem[];
+  int* hist = smem;                   // [kWarps][E]
+  int* warp_tot = smem + kWarps * E;  // [kWarps] scan scratch
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+
+  for (int i = tid; i < kWarps * E; i += kThreads) hist[i] = 0;
+  __syncthreads();
+
+  const int chunk = (S + kWarps - 1) / kWarps;
+  const int begin = warp * chunk;
+  const int end = min(S, begin + chunk);
+  bool bad = false;
+  for (int base = begin; base < end; base += 32) {
+    const int s = base + lane;
+    if (s < end) {
+      const int e = ids[s];
+      if (e >= 0 && e < E) atomicAdd(&hist[warp * E + e], 1);
+      else bad = true;
+    }
+  }
+  if (__any_sync(0xffffffffu, bad) && lane == 0) mq::flag(status, MQ_DEV_BAD_EXPERT_ID);
+  __syncthreads();
+
+  // ---- per-expert totals and exclusive scan of the padded sizes ----------
+  const int e = tid;  // E <= kThreads
+  int count = 0;
+  if (e < E)
+    for (int w = 0; w < kWarps; ++w) count += hist[w * E + e];
+  const int padded = (count + bm - 1) / bm * bm;
+  int incl = padded;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int t = warp_tot[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += n;
+    }
+    warp_tot[lane] = t;  // inclusive over warps
+  }
+  __syncthreads();
+  const int start = incl - padded + (warp ? warp_tot[warp - 1] : 0);
+  if (e < E) {
+    offsets[e] = start;
+    int run = start;
+    for (int w = 0; w < kWarps; ++w) {
+      const int c = hist[w * E + e];
+      hist[w * E + e] = run;
+      run += c;
+    }
+    for (int p = start + count; p < start + padded; ++p) sorted[p] = S;
+    for (int b = start / bm; b < (start + padded) / bm; ++b) block_expert[b] = e;
+  }
+  if (tid == 0) {
+    const int total = warp_tot[kWarps - 1];
+    offsets[E] = total;
+    num_padded[0] = total;
+  }
+  __syncthreads();
+
+  // ---- stable placement ---------------------------------------------------
+  for (int base = begin; base < end; base += 32) {
+    const int s = base + lane;
+    int ex = -1;
+    if (s < end) {
+      ex = ids[s];
+      if (ex < 0 || ex >= E) ex = -1;
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, ex);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    if (ex >= 0) sorted[hist[warp * E + ex] + rank] = s;
+    __syncwarp();
+    if (ex >= 0 && rank == 0) hist[warp * E + ex] += __popc(peers);
+    __syncwarp();
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int bm, int32_t* sorted,
+                         int32_t* block_expert, int32_t* offsets, int32_t* num_padded,
+                         unsigned* status, cudaStream_t st) {
+  const size_t smem = (size_t)(kWarps * E + kWarps) * sizeof(int);
+  if (smem > 48 * 1024) {
+    cudaError_t err =
+        cudaFuncSetAttribute(align_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+  }
+  align_kernel<<<1, kThreads, smem, st>>>(ids, T * k, E, bm, sorted, block_expert, offsets,
+                                          num_padded, status);
+  return cudaGetLastError();
+}

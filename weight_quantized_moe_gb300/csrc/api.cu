@@ -1,0 +1,386 @@
+// C ABI of libmoeq.so: argument validation, workspace layout and launches.
+// Every exported function is declared, with its contract, in include/moeq.h.
+#include "common.cuh"
+
+#include <atomic>
+#include <mutex>
+#include <stdarg.h>
+#include <stdio.h>
+#include <vector>
+
+#define MQ_EXPORT extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+// ---------------------------------------------------------------------------
+// Launch accounting and optional per-kernel CUDA-event timing.
+// ---------------------------------------------------------------------------
+std::atomic<long long> g_launches{0};
+std::atomic<int> g_prof_on{0};
+std::mutex g_prof_mu;
+struct ProfRec {
+  int slot;
+  cudaEvent_t a, b;
+};
+std::vector<ProfRec> g_prof_pending;
+std::vector<cudaEvent_t> g_event_pool;
+double g_prof_ms[MQ_PROF_SLOTS];
+long long g_prof_n[MQ_PROF_SLOTS];
+
+cudaEvent_t pool_event() {
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+// Counts one kernel launch and, while profiling is on, brackets it with a
+// pair of events on its stream.
+struct LaunchScope {
+  int slot;
+  cudaStream_t st;
+  cudaEvent_t a = nullptr;
+  LaunchScope(int s, cudaStream_t stream) : slot(s), st(stream) {
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (g_prof_on.load(std::memory_order_relaxed)) {
+      a = pool_event();
+      if (a) cudaEventRecord(a, st);
+    }
+  }
+  ~LaunchScope() {
+    if (!a) return;
+    cudaEvent_t b = pool_event();
+    if (!b) return;
+    cudaEventRecord(b, st);
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    g_prof_pending.push_back({slot, a, b});
+  }
+};
+
+thread_local char g_msg[512] = "";
+
+int fail(int status, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return status;
+}
+
+int cuda_fail(cudaError_t err, const char* what) {
+  return fail(MQ_ERR_CUDA, "%s: %s", what, cudaGetErrorString(err));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Device status word (one per device, in this library's module).
+__device__ unsigned g_dev_status;
+
+constexpr int kMaxDevices = 64;
+unsigned* g_status_ptr[kMaxDevices];
+std::mutex g_status_mu;
+
+unsigned* status_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_status_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_dev_status) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<unsigned*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+inline size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
+
+// Workspace layout of moe_quant_forward.  W8A16 runs the tensor-core path
+// (gathered activations, split-K partial outputs); W4A16 the CUDA-core path.
+struct WsLayout {
+  size_t sorted, block_expert, offsets, num_padded, xs, act, y, total;
+  int64_t cap;
+  TcPlan plan;
+  bool tc;
+};
+
+WsLayout ws_layout(int T, int H, int I, int E, int k, int bits) {
+  WsLayout L;
+  L.tc = (bits == 8);
+  L.plan = L.tc ? tc_plan(T, H, I, E, k) : TcPlan{simple_block_m(), 1};
+  const int bm = L.plan.bn;
+  const int64_t S = (int64_t)T * k;
+  const int64_t cap = moe_align_capacity(T, k, E, bm);
+  L.cap = cap;
+  size_t off = 0;
+  L.sorted = off;       off += align256(sizeof(int32_t) * (size_t)cap);
+  L.block_expert = off; off += align256(sizeof(int32_t) * (size_t)(cap / bm));
+  L.offsets = off;      off += align256(sizeof(int32_t) * (size_t)(E + 1));
+  L.num_padded = off;   off += align256(sizeof(int32_t));
+  L.xs = off;           off += L.tc ? align256(sizeof(__nv_bfloat16) * (size_t)cap * (size_t)H) : 0;
+  L.act = off;          off += align256(sizeof(__nv_bfloat16) * (size_t)cap * (size_t)I);
+  L.y = off;            off += align256(sizeof(float) * (size_t)L.plan.splits * (size_t)S * (size_t)H);
+  L.total = off;
+  return L;
+}
+
+bool fmt_ok(int bits, int group_size, int has_zp) {
+  if (bits == 8) return group_size == -1 && has_zp == 0;
+  if (bits == 4)
+    return (group_size == 32 || group_size == 64 || group_size == 128 || group_size == 256) &&
+           (has_zp == 0 || has_zp == 1);
+  return false;
+}
+
+}  // namespace
+
+MQ_EXPORT const char* mq_status_string(int status) {
+  switch (status) {
+    case MQ_OK: return "ok";
+    case MQ_ERR_INVALID_ARG: return "invalid argument";
+    case MQ_ERR_UNSUPPORTED: return "unsupported";
+    case MQ_ERR_CUDA: return "CUDA error";
+    case MQ_ERR_WORKSPACE: return "workspace too small";
+    default: return "unknown status";
+  }
+}
+
+MQ_EXPORT const char* mq_last_error_message(void) { return g_msg; }
+
+MQ_EXPORT long long mq_kernel_launch_count(void) { return g_launches.load(); }
+
+MQ_EXPORT int mq_profile_enable(int on) {
+  g_prof_on.store(on ? 1 : 0);
+  return MQ_OK;
+}
+
+MQ_EXPORT int mq_profile_read(double* total_ms, long long* launches, int n_slots) {
+  if (!total_ms || !launches || n_slots < 1) return fail(MQ_ERR_INVALID_ARG, "bad profile buffers");
+  std::vector<ProfRec> recs;
+  {
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    recs.swap(g_prof_pending);
+  }
+  int status = MQ_OK;
+  for (const ProfRec& r : recs) {
+    float ms = 0.0f;
+    cudaError_t err = cudaEventSynchronize(r.b);
+    if (err == cudaSuccess) err = cudaEventElapsedTime(&ms, r.a, r.b);
+    if (err != cudaSuccess) status = cuda_fail(err, "mq_profile_read");
+    g_prof_ms[r.slot] += ms;
+    g_prof_n[r.slot] += 1;
+  }
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  for (const ProfRec& r : recs) {
+    g_event_pool.push_back(r.a);
+    g_event_pool.push_back(r.b);
+  }
+  for (int i = 0; i < n_slots; ++i) {
+    total_ms[i] = i < MQ_PROF_SLOTS ? g_prof_ms[i] : 0.0;
+    launches[i] = i < MQ_PROF_SLOTS ? g_prof_n[i] : 0;
+  }
+  for (int i = 0; i < MQ_PROF_SLOTS; ++i) {
+    g_prof_ms[i] = 0.0;
+    g_prof_n[i] = 0;
+  }
+  return status;
+}
+
+MQ_EXPORT int mq_device_status(void* stream, uint32_t* flags) {
+  if (!flags) return fail(MQ_ERR_INVALID_ARG, "flags is NULL");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t err = cudaStreamSynchronize(st);
+  if (err != cudaSuccess) return cuda_fail(err, "mq_device_status: stream synchronize");
+  unsigned v = 0;
+  err = cudaMemcpyFromSymbol(&v, g_dev_status, sizeof(v));
+  if (err != cudaSuccess) return cuda_fail(err, "mq_device_status: read");
+  const unsigned zero = 0;
+  err = cudaMemcpyToSymbol(g_dev_status, &zero, sizeof(zero));
+  if (err != cudaSuccess) return cuda_fail(err, "mq_device_status: clear");
+  *flags = v;
+  return MQ_OK;
+}
+
+MQ_EXPORT int moe_quantize_int8_per_channel(const void* w, int64_t rows, int64_t cols, int8_t* q,
+                                            float* scale, void* stream) {
+  if (rows < 0 || cols < 0) return fail(MQ_ERR_INVALID_ARG, "negative size");
+  if (cols % 8 || cols > (int64_t(1) << 31) - 8)
+    return fail(MQ_ERR_INVALID_ARG, "cols must be a multiple of 8 below 2^31");
+  if (rows == 0) return MQ_OK;
+  if (cols == 0) return fail(MQ_ERR_INVALID_ARG, "cols must be positive");
+  if (!w || !q || !scale) return fail(MQ_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(w) || !aligned16(q)) return fail(MQ_ERR_INVALID_ARG, "w and q must be 16-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  LaunchScope ls(MQ_PROF_QUANT, st);
+  cudaError_t err = launch_quant_int8(w, rows, cols, q, scale, st);
+  return err == cudaSuccess ? MQ_OK : cuda_fail(err, "quantize_int8 launch");
+}
+
+MQ_EXPORT int moe_quantize_uint4_group(const void* w, int64_t rows, int64_t cols, int group_size,
+                                       uint8_t* qweight, uint16_t* scales, uint8_t* qzeros,
+                                       void* stream) {
+  if (rows < 0 || cols <= 0) return fail(MQ_ERR_INVALID_ARG, "bad size");
+  if (rows % 2) return fail(MQ_ERR_INVALID_ARG, "rows must be even (zero points pack two rows)");
+  if (!(group_size == 32 || group_size == 64 || group_size == 128 || group_size == 256))
+    return fail(MQ_ERR_INVALID_ARG, "group_size must be 32, 64, 128 or 256");
+  if (cols % group_size) return fail(MQ_ERR_INVALID_ARG, "group_size must divide cols");
+  if (cols > (int64_t(1) << 30)) return fail(MQ_ERR_INVALID_ARG, "cols too large");
+  if (rows == 0) return MQ_OK;
+  if (!w || !qweight || !scales || !qzeros) return fail(MQ_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(w) || !aligned16(qweight)) return fail(MQ_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  LaunchScope ls(MQ_PROF_QUANT, st);
+  cudaError_t err = launch_quant_uint4(w, rows, cols, group_size, qweight, scales, qzeros, st);
+  return err == cudaSuccess ? MQ_OK : cuda_fail(err, "quantize_uint4 launch");
+}
+
+MQ_EXPORT int moe_topk_route(const float* logits, int T, int E, int k, int renormalize,
+                             float* topk_w, int32_t* topk_ids, void* stream) {
+  if (T < 0) return fail(MQ_ERR_INVALID_ARG, "T must be >= 0");
+  if (E < 1 || E > 1024) return fail(MQ_ERR_UNSUPPORTED, "E must be in [1, 1024]");
+  if (k < 1 || k > E || k > 32) return fail(MQ_ERR_INVALID_ARG, "need 1 <= k <= min(E, 32)");
+  if (T == 0) return MQ_OK;
+  if (!logits || !topk_w || !topk_ids) return fail(MQ_ERR_INVALID_ARG, "null pointer");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  LaunchScope ls(MQ_PROF_ROUTE, st);
+  cudaError_t err = launch_route(logits, T, E, k, renormalize ? 1 : 0, topk_w, topk_ids, st);
+  return err == cudaSuccess ? MQ_OK : cuda_fail(err, "route launch");
+}
+
+MQ_EXPORT int64_t moe_align_capacity(int T, int k, int E, int block_m) {
+  if (T < 0 || k < 1 || E < 1 || block_m < 1) return -1;
+  const int64_t S = (int64_t)T * k;
+  const int64_t cap = S + (int64_t)(E < S ? E : S) * (block_m - 1);
+  return (cap + block_m - 1) / block_m * block_m;
+}
+
+MQ_EXPORT int moe_align_block(const int32_t* topk_ids, int T, int k, int E, int block_m,
+                              int32_t* sorted_slot_ids, int32_t* block_expert,
+                              int32_t* expert_offsets, int32_t* num_padded, int64_t capacity,
+                              void* stream) {
+  if (T < 0 || k < 1 || E < 1) return fail(MQ_ERR_INVALID_ARG, "bad T, k or E");
+  if (E > 1024) return fail(MQ_ERR_UNSUPPORTED, "E must be <= 1024");
+  if (block_m < 1 || block_m > 1024) return fail(MQ_ERR_INVALID_ARG, "block_m must be in [1, 1024]");
+  if ((int64_t)T * k > (int64_t(1) << 30)) return fail(MQ_ERR_UNSUPPORTED, "too many slots");
+  if (capacity < moe_align_capacity(T, k, E, block_m))
+    return fail(MQ_ERR_INVALID_ARG, "capacity below moe_align_capacity()");
+  if ((T > 0 && !topk_ids) || !sorted_slot_ids || !block_expert || !expert_offsets || !num_padded)
+    return fail(MQ_ERR_INVALID_ARG, "null pointer");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned* status = status_ptr();
+  LaunchScope ls(MQ_PROF_ALIGN, st);
+  cudaError_t err = launch_align(topk_ids, T, k, E, block_m, sorted_slot_ids, block_expert,
+                                 expert_offsets, num_padded, status, st);
+  return err == cudaSuccess ? MQ_OK : cuda_fail(err, "align launch");
+}
+
+MQ_EXPORT size_t moe_quant_forward_workspace(int T, int H, int I, int E, int k, int bits,
+                                             int group_size) {
+  if (T < 0 || H <= 0 || I <= 0 || E < 1 || k < 1 || k > E) return 0;
+  if (!fmt_ok(bits, group_size, 0)) return 0;
+  return ws_layout(T, H, I, E, k, bits).total;
+}
+
+MQ_EXPORT int moe_quant_forward(const void* x, int T, int H, int I, int E, int k, int bits,
+                                int group_size, int has_zp, const void* w13, const void* w2,
+                                const void* s13, const void* s2, const uint8_t* z13,
+                                const uint8_t* z2, const float* topk_w, const int32_t* topk_ids,
+                                void* workspace, size_t ws_bytes, void* out, void* stream) {
+  if (T < 0 || H <= 0 || I <= 0 || E < 1) return fail(MQ_ERR_INVALID_ARG, "bad T, H, I or E");
+  if (k < 1 || k > E || k > 32) return fail(MQ_ERR_INVALID_ARG, "need 1 <= k <= min(E, 32)");
+  if (E > 1024) return fail(MQ_ERR_UNSUPPORTED, "E must be <= 1024");
+  if (!fmt_ok(bits, group_size, has_zp))
+    return fail(MQ_ERR_UNSUPPORTED, "format must be (8, -1, 0) or (4, 32..256, 0|1)");
+  if (H % 128 || I % 128) return fail(MQ_ERR_UNSUPPORTED, "H and I must be multiples of 128");
+  if (bits == 4 && (H % group_size || I % group_size))
+    return fail(MQ_ERR_UNSUPPORTED, "group_size must divide H and I");
+  if ((int64_t)T * k > (int64_t(1) << 24)) return fail(MQ_ERR_UNSUPPORTED, "too many token-slots");
+  if (T == 0) return MQ_OK;
+  if (!x || !w13 || !w2 || !s13 || !s2 || !topk_w || !topk_ids || !out || !workspace)
+    return fail(MQ_ERR_INVALID_ARG, "null pointer");
+  if (bits == 4 && has_zp && (!z13 || !z2)) return fail(MQ_ERR_INVALID_ARG, "null zero points");
+  if (bits == 4 && !has_zp && (z13 || z2))
+    return fail(MQ_ERR_INVALID_ARG, "zero points given with has_zp = 0");
+  if (!aligned16(x) || !aligned16(w13) || !aligned16(w2) || !aligned16(out) || !aligned16(workspace))
+    return fail(MQ_ERR_INVALID_ARG, "x, w13, w2, out and workspace must be 16-byte aligned");
+  {
+    const char* xb = static_cast<const char*>(x);
+    const char* ob = static_cast<const char*>(out);
+    const size_t nb = (size_t)T * H * 2;
+    if (ob < xb + nb && xb < ob + nb) return fail(MQ_ERR_INVALID_ARG, "out overlaps x");
+  }
+  const WsLayout L = ws_layout(T, H, I, E, k, bits);
+  const int bm = L.plan.bn;
+  if (ws_bytes < L.total)
+    return fail(MQ_ERR_WORKSPACE, "workspace %zu bytes, need %zu", ws_bytes, L.total);
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  MoeArgs a;
+  a.x = static_cast<const __nv_bfloat16*>(x);
+  a.T = T; a.H = H; a.I = I; a.E = E; a.k = k;
+  a.bits = bits; a.group_size = group_size; a.has_zp = has_zp;
+  a.w13 = w13; a.w2 = w2; a.s13 = s13; a.s2 = s2; a.z13 = z13; a.z2 = z2;
+  a.topk_w = topk_w; a.topk_ids = topk_ids;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.status = status_ptr();
+  a.sorted = reinterpret_cast<int32_t*>(ws + L.sorted);
+  a.block_expert = reinterpret_cast<int32_t*>(ws + L.block_expert);
+  a.offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
+  a.num_padded = reinterpret_cast<int32_t*>(ws + L.num_padded);
+  a.act = reinterpret_cast<__nv_bfloat16*>(ws + L.act);
+  a.y = reinterpret_cast<float*>(ws + L.y);
+  a.bm = bm;
+  a.cap = L.cap;
+
+  cudaError_t err;
+  {
+    LaunchScope ls(MQ_PROF_ALIGN, st);
+    err = launch_align(topk_ids, T, k, E, bm, a.sorted, a.block_expert, a.offsets, a.num_padded,
+                       a.status, st);
+  }
+  if (err != cudaSuccess) return cuda_fail(err, "forward: align launch");
+  if (L.tc) {
+    __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(ws + L.xs);
+    {
+      LaunchScope ls(MQ_PROF_GATHER, st);
+      err = launch_gather_rows(a, xs, st);
+    }
+    if (err != cudaSuccess) return cuda_fail(err, "forward: gather launch");
+    {
+      LaunchScope ls(MQ_PROF_GEMM1, st);
+      err = launch_gemm1_tc(a, L.plan, xs, st);
+    }
+    if (err != cudaSuccess) return cuda_fail(err, "forward: gate/up GEMM launch");
+    {
+      LaunchScope ls(MQ_PROF_GEMM2, st);
+      err = launch_gemm2_tc(a, L.plan, a.y, st);
+    }
+    if (err != cudaSuccess) return cuda_fail(err, "forward: down GEMM launch");
+    {
+      LaunchScope ls(MQ_PROF_COMBINE, st);
+      err = launch_combine_splits(a, a.y, L.plan.splits, st);
+    }
+  } else {
+    {
+      LaunchScope ls(MQ_PROF_GEMM1, st);
+      err = launch_gemm1_simple(a, st);
+    }
+    if (err != cudaSuccess) return cuda_fail(err, "forward: gate/up GEMM launch");
+    {
+      LaunchScope ls(MQ_PROF_GEMM2, st);
+      err = launch_gemm2_simple(a, st);
+    }
+    if (err != cudaSuccess) return cuda_fail(err, "forward: down GEMM launch");
+    {
+      LaunchScope ls(MQ_PROF_COMBINE, st);
+      err = launch_combine(a, st);
+    }
+  }
+  if (err != cudaSuccess) return cuda_fail(err, "forward: combine launch");
+  return MQ_OK;
+}

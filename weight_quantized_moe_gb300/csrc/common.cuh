@@ -1,0 +1,99 @@
+// Shared device helpers for the moeq kernels (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "../../include/moeq.h"
+
+#define MQ_HIDDEN __attribute__((visibility("hidden")))
+
+namespace mq {
+
+// Per-device status word: kernels OR MQ_DEV_* bits into it.  Each launcher
+// receives its device address from the API layer.
+__device__ __forceinline__ void flag(unsigned* status, unsigned bits) {
+  if (status) atomicOr(status, bits);
+}
+
+__device__ __forceinline__ unsigned lane_id() {
+  unsigned r;
+  asm volatile("mov.u32 %0, %%laneid;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+// silu(u) * v in float32; silu(u) = u / (1 + exp(-u)).
+__device__ __forceinline__ float silu_mul(float u, float v) {
+  return u / (1.0f + expf(-u)) * v;
+}
+
+}  // namespace mq
+
+// ---------------------------------------------------------------------------
+// Internal launchers (one translation unit each, not exported).
+// ---------------------------------------------------------------------------
+MQ_HIDDEN cudaError_t launch_quant_int8(const void* w, int64_t rows, int64_t cols, int8_t* q,
+                                        float* scale, cudaStream_t st);
+MQ_HIDDEN cudaError_t launch_quant_uint4(const void* w, int64_t rows, int64_t cols, int gs,
+                                         uint8_t* qw, uint16_t* sc, uint8_t* qz, cudaStream_t st);
+MQ_HIDDEN cudaError_t launch_route(const float* logits, int T, int E, int k, int renorm,
+                                   float* topk_w, int32_t* topk_ids, cudaStream_t st);
+MQ_HIDDEN cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int bm,
+                                   int32_t* sorted, int32_t* block_expert, int32_t* offsets,
+                                   int32_t* num_padded, unsigned* status, cudaStream_t st);
+
+struct MoeArgs {
+  const __nv_bfloat16* x;
+  int T, H, I, E, k;
+  int bits, group_size, has_zp;
+  const void* w13;
+  const void* w2;
+  const void* s13;
+  const void* s2;
+  const uint8_t* z13;
+  const uint8_t* z2;
+  const float* topk_w;
+  const int32_t* topk_ids;
+  __nv_bfloat16* out;
+  unsigned* status;
+  // workspace views
+  int32_t* sorted;        // [cap]
+  int32_t* block_expert;  // [cap / bm]
+  int32_t* offsets;       // [E + 1]
+  int32_t* num_padded;    // [1]
+  __nv_bfloat16* act;     // [cap, I]
+  float* y;               // [S, H]
+  int bm;
+  int64_t cap;
+};
+
+// Tensor-core path (tcgen05): tile plan and launchers.
+struct TcPlan {
+  int bn;      // token-slots per aligned block (MMA N)
+  int splits;  // K splits of the down GEMM
+};
+MQ_HIDDEN TcPlan tc_plan(int T, int H, int I, int E, int k);
+MQ_HIDDEN int tc_num_sms();
+MQ_HIDDEN cudaError_t launch_gather_rows(const MoeArgs& a, __nv_bfloat16* xs, cudaStream_t st);
+MQ_HIDDEN cudaError_t launch_gemm1_tc(const MoeArgs& a, const TcPlan& pl, const __nv_bfloat16* xs,
+                                      cudaStream_t st);
+MQ_HIDDEN cudaError_t launch_gemm2_tc(const MoeArgs& a, const TcPlan& pl, float* ypart,
+                                      cudaStream_t st);
+MQ_HIDDEN cudaError_t launch_combine_splits(const MoeArgs& a, const float* ypart, int splits,
+                                            cudaStream_t st);
+
+MQ_HIDDEN int simple_block_m();
+MQ_HIDDEN cudaError_t launch_gemm1_simple(const MoeArgs& a, cudaStream_t st);
+MQ_HIDDEN cudaError_t launch_gemm2_simple(const MoeArgs& a, cudaStream_t st);
+MQ_HIDDEN cudaError_t launch_combine(const MoeArgs& a, cudaStream_t st);

@@ -1,0 +1,630 @@
+// Tensor-core expert GEMMs for sm_103a (tcgen05 + TMA + TMEM).
+//
+// fused_experts' two grouped GEMMs (gate/up with SiLU-and-mul, then down
+// with the router-weighted scatter), restated for Blackwell:
+//
+//   D[128 weight rows x BN token-slots] = W[rows, K] . X[slots, K]^T
+//
+// * The weight tile is the MMA's A operand.  TMA stages the int8 codes in
+//   shared memory; a converter warpgroup turns them into bf16 (exact: every
+//   int8 value is a bf16) and writes them straight into tensor memory with
+//   tcgen05.st, so shared memory never holds bf16 weights.  The per-channel
+//   scale is applied once per output in the epilogue (sum_k x*(q*s) =
+//   s * sum_k x*q).
+// * The activations (token rows gathered per expert block) are the B
+//   operand: TMA tiles with the 128-byte swizzle, read by tcgen05.mma from
+//   shared memory.
+// * The accumulator lives in tensor memory (double-buffered for BN <= 128)
+//   and is drained by an epilogue warpgroup with tcgen05.ld.
+// * One persistent CTA per SM walks the work units (expert block, weight
+//   tile, K split); warp roles: 0 TMA producer, 1 MMA issuer, 2-5
+//   converters, 6-9 epilogue.
+// * Every mbarrier wait is bounded: after kWaitNs the CTA flags
+//   MQ_DEV_WAIT_TIMEOUT, stops issuing work, drains its own copies and MMAs
+//   (with a bound again), frees its tensor memory and exits.
+#include "common.cuh"
+#include "sm100_ptx.cuh"
+
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+namespace {
+
+using namespace mq::ptx;
+
+constexpr int kBK = 64;             // K elements per pipeline stage
+constexpr int kTileM = 128;         // weight rows per tile (MMA M)
+constexpr int kAStages = 4;         // tensor-memory stages of converted A
+constexpr int kAColsPerStage = kBK / 2;  // bf16 pairs per row
+constexpr int kThreads = 320;       // 10 warps
+constexpr int kABytes = kTileM * kBK;  // int8 A tile per stage
+constexpr unsigned long long kWaitNs = 1000000000ull;
+constexpr int kRasterGroup = 8;     // weight tiles per raster group
+
+struct TcParams {
+  int H, I, E, k, S;
+  int ksteps;        // K / kBK
+  int MT;            // weight tiles per expert
+  int splits;        // K splits
+  const int32_t* sorted;
+  const int32_t* block_expert;
+  const int32_t* offsets;
+  const int32_t* num_padded;
+  const float* scale;     // fp32 per-output-row scales of this GEMM's weights
+  const float* topk_w;
+  __nv_bfloat16* act;     // gate/up output [cap, I]
+  float* ypart;           // down output [splits, S, H]
+  unsigned* status;
+};
+
+struct Unit {
+  int e, b, mt, split;
+};
+
+template <int BN>
+__device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
+  const int V = p.MT * p.splits;
+  const int b0 = u / V;
+  const int e = p.block_expert[b0];
+  const int bs = p.offsets[e] / BN;
+  const int nbe = p.offsets[e + 1] / BN - bs;
+  const int ue = u - bs * V;
+  const int g = ue / (kRasterGroup * nbe);
+  const int r = ue - g * kRasterGroup * nbe;
+  const int gsz = min(kRasterGroup, V - g * kRasterGroup);
+  const int bl = r / gsz;
+  const int v = g * kRasterGroup + (r - bl * gsz);
+  Unit out;
+  out.e = e;
+  out.b = bs + bl;
+  out.mt = v % p.MT;
+  out.split = v / p.MT;
+  return out;
+}
+
+struct SharedCtl {
+  uint64_t full[16];
+  uint64_t empty[16];
+  uint64_t afull[kAStages];
+  uint64_t afree[kAStages];
+  uint64_t accfull[2];
+  uint64_t accempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  volatile int abort_flag;
+};
+
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, SharedCtl* ctl,
+                                             unsigned* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = mq::global_timer_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 63u) == 0) {
+      if (ctl->abort_flag) return false;
+      if (mq::global_timer_ns() - t0 > kWaitNs) {
+        ctl->abort_flag = 1;
+        mq::flag(status, MQ_DEV_WAIT_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// Warp-uniform bounded wait: lane 0 polls, every lane gets its verdict.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, SharedCtl* ctl,
+                                          unsigned* status, int lane) {
+  int ok = 0;
+  if (lane == 0) ok = wait_bounded(bar, parity, ctl, status) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// Wait used while draining after an abort: ignores the abort flag, still
+// bounded in time.
+__device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity) {
+  const unsigned long long t0 = mq::global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (mq::global_timer_ns() - t0 > kWaitNs) return;
+  }
+}
+
+// int8 x4 (one 32-bit word) -> two bf16x2 words, exact.
+// Each byte b is placed in the low byte of a bf16 whose high byte is 0x43:
+// for b < 128 that bf16 is 128 + b, for b >= 128 (negative x = b - 256) it
+// is 256 + 2 * (b - 128) = 512 + 2x.  One bf16x2 FMA with per-half
+// coefficients (1, -128) or (0.5, -256), chosen by the byte's top bit,
+// returns x exactly.
+__device__ __forceinline__ void int8x4_to_bf16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t v0 = __byte_perm(w, 0x43u, 0x4140);  // [b0, 0x43, b1, 0x43]
+  const uint32_t v1 = __byte_perm(w, 0x43u, 0x4342);  // [b2, 0x43, b3, 0x43]
+  const uint32_t t0 = v0 & 0x00800080u;
+  const uint32_t t1 = v1 & 0x00800080u;
+  const uint32_t a0 = t0 ^ 0x3F803F80u, c0 = t0 | 0xC300C300u;
+  const uint32_t a1 = t1 ^ 0x3F803F80u, c1 = t1 | 0xC300C300u;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(lo) : "r"(v0), "r"(a0), "r"(c0));
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(hi) : "r"(v1), "r"(a1), "r"(c1));
+}
+
+template <int MODE, int BN, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+    moe_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const TcParams p) {
+  constexpr int kAcc = BN <= 128 ? 2 : 1;
+  constexpr int kBBytes = BN * kBK * 2;
+  constexpr int kACol0 = kAcc * BN;
+  constexpr uint32_t kTmemCols = 512;
+  constexpr uint32_t kIdesc = idesc_bf16_f32(kTileM, BN);
+  static_assert(kACol0 + kAStages * kAColsPerStage <= (int)kTmemCols, "tensor memory budget");
+  static_assert(STAGES <= 16, "stage count");
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* sA = smem;                                 // STAGES x 8 KB (int8 codes)
+  uint8_t* sB = smem + STAGES * kABytes;              // STAGES x BN x 128 B (bf16)
+  SharedCtl* ctl = reinterpret_cast<SharedCtl*>(sB + STAGES * kBBytes);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&ctl->full[s], 1);
+      mbar_init(&ctl->empty[s], 4 + 1);
+    }
+    for (int s = 0; s < kAStages; ++s) {
+      mbar_init(&ctl->afull[s], 4);
+      mbar_init(&ctl->afree[s], 1);
+    }
+    for (int s = 0; s < kAcc; ++s) {
+      mbar_init(&ctl->accfull[s], 1);
+      mbar_init(&ctl->accempty[s], 4);
+    }
+    mbar_init(&ctl->drain, 1);
+    ctl->abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&ctl->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+
+  const int nb = *p.num_padded / BN;
+  const int total = nb * p.MT * p.splits;
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer ----
+    // The whole warp walks the schedule (so it stays converged); lane 0
+    // waits, issues the copies, and broadcasts the wait outcome.
+    if (lane == 0) {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+    }
+    int it = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+      const Unit w = decode_unit<BN>(p, u);
+      const int ks0 = w.split * p.ksteps / p.splits;
+      const int ks1 = (w.split + 1) * p.ksteps / p.splits;
+      for (int ks = ks0; ks < ks1; ++ks, ++it) {
+        const int s = it % STAGES;
+        const uint32_t ph = (it / STAGES) & 1;
+        ok = warp_wait(&ctl->empty[s], ph ^ 1, ctl, p.status, lane);
+        if (!ok) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&ctl->full[s], kABytes + kBBytes);
+          uint8_t* a = sA + s * kABytes;
+          if (MODE == 1) {
+            const int row = w.e * 2 * p.I + w.mt * 64;
+            tma_load_2d(a, &tmA, &ctl->full[s], ks * kBK, row);
+            tma_load_2d(a + 64 * kBK, &tmA, &ctl->full[s], ks * kBK, row + p.I);
+          } else {
+            tma_load_2d(a, &tmA, &ctl->full[s], ks * kBK, w.e * p.H + w.mt * kTileM);
+          }
+          tma_load_2d(sB + s * kBBytes, &tmB, &ctl->full[s], ks * kBK, w.b * BN);
+        }
+        __syncwarp();
+      }
+    }
+    // Never leave with copies in flight: the last load issued into each
+    // stage is iteration it-1, it-2, ...; wait for each of them.
+    if (lane == 0) {
+      const int n = it < STAGES ? it : STAGES;
+      for (int d = 1; d <= n; ++d) {
+        const int j = it - d;
+        wait_drain(&ctl->full[j % STAGES], (j / STAGES) & 1);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------- MMA issuer ----
+    int it = 0, t = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < total && ok; u += gridDim.x, ++t) {
+      const Unit w = decode_unit<BN>(p, u);
+      const int ks0 = w.split * p.ksteps / p.splits;
+      const int ks1 = (w.split + 1) * p.ksteps / p.splits;
+      const int acc = t % kAcc;
+      const uint32_t accph = (t / kAcc) & 1;
+      ok = warp_wait(&ctl->accempty[acc], accph ^ 1, ctl, p.status, lane);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem + acc * BN;
+      for (int ks = ks0; ks < ks1; ++ks, ++it) {
+        const int s = it % STAGES;
+        const uint32_t ph = (it / STAGES) & 1;
+        const int as = it % kAStages;
+        const uint32_t aph = (it / kAStages) & 1;
+        ok = warp_wait(&ctl->afull[as], aph, ctl, p.status, lane) &&
+             warp_wait(&ctl->full[s], ph, ctl, p.status, lane);
+        if (!ok) break;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t b_base = smem_addr(sB + s * kBBytes);
+          const uint32_t a_tmem = tmem + kACol0 + as * kAColsPerStage;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            mma_ts(d_tmem, a_tmem + kk * 8, smem_desc_k_sw128(b_base + kk * 32), kIdesc,
+                   (ks > ks0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&ctl->empty[s]);
+          mma_commit(&ctl->afree[as]);
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (lane == 0) mma_commit(&ctl->accfull[acc]);
+      __syncwarp();
+    }
+    // every MMA issued here must finish before tensor memory is freed
+    if (lane == 0) {
+      mma_commit(&ctl->drain);
+      wait_drain(&ctl->drain, 0);
+    }
+    __syncwarp();
+  } else if (warp < 6) {
+    // -------------------------------------------------- converters ----
+    const int q = warp & 3;  // tensor-memory lane quarter of this warp
+    const int r = q * 32 + lane;
+    int srow;
+    bool rot = false;
+    if (MODE == 1) {
+      // lanes (2i, 2i+1) hold gate row i and up row i of this tile
+      const int i = q * 16 + (lane >> 1);
+      srow = (lane & 1) ? 64 + i : i;
+      rot = (lane & 1) != 0;  // read order rotated by two chunks: distinct banks
+    } else {
+      srow = r;
+    }
+    const uint32_t sw = (srow >> 1) & 3;  // 64-byte swizzle phase of this row
+    int it = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+      const Unit w = decode_unit<BN>(p, u);
+      const int ks0 = w.split * p.ksteps / p.splits;
+      const int ks1 = (w.split + 1) * p.ksteps / p.splits;
+      for (int ks = ks0; ks < ks1; ++ks, ++it) {
+        const int s = it % STAGES;
+        const uint32_t ph = (it / STAGES) & 1;
+        const int as = it % kAStages;
+        const uint32_t aph = (it / kAStages) & 1;
+        ok = warp_wait(&ctl->full[s], ph, ctl, p.status, lane) &&
+             warp_wait(&ctl->afree[as], aph ^ 1, ctl, p.status, lane);
+        if (!ok) break;
+        tc_fence_after();
+        const uint8_t* row = sA + s * kABytes + srow * kBK;
+        uint4 raw[4];
+#pragma unroll
+        for (int i4 = 0; i4 < 4; ++i4) {
+          const uint32_t c = (uint32_t)(i4 + (rot ? 2 : 0)) & 3u;
+          raw[i4] = *reinterpret_cast<const uint4*>(row + ((c ^ sw) << 4));
+        }
+        uint32_t words[32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint4 v = rot ? raw[(c + 2) & 3] : raw[c];
+          int8x4_to_bf16x4(v.x, words[c * 8 + 0], words[c * 8 + 1]);
+          int8x4_to_bf16x4(v.y, words[c * 8 + 2], words[c * 8 + 3]);
+          int8x4_to_bf16x4(v.z, words[c * 8 + 4], words[c * 8 + 5]);
+          int8x4_to_bf16x4(v.w, words[c * 8 + 6], words[c * 8 + 7]);
+        }
+        tmem_st32(tmem + ((uint32_t)(q * 32) << 16) + kACol0 + as * kAColsPerStage, words);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&ctl->afull[as]);
+          mbar_arrive(&ctl->empty[s]);
+        }
+      }
+    }
+  } else {
+    // ---------------------------------------------------- epilogue ----
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    int t = 0;
+    for (int u = blockIdx.x; u < total; u += gridDim.x, ++t) {
+      const Unit w = decode_unit<BN>(p, u);
+      const int acc = t % kAcc;
+      const uint32_t accph = (t / kAcc) & 1;
+      if (!warp_wait(&ctl->accfull[acc], accph, ctl, p.status, lane)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + acc * BN;
+      constexpr int CH = BN < 32 ? BN : 32;  // accumulator columns per tcgen05.ld
+      if (MODE == 1) {
+        const int i = q * 16 + (lane >> 1);
+        const int wrow = w.e * 2 * p.I + ((lane & 1) ? p.I : 0) + w.mt * 64 + i;
+        const float sc = p.scale[wrow];
+        const int col = w.mt * 64 + i;
+        for (int c0 = 0; c0 < BN; c0 += CH) {
+          uint32_t v[CH];
+          tmem_ld_cols<CH>(taddr + c0, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int jj = 0; jj < CH; ++jj) {
+            const float own = __uint_as_float(v[jj]) * sc;
+            const float other = __shfl_xor_sync(0xffffffffu, own, 1);
+            const float g = (lane & 1) ? other : own;
+            const float up = (lane & 1) ? own : other;
+            // even lane stores the first half of the columns, odd lane the rest
+            if ((jj >= CH / 2) == ((lane & 1) != 0)) {
+              const int prow = w.b * BN + c0 + jj;
+              p.act[(int64_t)prow * p.I + col] = __float2bfloat16_rn(mq::silu_mul(g, up));
+            }
+          }
+        }
+      } else {
+        const int h = w.mt * kTileM + r;
+        const float sc = p.scale[w.e * p.H + h];
+        float* yp = p.ypart + (int64_t)w.split * p.S * p.H;
+        for (int c0 = 0; c0 < BN; c0 += CH) {
+          uint32_t v[CH];
+          tmem_ld_cols<CH>(taddr + c0, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int jj = 0; jj < CH; ++jj) {
+            const int slot = p.sorted[w.b * BN + c0 + jj];
+            if (slot < p.S) yp[(int64_t)slot * p.H + h] = __uint_as_float(v[jj]) * sc * p.topk_w[slot];
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->accempty[acc]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// Rows of x gathered into expert-sorted order (zeros for padding slots).
+__global__ void __launch_bounds__(256) gather_rows(const __nv_bfloat16* __restrict__ x,
+                                                   const int32_t* __restrict__ sorted,
+                                                   const int32_t* __restrict__ num_padded, int k,
+                                                   int S, int H, __nv_bfloat16* __restrict__ xs) {
+  const int p = blockIdx.x;
+  if (p >= *num_padded) return;
+  const int s = sorted[p];
+  uint4* dst = reinterpret_cast<uint4*>(xs + (int64_t)p * H);
+  const int n = H / 8;
+  if (s < S) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)(s / k) * H);
+    for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = src[i];
+  } else {
+    for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = make_uint4(0, 0, 0, 0);
+  }
+}
+
+// out[t, :] = sum over valid slots j and K splits of ypart[split, t*k + j, :].
+__global__ void __launch_bounds__(256) combine_splits(const float* __restrict__ ypart,
+                                                      const int32_t* __restrict__ ids, int T,
+                                                      int k, int E, int H, int splits,
+                                                      __nv_bfloat16* __restrict__ out) {
+  const int64_t i4 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int H4 = H / 4;
+  if (i4 >= (int64_t)T * H4) return;
+  const int t = (int)(i4 / H4);
+  const int c = (int)(i4 % H4) * 4;
+  const int64_t S = (int64_t)T * k;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j = 0; j < k; ++j) {
+    const int64_t s = (int64_t)t * k + j;
+    const int e = ids[s];
+    if (e < 0 || e >= E) continue;
+    for (int sp = 0; sp < splits; ++sp) {
+      const float4 v = *reinterpret_cast<const float4*>(ypart + (sp * S + s) * H + c);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+  }
+  __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+  __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+  uint2 o;
+  o.x = *reinterpret_cast<uint32_t*>(&lo);
+  o.y = *reinterpret_cast<uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(out + (int64_t)t * H + c) = o;
+}
+
+// ------------------------------------------------------------ host side --
+int g_num_sms = 0;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+cudaError_t get_encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode ? cudaSuccess : cudaErrorNotSupported;
+}
+
+cudaError_t make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, int esize, const void* base,
+                        uint64_t cols, uint64_t rows, uint32_t box_cols, uint32_t box_rows,
+                        CUtensorMapSwizzle sw) {
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * (uint64_t)esize};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int BN>
+constexpr int stages_for() {
+  return (200 * 1024) / (kABytes + BN * kBK * 2) > 8 ? 8 : (200 * 1024) / (kABytes + BN * kBK * 2);
+}
+
+// At least 120 KB so that only one CTA fits on an SM: each CTA allocates all
+// 512 tensor-memory columns.
+template <int BN>
+constexpr size_t smem_for() {
+  const size_t need = 1024 + (size_t)stages_for<BN>() * (kABytes + BN * kBK * 2) + sizeof(SharedCtl);
+  return need < 120 * 1024 ? 120 * 1024 : need;
+}
+
+
+template <int MODE, int BN>
+cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const TcParams& p,
+                        int max_units, cudaStream_t st) {
+  constexpr int STAGES = stages_for<BN>();
+  constexpr size_t smem = smem_for<BN>();
+  auto kern = moe_gemm_tc<MODE, BN, STAGES>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  const int sms = tc_num_sms();
+  const int grid = max_units < sms ? max_units : sms;
+  if (grid <= 0) return cudaSuccess;
+  kern<<<grid, kThreads, smem, st>>>(ta, tb, p);
+  return cudaGetLastError();
+}
+
+template <int MODE>
+cudaError_t launch_gemm_bn(int bn, const CUtensorMap& ta, const CUtensorMap& tb,
+                           const TcParams& p, int max_units, cudaStream_t st) {
+  switch (bn) {
+    case 16: return launch_gemm<MODE, 16>(ta, tb, p, max_units, st);
+    case 32: return launch_gemm<MODE, 32>(ta, tb, p, max_units, st);
+    case 64: return launch_gemm<MODE, 64>(ta, tb, p, max_units, st);
+    case 128: return launch_gemm<MODE, 128>(ta, tb, p, max_units, st);
+    case 256: return launch_gemm<MODE, 256>(ta, tb, p, max_units, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+TcPlan tc_plan(int T, int H, int I, int E, int k) {
+  TcPlan pl;
+  const int64_t S = (int64_t)T * k;
+  const int64_t per_expert = (S + E - 1) / E;
+  // token-slots per block: cover an average expert's load with some slack
+  int bn = 16;
+  while (bn < 128 && bn < per_expert + per_expert / 2) bn *= 2;
+  pl.bn = bn;
+  // K splits of the down GEMM: enough work units (about 600, four per SM)
+  // to keep every SM streaming weights; a fixed target keeps the workspace
+  // size independent of the device.
+  const int64_t blocks = (S < E ? S : E) > S / bn ? (S < E ? S : E) : S / bn;
+  const int mt2 = H / kTileM;
+  const int ksteps2 = I / kBK;
+  int splits = 1;
+  while (splits < 8 && blocks * mt2 * splits < 600 && ksteps2 / (splits * 2) >= 4) splits *= 2;
+  pl.splits = splits;
+  return pl;
+}
+
+int tc_num_sms() {
+  if (g_num_sms == 0) {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+      g_num_sms = n;
+  }
+  return g_num_sms > 0 ? g_num_sms : 148;
+}
+
+cudaError_t launch_gather_rows(const MoeArgs& a, __nv_bfloat16* xs, cudaStream_t st) {
+  if (a.cap == 0) return cudaSuccess;
+  gather_rows<<<(unsigned)a.cap, 128, 0, st>>>(a.x, a.sorted, a.num_padded, a.k, a.T * a.k, a.H, xs);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm1_tc(const MoeArgs& a, const TcPlan& pl, const __nv_bfloat16* xs,
+                            cudaStream_t st) {
+  cudaError_t err = get_encoder();
+  if (err != cudaSuccess) return err;
+  CUtensorMap ta, tb;
+  err = make_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.w13, (uint64_t)a.H,
+                    (uint64_t)a.E * 2 * a.I, kBK, 64, CU_TENSOR_MAP_SWIZZLE_64B);
+  if (err != cudaSuccess) return err;
+  err = make_map_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, xs, (uint64_t)a.H, (uint64_t)a.cap,
+                    kBK, pl.bn, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (err != cudaSuccess) return err;
+  TcParams p;
+  p.H = a.H; p.I = a.I; p.E = a.E; p.k = a.k; p.S = a.T * a.k;
+  p.ksteps = a.H / kBK;
+  p.MT = a.I / 64;
+  p.splits = 1;
+  p.sorted = a.sorted; p.block_expert = a.block_expert; p.offsets = a.offsets;
+  p.num_padded = a.num_padded;
+  p.scale = static_cast<const float*>(a.s13);
+  p.topk_w = a.topk_w;
+  p.act = a.act;
+  p.ypart = nullptr;
+  p.status = a.status;
+  const int64_t units = (a.cap / pl.bn) * (int64_t)p.MT;
+  return launch_gemm_bn<1>(pl.bn, ta, tb, p, (int)(units < (1 << 30) ? units : (1 << 30)), st);
+}
+
+cudaError_t launch_gemm2_tc(const MoeArgs& a, const TcPlan& pl, float* ypart, cudaStream_t st) {
+  cudaError_t err = get_encoder();
+  if (err != cudaSuccess) return err;
+  CUtensorMap ta, tb;
+  err = make_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.w2, (uint64_t)a.I,
+                    (uint64_t)a.E * a.H, kBK, kTileM, CU_TENSOR_MAP_SWIZZLE_64B);
+  if (err != cudaSuccess) return err;
+  err = make_map_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.act, (uint64_t)a.I,
+                    (uint64_t)a.cap, kBK, pl.bn, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (err != cudaSuccess) return err;
+  TcParams p;
+  p.H = a.H; p.I = a.I; p.E = a.E; p.k = a.k; p.S = a.T * a.k;
+  p.ksteps = a.I / kBK;
+  p.MT = a.H / kTileM;
+  p.splits = pl.splits;
+  p.sorted = a.sorted; p.block_expert = a.block_expert; p.offsets = a.offsets;
+  p.num_padded = a.num_padded;
+  p.scale = static_cast<const float*>(a.s2);
+  p.topk_w = a.topk_w;
+  p.act = nullptr;
+  p.ypart = ypart;
+  p.status = a.status;
+  const int64_t units = (a.cap / pl.bn) * (int64_t)p.MT * p.splits;
+  return launch_gemm_bn<2>(pl.bn, ta, tb, p, (int)(units < (1 << 30) ? units : (1 << 30)), st);
+}
+
+cudaError_t launch_combine_splits(const MoeArgs& a, const float* ypart, int splits,
+                                  cudaStream_t st) {
+  const int64_t n = (int64_t)a.T * (a.H / 4);
+  if (n == 0) return cudaSuccess;
+  combine_splits<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(ypart, a.topk_ids, a.T, a.k, a.E,
+                                                              a.H, splits, a.out);
+  return cudaGetLastError();
+}
