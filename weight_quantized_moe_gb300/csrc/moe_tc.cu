@@ -6,19 +6,23 @@
 //   D[128 weight rows x BN token-slots] = W[rows, K] . X[slots, K]^T
 //
 // * The weight tile is the MMA's A operand.  TMA stages the int8 codes in
-//   shared memory; a converter warpgroup turns them into bf16 (exact: every
-//   int8 value is a bf16) and writes them straight into tensor memory with
-//   tcgen05.st, so shared memory never holds bf16 weights.  The per-channel
-//   scale is applied once per output in the epilogue (sum_k x*(q*s) =
-//   s * sum_k x*q).
+//   shared memory, one 16 KB box (128 rows x 128 bytes) per K step; for the
+//   gate/up GEMM a 4-D tensor map fetches the 64 gate rows and the matching
+//   64 up rows in that one box.  Converter warpgroups turn the codes into
+//   bf16 (exact: every int8 value is a bf16) and write them straight into
+//   tensor memory with tcgen05.st, so shared memory never holds bf16
+//   weights.  The per-channel scale is applied once per output in the
+//   epilogue (sum_k x*(q*s) = s * sum_k x*q).
 // * The activations (token rows gathered per expert block) are the B
 //   operand: TMA tiles with the 128-byte swizzle, read by tcgen05.mma from
 //   shared memory.
-// * The accumulator lives in tensor memory (double-buffered for BN <= 128)
-//   and is drained by an epilogue warpgroup with tcgen05.ld.
+// * Accumulators live in tensor memory, double-buffered across work units.
+//   For small BN the K steps are spread round-robin over NKACC independent
+//   accumulators (summed in the epilogue) so that consecutive MMAs do not
+//   wait on each other's results.
 // * One persistent CTA per SM walks the work units (expert block, weight
-//   tile, K split); warp roles: 0 TMA producer, 1 MMA issuer, 2-5
-//   converters, 6-9 epilogue.
+//   tile, K split).  Warp roles: 0 TMA producer, 1 MMA issuer, 2-9 two
+//   converter warpgroups taking alternate K steps, 10-13 epilogue.
 // * Every mbarrier wait is bounded: after kWaitNs the CTA flags
 //   MQ_DEV_WAIT_TIMEOUT, stops issuing work, drains its own copies and MMAs
 //   (with a bound again), frees its tensor memory and exits.
@@ -33,14 +37,30 @@ namespace {
 
 using namespace mq::ptx;
 
-constexpr int kBK = 64;             // K elements per pipeline stage
-constexpr int kTileM = 128;         // weight rows per tile (MMA M)
-constexpr int kAStages = 4;         // tensor-memory stages of converted A
-constexpr int kAColsPerStage = kBK / 2;  // bf16 pairs per row
-constexpr int kThreads = 320;       // 10 warps
-constexpr int kABytes = kTileM * kBK;  // int8 A tile per stage
+constexpr int kBK = 128;                  // K elements per pipeline stage
+constexpr int kTileM = 128;               // weight rows per tile (MMA M)
+constexpr int kAStages = 4;               // tensor-memory stages of converted A
+constexpr int kAColsPerStage = kBK / 2;   // bf16 pairs per row = TMEM columns
+constexpr int kABytes = kTileM * kBK;     // int8 A tile per stage (16 KB)
+constexpr int kConvGroups = 2;            // converter warpgroups (alternate K steps)
+constexpr int kEpiWarp0 = 2 + 4 * kConvGroups;  // first epilogue warp
+constexpr int kThreads = (kEpiWarp0 + 4) * 32;
 constexpr unsigned long long kWaitNs = 1000000000ull;
-constexpr int kRasterGroup = 8;     // weight tiles per raster group
+constexpr int kRasterGroup = 8;           // weight tiles per raster group
+constexpr uint32_t kTmemCols = 512;
+
+// Independent K accumulators and buffering per token-tile width.
+template <int BN>
+struct TileCfg {
+  static constexpr int kKAcc = BN <= 32 ? 4 : (BN <= 64 ? 2 : 1);
+  static constexpr int kBufs = 2;
+  static constexpr int kACol0 = kBufs * kKAcc * BN;
+  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kStages =
+      (200 * 1024) / (kABytes + kBBytes) > 8 ? 8 : (200 * 1024) / (kABytes + kBBytes);
+  static_assert(kACol0 + kAStages * kAColsPerStage <= (int)kTmemCols, "tensor memory budget");
+  static_assert(kStages >= 2, "pipeline depth");
+};
 
 struct TcParams {
   int H, I, E, k, S;
@@ -62,6 +82,10 @@ struct Unit {
   int e, b, mt, split;
 };
 
+// Work unit u -> (expert, block, weight tile, K split).  Units of one expert
+// are contiguous; inside an expert, groups of kRasterGroup weight tiles sweep
+// all of its token blocks, so a weight tile is reused from L2 by the blocks
+// that run at the same time.
 template <int BN>
 __device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
   const int V = p.MT * p.splits;
@@ -120,6 +144,31 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, Shared
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
+// Same, for long waits off the critical path (the epilogue waiting for a
+// whole tile): a short sleep between polls leaves the issue slots to the
+// converter warps.
+__device__ __forceinline__ bool warp_wait_sleepy(uint64_t* bar, uint32_t parity, SharedCtl* ctl,
+                                                 unsigned* status, int lane) {
+  int ok = 0;
+  if (lane == 0) {
+    const unsigned long long t0 = mq::global_timer_ns();
+    for (;;) {
+      if (mbar_try_wait(bar, parity)) {
+        ok = 1;
+        break;
+      }
+      if (ctl->abort_flag) break;
+      if (mq::global_timer_ns() - t0 > kWaitNs) {
+        ctl->abort_flag = 1;
+        mq::flag(status, MQ_DEV_WAIT_TIMEOUT);
+        break;
+      }
+      __nanosleep(256);
+    }
+  }
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
 // Wait used while draining after an abort: ignores the abort flag, still
 // bounded in time.
 __device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity) {
@@ -146,23 +195,39 @@ __device__ __forceinline__ void int8x4_to_bf16x4(uint32_t w, uint32_t& lo, uint3
   asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(hi) : "r"(v1), "r"(a1), "r"(c1));
 }
 
-template <int MODE, int BN, int STAGES>
+__device__ __forceinline__ void convert16(const uint4& v, uint32_t* w) {
+  int8x4_to_bf16x4(v.x, w[0], w[1]);
+  int8x4_to_bf16x4(v.y, w[2], w[3]);
+  int8x4_to_bf16x4(v.z, w[4], w[5]);
+  int8x4_to_bf16x4(v.w, w[6], w[7]);
+}
+
+// 16-byte chunk c of a 128-byte swizzled shared-memory row.
+__device__ __forceinline__ uint4 ld_chunk(const uint8_t* row, uint32_t c, uint32_t sw) {
+  return *reinterpret_cast<const uint4*>(row + ((c ^ sw) << 4));
+}
+
+__device__ __forceinline__ uint4 sel4(bool p, const uint4& a, const uint4& b) {
+  return make_uint4(p ? a.x : b.x, p ? a.y : b.y, p ? a.z : b.z, p ? a.w : b.w);
+}
+
+template <int MODE, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const TcParams p) {
-  constexpr int kAcc = BN <= 128 ? 2 : 1;
-  constexpr int kBBytes = BN * kBK * 2;
-  constexpr int kACol0 = kAcc * BN;
-  constexpr uint32_t kTmemCols = 512;
+  using C = TileCfg<BN>;
+  constexpr int STAGES = C::kStages;
+  constexpr int NKACC = C::kKAcc;
+  constexpr int kBBytes = C::kBBytes;
+  constexpr int kACol0 = C::kACol0;
   constexpr uint32_t kIdesc = idesc_bf16_f32(kTileM, BN);
-  static_assert(kACol0 + kAStages * kAColsPerStage <= (int)kTmemCols, "tensor memory budget");
   static_assert(STAGES <= 16, "stage count");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* sA = smem;                                 // STAGES x 8 KB (int8 codes)
-  uint8_t* sB = smem + STAGES * kABytes;              // STAGES x BN x 128 B (bf16)
+  uint8_t* sA = smem;                     // STAGES x 16 KB (int8 codes, 128-byte swizzle)
+  uint8_t* sB = smem + STAGES * kABytes;  // STAGES x 2 x BN x 128 B (bf16, 128-byte swizzle)
   SharedCtl* ctl = reinterpret_cast<SharedCtl*>(sB + STAGES * kBBytes);
 
   const int warp = threadIdx.x >> 5;
@@ -171,13 +236,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&ctl->full[s], 1);
-      mbar_init(&ctl->empty[s], 4 + 1);
+      mbar_init(&ctl->empty[s], 4 + 1);  // 4 converter warps + 1 MMA commit
     }
     for (int s = 0; s < kAStages; ++s) {
       mbar_init(&ctl->afull[s], 4);
       mbar_init(&ctl->afree[s], 1);
     }
-    for (int s = 0; s < kAcc; ++s) {
+    for (int s = 0; s < 2; ++s) {
       mbar_init(&ctl->accfull[s], 1);
       mbar_init(&ctl->accempty[s], 4);
     }
@@ -220,19 +285,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(&ctl->full[s], kABytes + kBBytes);
           uint8_t* a = sA + s * kABytes;
           if (MODE == 1) {
-            const int row = w.e * 2 * p.I + w.mt * 64;
-            tma_load_2d(a, &tmA, &ctl->full[s], ks * kBK, row);
-            tma_load_2d(a + 64 * kBK, &tmA, &ctl->full[s], ks * kBK, row + p.I);
+            // {K, row in half, gate/up half, expert}: 64 gate rows then 64 up rows
+            tma_load_4d(a, &tmA, &ctl->full[s], ks * kBK, w.mt * 64, 0, w.e);
           } else {
             tma_load_2d(a, &tmA, &ctl->full[s], ks * kBK, w.e * p.H + w.mt * kTileM);
           }
-          tma_load_2d(sB + s * kBBytes, &tmB, &ctl->full[s], ks * kBK, w.b * BN);
+          uint8_t* b = sB + s * kBBytes;
+          tma_load_2d(b, &tmB, &ctl->full[s], ks * kBK, w.b * BN);
+          tma_load_2d(b + kBBytes / 2, &tmB, &ctl->full[s], ks * kBK + 64, w.b * BN);
         }
         __syncwarp();
       }
     }
-    // Never leave with copies in flight: the last load issued into each
-    // stage is iteration it-1, it-2, ...; wait for each of them.
+    // Never leave with copies in flight: wait for the last load issued into
+    // each stage (iterations it-1, it-2, ...).
     if (lane == 0) {
       const int n = it < STAGES ? it : STAGES;
       for (int d = 1; d <= n; ++d) {
@@ -249,12 +315,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Unit w = decode_unit<BN>(p, u);
       const int ks0 = w.split * p.ksteps / p.splits;
       const int ks1 = (w.split + 1) * p.ksteps / p.splits;
-      const int acc = t % kAcc;
-      const uint32_t accph = (t / kAcc) & 1;
-      ok = warp_wait(&ctl->accempty[acc], accph ^ 1, ctl, p.status, lane);
+      const int buf = t & 1;
+      const uint32_t bph = (t >> 1) & 1;
+      ok = warp_wait(&ctl->accempty[buf], bph ^ 1, ctl, p.status, lane);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t d_tmem = tmem + acc * BN;
+      const uint32_t d_tmem = tmem + buf * NKACC * BN;
       for (int ks = ks0; ks < ks1; ++ks, ++it) {
         const int s = it % STAGES;
         const uint32_t ph = (it / STAGES) & 1;
@@ -269,8 +335,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t a_tmem = tmem + kACol0 + as * kAColsPerStage;
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
-            mma_ts(d_tmem, a_tmem + kk * 8, smem_desc_k_sw128(b_base + kk * 32), kIdesc,
-                   (ks > ks0 || kk > 0) ? 1u : 0u);
+            // K slices 0-3 in the first 64-column box, 4-7 in the second
+            const uint32_t b_addr = b_base + (kk >> 2) * (kBBytes / 2) + (kk & 3) * 32;
+            const int acc = kk % NKACC;
+            mma_ts(d_tmem + acc * BN, a_tmem + kk * 8, smem_desc_k_sw128(b_addr), kIdesc,
+                   (ks > ks0 || kk >= NKACC) ? 1u : 0u);
           }
           mma_commit(&ctl->empty[s]);
           mma_commit(&ctl->afree[as]);
@@ -278,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
       }
       if (!ok) break;
-      if (lane == 0) mma_commit(&ctl->accfull[acc]);
+      if (lane == 0) mma_commit(&ctl->accfull[buf]);
       __syncwarp();
     }
     // every MMA issued here must finish before tensor memory is freed
@@ -287,21 +356,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       wait_drain(&ctl->drain, 0);
     }
     __syncwarp();
-  } else if (warp < 6) {
+  } else if (warp < kEpiWarp0) {
     // -------------------------------------------------- converters ----
-    const int q = warp & 3;  // tensor-memory lane quarter of this warp
+    const int grp = (warp - 2) >> 2;  // takes the K steps with it % kConvGroups == grp
+    const int q = warp & 3;           // tensor-memory lane quarter of this warp
     const int r = q * 32 + lane;
     int srow;
-    bool rot = false;
+    int rot = 0;
     if (MODE == 1) {
       // lanes (2i, 2i+1) hold gate row i and up row i of this tile
       const int i = q * 16 + (lane >> 1);
       srow = (lane & 1) ? 64 + i : i;
-      rot = (lane & 1) != 0;  // read order rotated by two chunks: distinct banks
+      rot = (lane & 1) ? 2 : 0;  // rotated read order keeps the pair on distinct banks
     } else {
       srow = r;
     }
-    const uint32_t sw = (srow >> 1) & 3;  // 64-byte swizzle phase of this row
+    const uint32_t sw = srow & 7;  // 128-byte swizzle phase of this row
+    const uint32_t tcol = ((uint32_t)(q * 32) << 16) + kACol0;
     int it = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
@@ -309,6 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ks0 = w.split * p.ksteps / p.splits;
       const int ks1 = (w.split + 1) * p.ksteps / p.splits;
       for (int ks = ks0; ks < ks1; ++ks, ++it) {
+        if (it % kConvGroups != grp) continue;
         const int s = it % STAGES;
         const uint32_t ph = (it / STAGES) & 1;
         const int as = it % kAStages;
@@ -318,22 +390,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc_fence_after();
         const uint8_t* row = sA + s * kABytes + srow * kBK;
-        uint4 raw[4];
 #pragma unroll
-        for (int i4 = 0; i4 < 4; ++i4) {
-          const uint32_t c = (uint32_t)(i4 + (rot ? 2 : 0)) & 3u;
-          raw[i4] = *reinterpret_cast<const uint4*>(row + ((c ^ sw) << 4));
+        for (int h = 0; h < 2; ++h) {
+          // x_j holds logical chunk 4h + ((j + rot) & 3)
+          const uint4 x0 = ld_chunk(row, 4 * h + ((0 + rot) & 3), sw);
+          const uint4 x1 = ld_chunk(row, 4 * h + ((1 + rot) & 3), sw);
+          const uint4 x2 = ld_chunk(row, 4 * h + ((2 + rot) & 3), sw);
+          const uint4 x3 = ld_chunk(row, 4 * h + ((3 + rot) & 3), sw);
+          const bool rt = rot != 0;
+          uint32_t words[32];
+          convert16(sel4(rt, x2, x0), &words[0]);
+          convert16(sel4(rt, x3, x1), &words[8]);
+          convert16(sel4(rt, x0, x2), &words[16]);
+          convert16(sel4(rt, x1, x3), &words[24]);
+          tmem_st32(tmem + tcol + as * kAColsPerStage + h * 32, words);
         }
-        uint32_t words[32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint4 v = rot ? raw[(c + 2) & 3] : raw[c];
-          int8x4_to_bf16x4(v.x, words[c * 8 + 0], words[c * 8 + 1]);
-          int8x4_to_bf16x4(v.y, words[c * 8 + 2], words[c * 8 + 3]);
-          int8x4_to_bf16x4(v.z, words[c * 8 + 4], words[c * 8 + 5]);
-          int8x4_to_bf16x4(v.w, words[c * 8 + 6], words[c * 8 + 7]);
-        }
-        tmem_st32(tmem + ((uint32_t)(q * 32) << 16) + kACol0 + as * kAColsPerStage, words);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -347,27 +418,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------- epilogue ----
     const int q = warp & 3;
     const int r = q * 32 + lane;
+    // accumulator columns per tcgen05.ld (16 when several K accumulators are summed)
+    constexpr int CH = (BN < 32 || NKACC > 1) ? 16 : 32;
     int t = 0;
     for (int u = blockIdx.x; u < total; u += gridDim.x, ++t) {
       const Unit w = decode_unit<BN>(p, u);
-      const int acc = t % kAcc;
-      const uint32_t accph = (t / kAcc) & 1;
-      if (!warp_wait(&ctl->accfull[acc], accph, ctl, p.status, lane)) break;
+      const int buf = t & 1;
+      const uint32_t bph = (t >> 1) & 1;
+      if (!warp_wait_sleepy(&ctl->accfull[buf], bph, ctl, p.status, lane)) break;
       tc_fence_after();
-      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + acc * BN;
-      constexpr int CH = BN < 32 ? BN : 32;  // accumulator columns per tcgen05.ld
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + buf * NKACC * BN;
       if (MODE == 1) {
         const int i = q * 16 + (lane >> 1);
         const int wrow = w.e * 2 * p.I + ((lane & 1) ? p.I : 0) + w.mt * 64 + i;
         const float sc = p.scale[wrow];
         const int col = w.mt * 64 + i;
         for (int c0 = 0; c0 < BN; c0 += CH) {
-          uint32_t v[CH];
-          tmem_ld_cols<CH>(taddr + c0, v);
-          tmem_ld_wait();
+          float acc[CH];
+          {
+            uint32_t v[CH];
+            tmem_ld_cols<CH>(taddr + c0, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int jj = 0; jj < CH; ++jj) acc[jj] = __uint_as_float(v[jj]);
+          }
+#pragma unroll
+          for (int a = 1; a < NKACC; ++a) {
+            uint32_t v[CH];
+            tmem_ld_cols<CH>(taddr + a * BN + c0, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int jj = 0; jj < CH; ++jj) acc[jj] += __uint_as_float(v[jj]);
+          }
 #pragma unroll
           for (int jj = 0; jj < CH; ++jj) {
-            const float own = __uint_as_float(v[jj]) * sc;
+            const float own = acc[jj] * sc;
             const float other = __shfl_xor_sync(0xffffffffu, own, 1);
             const float g = (lane & 1) ? other : own;
             const float up = (lane & 1) ? own : other;
@@ -383,19 +468,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float sc = p.scale[w.e * p.H + h];
         float* yp = p.ypart + (int64_t)w.split * p.S * p.H;
         for (int c0 = 0; c0 < BN; c0 += CH) {
-          uint32_t v[CH];
-          tmem_ld_cols<CH>(taddr + c0, v);
-          tmem_ld_wait();
+          float acc[CH];
+          {
+            uint32_t v[CH];
+            tmem_ld_cols<CH>(taddr + c0, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int jj = 0; jj < CH; ++jj) acc[jj] = __uint_as_float(v[jj]);
+          }
+#pragma unroll
+          for (int a = 1; a < NKACC; ++a) {
+            uint32_t v[CH];
+            tmem_ld_cols<CH>(taddr + a * BN + c0, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int jj = 0; jj < CH; ++jj) acc[jj] += __uint_as_float(v[jj]);
+          }
 #pragma unroll
           for (int jj = 0; jj < CH; ++jj) {
             const int slot = p.sorted[w.b * BN + c0 + jj];
-            if (slot < p.S) yp[(int64_t)slot * p.H + h] = __uint_as_float(v[jj]) * sc * p.topk_w[slot];
+            if (slot < p.S) yp[(int64_t)slot * p.H + h] = acc[jj] * sc * p.topk_w[slot];
           }
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl->accempty[acc]);
+      if (lane == 0) mbar_arrive(&ctl->accempty[buf]);
     }
   }
 
@@ -408,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Rows of x gathered into expert-sorted order (zeros for padding slots).
-__global__ void __launch_bounds__(256) gather_rows(const __nv_bfloat16* __restrict__ x,
+__global__ void __launch_bounds__(128) gather_rows(const __nv_bfloat16* __restrict__ x,
                                                    const int32_t* __restrict__ sorted,
                                                    const int32_t* __restrict__ num_padded, int k,
                                                    int S, int H, __nv_bfloat16* __restrict__ xs) {
@@ -474,39 +572,32 @@ cudaError_t get_encoder() {
   return g_encode ? cudaSuccess : cudaErrorNotSupported;
 }
 
-cudaError_t make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, int esize, const void* base,
-                        uint64_t cols, uint64_t rows, uint32_t box_cols, uint32_t box_rows,
-                        CUtensorMapSwizzle sw) {
-  const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols * (uint64_t)esize};
-  const cuuint32_t box[2] = {box_cols, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  CUresult r = g_encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+// Tensor map of `rank` dims; dims[0] is innermost, strides are in bytes for
+// dims 1..rank-1.
+cudaError_t make_map(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* base,
+                     const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+                     CUtensorMapSwizzle sw) {
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(map, dt, rank, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
-template <int BN>
-constexpr int stages_for() {
-  return (200 * 1024) / (kABytes + BN * kBK * 2) > 8 ? 8 : (200 * 1024) / (kABytes + BN * kBK * 2);
 }
 
 // At least 120 KB so that only one CTA fits on an SM: each CTA allocates all
 // 512 tensor-memory columns.
 template <int BN>
 constexpr size_t smem_for() {
-  const size_t need = 1024 + (size_t)stages_for<BN>() * (kABytes + BN * kBK * 2) + sizeof(SharedCtl);
+  using C = TileCfg<BN>;
+  const size_t need = 1024 + (size_t)C::kStages * (kABytes + C::kBBytes) + sizeof(SharedCtl);
   return need < 120 * 1024 ? 120 * 1024 : need;
 }
-
 
 template <int MODE, int BN>
 cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const TcParams& p,
                         int max_units, cudaStream_t st) {
-  constexpr int STAGES = stages_for<BN>();
   constexpr size_t smem = smem_for<BN>();
-  auto kern = moe_gemm_tc<MODE, BN, STAGES>;
+  auto kern = moe_gemm_tc<MODE, BN>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   const int sms = tc_num_sms();
@@ -524,7 +615,6 @@ cudaError_t launch_gemm_bn(int bn, const CUtensorMap& ta, const CUtensorMap& tb,
     case 32: return launch_gemm<MODE, 32>(ta, tb, p, max_units, st);
     case 64: return launch_gemm<MODE, 64>(ta, tb, p, max_units, st);
     case 128: return launch_gemm<MODE, 128>(ta, tb, p, max_units, st);
-    case 256: return launch_gemm<MODE, 256>(ta, tb, p, max_units, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -542,11 +632,12 @@ TcPlan tc_plan(int T, int H, int I, int E, int k) {
   // K splits of the down GEMM: enough work units (about 600, four per SM)
   // to keep every SM streaming weights; a fixed target keeps the workspace
   // size independent of the device.
-  const int64_t blocks = (S < E ? S : E) > S / bn ? (S < E ? S : E) : S / bn;
+  const int64_t live = S < E ? S : E;
+  const int64_t blocks = live > S / bn ? live : S / bn;
   const int mt2 = H / kTileM;
   const int ksteps2 = I / kBK;
   int splits = 1;
-  while (splits < 8 && blocks * mt2 * splits < 600 && ksteps2 / (splits * 2) >= 4) splits *= 2;
+  while (splits < 8 && blocks * mt2 * splits < 600 && ksteps2 / (splits * 2) >= 2) splits *= 2;
   pl.splits = splits;
   return pl;
 }
@@ -572,12 +663,23 @@ cudaError_t launch_gemm1_tc(const MoeArgs& a, const TcPlan& pl, const __nv_bfloa
   cudaError_t err = get_encoder();
   if (err != cudaSuccess) return err;
   CUtensorMap ta, tb;
-  err = make_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.w13, (uint64_t)a.H,
-                    (uint64_t)a.E * 2 * a.I, kBK, 64, CU_TENSOR_MAP_SWIZZLE_64B);
-  if (err != cudaSuccess) return err;
-  err = make_map_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, xs, (uint64_t)a.H, (uint64_t)a.cap,
-                    kBK, pl.bn, CU_TENSOR_MAP_SWIZZLE_128B);
-  if (err != cudaSuccess) return err;
+  {
+    // w13 int8 [E, 2, I, H] viewed as {H, I, 2, E}: one box = 64 gate rows + 64 up rows
+    const cuuint64_t dims[4] = {(cuuint64_t)a.H, (cuuint64_t)a.I, 2, (cuuint64_t)a.E};
+    const cuuint64_t strides[3] = {(cuuint64_t)a.H, (cuuint64_t)a.I * a.H, (cuuint64_t)2 * a.I * a.H};
+    const cuuint32_t box[4] = {kBK, 64, 2, 1};
+    err = make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, a.w13, dims, strides, box,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
+    if (err != cudaSuccess) return err;
+  }
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)a.H, (cuuint64_t)a.cap};
+    const cuuint64_t strides[1] = {(cuuint64_t)a.H * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)pl.bn};
+    err = make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, xs, dims, strides, box,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
+    if (err != cudaSuccess) return err;
+  }
   TcParams p;
   p.H = a.H; p.I = a.I; p.E = a.E; p.k = a.k; p.S = a.T * a.k;
   p.ksteps = a.H / kBK;
@@ -598,12 +700,22 @@ cudaError_t launch_gemm2_tc(const MoeArgs& a, const TcPlan& pl, float* ypart, cu
   cudaError_t err = get_encoder();
   if (err != cudaSuccess) return err;
   CUtensorMap ta, tb;
-  err = make_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.w2, (uint64_t)a.I,
-                    (uint64_t)a.E * a.H, kBK, kTileM, CU_TENSOR_MAP_SWIZZLE_64B);
-  if (err != cudaSuccess) return err;
-  err = make_map_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.act, (uint64_t)a.I,
-                    (uint64_t)a.cap, kBK, pl.bn, CU_TENSOR_MAP_SWIZZLE_128B);
-  if (err != cudaSuccess) return err;
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)a.I, (cuuint64_t)a.E * a.H};
+    const cuuint64_t strides[1] = {(cuuint64_t)a.I};
+    const cuuint32_t box[2] = {kBK, kTileM};
+    err = make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.w2, dims, strides, box,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
+    if (err != cudaSuccess) return err;
+  }
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)a.I, (cuuint64_t)a.cap};
+    const cuuint64_t strides[1] = {(cuuint64_t)a.I * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)pl.bn};
+    err = make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.act, dims, strides, box,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
+    if (err != cudaSuccess) return err;
+  }
   TcParams p;
   p.H = a.H; p.I = a.I; p.E = a.E; p.k = a.k; p.S = a.T * a.k;
   p.ksteps = a.I / kBK;
