@@ -102,7 +102,7 @@ inline size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
 // Workspace layout of moe_quant_forward.  W8A16 runs the tensor-core path
 // (gathered activations, split-K partial outputs); W4A16 the CUDA-core path.
 struct WsLayout {
-  size_t sorted, block_expert, offsets, num_padded, xs, act, y, total;
+  size_t sorted, block_expert, offsets, num_padded, xs, xinv, act, y, total;
   int64_t cap;
   TcPlan plan;
   bool tc;
@@ -121,7 +121,8 @@ WsLayout ws_layout(int T, int H, int I, int E, int k, int bits) {
   L.block_expert = off; off += align256(sizeof(int32_t) * (size_t)(cap / bm));
   L.offsets = off;      off += align256(sizeof(int32_t) * (size_t)(E + 1));
   L.num_padded = off;   off += align256(sizeof(int32_t));
-  L.xs = off;           off += L.tc ? align256(sizeof(__nv_bfloat16) * (size_t)cap * (size_t)H) : 0;
+  L.xs = off;           off += L.tc ? align256(sizeof(__half) * (size_t)cap * (size_t)H) : 0;
+  L.xinv = off;         off += L.tc ? align256(sizeof(float) * (size_t)cap) : 0;
   L.act = off;          off += align256(sizeof(__nv_bfloat16) * (size_t)cap * (size_t)I);
   L.y = off;            off += align256(sizeof(float) * (size_t)L.plan.splits * (size_t)S * (size_t)H);
   L.total = off;
@@ -345,15 +346,16 @@ MQ_EXPORT int moe_quant_forward(const void* x, int T, int H, int I, int E, int k
   }
   if (err != cudaSuccess) return cuda_fail(err, "forward: align launch");
   if (L.tc) {
-    __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(ws + L.xs);
+    void* xs = ws + L.xs;
+    float* xinv = reinterpret_cast<float*>(ws + L.xinv);
     {
       LaunchScope ls(MQ_PROF_GATHER, st);
-      err = launch_gather_rows(a, xs, st);
+      err = launch_gather_rows(a, xs, xinv, st);
     }
     if (err != cudaSuccess) return cuda_fail(err, "forward: gather launch");
     {
       LaunchScope ls(MQ_PROF_GEMM1, st);
-      err = launch_gemm1_tc(a, L.plan, xs, st);
+      err = launch_gemm1_tc(a, L.plan, xs, xinv, st);
     }
     if (err != cudaSuccess) return cuda_fail(err, "forward: gate/up GEMM launch");
     {

@@ -85,9 +85,9 @@ struct TcPlan {
 };
 MQ_HIDDEN TcPlan tc_plan(int T, int H, int I, int E, int k);
 MQ_HIDDEN int tc_num_sms();
-MQ_HIDDEN cudaError_t launch_gather_rows(const MoeArgs& a, __nv_bfloat16* xs, cudaStream_t st);
-MQ_HIDDEN cudaError_t launch_gemm1_tc(const MoeArgs& a, const TcPlan& pl, const __nv_bfloat16* xs,
-                                      cudaStream_t st);
+MQ_HIDDEN cudaError_t launch_gather_rows(const MoeArgs& a, void* xs, float* xinv, cudaStream_t st);
+MQ_HIDDEN cudaError_t launch_gemm1_tc(const MoeArgs& a, const TcPlan& pl, const void* xs,
+                                      const float* xinv, cudaStream_t st);
 MQ_HIDDEN cudaError_t launch_gemm2_tc(const MoeArgs& a, const TcPlan& pl, float* ypart,
                                       cudaStream_t st);
 MQ_HIDDEN cudaError_t launch_combine_splits(const MoeArgs& a, const float* ypart, int splits,

@@ -37,29 +37,46 @@ namespace {
 
 using namespace mq::ptx;
 
-constexpr int kBK = 128;                  // K elements per pipeline stage
+constexpr int kBK = 128;                  // K elements per weight stage (one 16 KB TMA box)
+constexpr int kG = 2;                     // weight stages per MMA step
 constexpr int kTileM = 128;               // weight rows per tile (MMA M)
-constexpr int kAStages = 4;               // tensor-memory stages of converted A
-constexpr int kAColsPerStage = kBK / 2;   // bf16 pairs per row = TMEM columns
-constexpr int kABytes = kTileM * kBK;     // int8 A tile per stage (16 KB)
-constexpr int kConvGroups = 2;            // converter warpgroups (alternate K steps)
-constexpr int kEpiWarp0 = 2 + 4 * kConvGroups;  // first epilogue warp
+constexpr int kAColsPerK = kBK / 2;       // TMEM columns per weight stage (16-bit pairs)
+constexpr int kAColsPerStep = kG * kAColsPerK;
+constexpr int kABytes = kTileM * kBK;     // int8 A tile per weight stage (16 KB)
+constexpr int kConvGroups = 2;            // converter warpgroups (alternate MMA steps)
+constexpr int kConvWarp0 = 3;             // warps 0: A producer, 1: MMA, 2: B producer
+constexpr int kEpiWarp0 = kConvWarp0 + 4 * kConvGroups;  // first epilogue warp
 constexpr int kThreads = (kEpiWarp0 + 4) * 32;
 constexpr unsigned long long kWaitNs = 1000000000ull;
 constexpr int kRasterGroup = 8;           // weight tiles per raster group
 constexpr uint32_t kTmemCols = 512;
+constexpr int kSmemBudget = 212 * 1024;   // A ring + B ring
+constexpr int kMaxSteps = 4;              // MMA-step ring depth (max)
 
-// Independent K accumulators and buffering per token-tile width.
+// Pipeline shape per token-tile width BN.
+//
+// * The int8 weight ring (16 KB entries) is as deep as shared memory allows:
+//   HBM needs about 200 KB in flight per SM.
+// * Synchronisation with the MMA issuer happens per MMA step of kG weight
+//   stages (16 MMAs).  A tcgen05.mma with M = 128, K = 16 issues in about 45
+//   cycles for any N <= 64, and each wait or commit costs about as much as
+//   an MMA, so batching keeps the issuing thread below the time HBM needs to
+//   deliver the weights.
+// * Tensor memory holds two BN-column accumulators and kSteps converted-A
+//   stages of kG * 64 columns; the activation ring has the same depth, and
+//   one MMA commit per step frees both.
 template <int BN>
 struct TileCfg {
-  static constexpr int kKAcc = BN <= 32 ? 4 : (BN <= 64 ? 2 : 1);
-  static constexpr int kBufs = 2;
-  static constexpr int kACol0 = kBufs * kKAcc * BN;
-  static constexpr int kBBytes = BN * kBK * 2;
-  static constexpr int kStages =
-      (200 * 1024) / (kABytes + kBBytes) > 8 ? 8 : (200 * 1024) / (kABytes + kBBytes);
-  static_assert(kACol0 + kAStages * kAColsPerStage <= (int)kTmemCols, "tensor memory budget");
-  static_assert(kStages >= 2, "pipeline depth");
+  static constexpr int kACol0 = 2 * BN;  // two accumulator buffers
+  static constexpr int kStepFit = ((int)kTmemCols - kACol0) / kAColsPerStep;
+  static constexpr int kSteps = kStepFit > kMaxSteps ? kMaxSteps : kStepFit;
+  static constexpr int kBBytesK = BN * kBK * 2;     // activations per weight stage
+  static constexpr int kBBytes = kG * kBBytesK;     // activations per MMA step
+  static constexpr int kAFit = (kSmemBudget - kSteps * kBBytes) / kABytes;
+  static constexpr int kAStagesSmem = kAFit > 12 ? 12 : kAFit;
+  static_assert(kACol0 + kSteps * kAColsPerStep <= (int)kTmemCols, "tensor memory budget");
+  static_assert(kSteps >= 2, "MMA-step depth");
+  static_assert(kAStagesSmem >= 3, "weight ring depth");
 };
 
 struct TcParams {
@@ -75,6 +92,7 @@ struct TcParams {
   const float* topk_w;
   __nv_bfloat16* act;     // gate/up output [cap, I]
   float* ypart;           // down output [splits, S, H]
+  const float* xinv;      // gate/up: per activation row, 1 / (its power-of-two scale)
   unsigned* status;
 };
 
@@ -108,10 +126,11 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
 }
 
 struct SharedCtl {
-  uint64_t full[16];
-  uint64_t empty[16];
-  uint64_t afull[kAStages];
-  uint64_t afree[kAStages];
+  uint64_t fullA[16];
+  uint64_t emptyA[16];
+  uint64_t fullB[kMaxSteps];
+  uint64_t afull[kMaxSteps];     // converted A (and its activations) ready for the MMA
+  uint64_t stepfree[kMaxSteps];  // MMAs of the step done: TMEM A stage and B stage free
   uint64_t accfull[2];
   uint64_t accempty[2];
   uint64_t drain;
@@ -136,12 +155,16 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, Sha
   }
 }
 
-// Warp-uniform bounded wait: lane 0 polls, every lane gets its verdict.
+// Warp-uniform bounded wait.  Every lane polls the same barrier (one shared
+// access per poll, all lanes see the same phase), so the warp stays
+// converged; the verdict is agreed with one vote.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, SharedCtl* ctl,
                                           unsigned* status, int lane) {
-  int ok = 0;
-  if (lane == 0) ok = wait_bounded(bar, parity, ctl, status) ? 1 : 0;
-  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+  (void)lane;
+  bool ok = mbar_try_wait(bar, parity);
+  if (__all_sync(0xffffffffu, ok)) return true;
+  ok = ok || wait_bounded(bar, parity, ctl, status);
+  return __all_sync(0xffffffffu, ok);
 }
 
 // Same, for long waits off the critical path (the epilogue waiting for a
@@ -195,11 +218,31 @@ __device__ __forceinline__ void int8x4_to_bf16x4(uint32_t w, uint32_t& lo, uint3
   asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(hi) : "r"(v1), "r"(a1), "r"(c1));
 }
 
+// int8 x4 -> two f16x2 words, exact.  Flipping the sign bit gives u = x + 128
+// in [0, 255]; the half with bits 0x64uu is 1024 + u; subtracting 1152
+// leaves x.
+__device__ __forceinline__ void int8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  const uint32_t v0 = __byte_perm(u, 0x64u, 0x4140);  // [u0, 0x64, u1, 0x64]
+  const uint32_t v1 = __byte_perm(u, 0x64u, 0x4342);  // [u2, 0x64, u3, 0x64]
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(v0), "r"(0x64806480u));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(v1), "r"(0x64806480u));
+}
+
+// 16 int8 -> 8 words of 16-bit pairs (f16 when F16, else bf16).
+template <bool F16>
 __device__ __forceinline__ void convert16(const uint4& v, uint32_t* w) {
-  int8x4_to_bf16x4(v.x, w[0], w[1]);
-  int8x4_to_bf16x4(v.y, w[2], w[3]);
-  int8x4_to_bf16x4(v.z, w[4], w[5]);
-  int8x4_to_bf16x4(v.w, w[6], w[7]);
+  if constexpr (F16) {
+    int8x4_to_f16x4(v.x, w[0], w[1]);
+    int8x4_to_f16x4(v.y, w[2], w[3]);
+    int8x4_to_f16x4(v.z, w[4], w[5]);
+    int8x4_to_f16x4(v.w, w[6], w[7]);
+  } else {
+    int8x4_to_bf16x4(v.x, w[0], w[1]);
+    int8x4_to_bf16x4(v.y, w[2], w[3]);
+    int8x4_to_bf16x4(v.z, w[4], w[5]);
+    int8x4_to_bf16x4(v.w, w[6], w[7]);
+  }
 }
 
 // 16-byte chunk c of a 128-byte swizzled shared-memory row.
@@ -211,36 +254,46 @@ __device__ __forceinline__ uint4 sel4(bool p, const uint4& a, const uint4& b) {
   return make_uint4(p ? a.x : b.x, p ? a.y : b.y, p ? a.z : b.z, p ? a.w : b.w);
 }
 
+// MODE 1: gate/up GEMM (f16 operands: activations pre-scaled per row by a
+//         power of two), SiLU-and-mul epilogue -> act (bf16).
+// MODE 2: down GEMM (bf16 operands), router-weighted epilogue -> ypart.
+//
+// Counters shared by all roles: `it` numbers weight stages (16 KB, kBK of K)
+// in schedule order, `st` numbers MMA steps (up to kG weight stages of one
+// work unit).  Ring slots are it % NA and st % ND.
 template <int MODE, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const TcParams p) {
   using C = TileCfg<BN>;
-  constexpr int STAGES = C::kStages;
-  constexpr int NKACC = C::kKAcc;
+  constexpr int NA = C::kAStagesSmem;
+  constexpr int ND = C::kSteps;
+  constexpr int kBBytesK = C::kBBytesK;
   constexpr int kBBytes = C::kBBytes;
   constexpr int kACol0 = C::kACol0;
-  constexpr uint32_t kIdesc = idesc_bf16_f32(kTileM, BN);
-  static_assert(STAGES <= 16, "stage count");
+  constexpr bool kF16 = (MODE == 1);
+  constexpr uint32_t kIdesc = kF16 ? idesc_f16_f32(kTileM, BN) : idesc_bf16_f32(kTileM, BN);
+  static_assert(NA <= 16, "ring sizes");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* sA = smem;                     // STAGES x 16 KB (int8 codes, 128-byte swizzle)
-  uint8_t* sB = smem + STAGES * kABytes;  // STAGES x 2 x BN x 128 B (bf16, 128-byte swizzle)
-  SharedCtl* ctl = reinterpret_cast<SharedCtl*>(sB + STAGES * kBBytes);
+  uint8_t* sA = smem;                 // NA x 16 KB (int8 codes, 128-byte swizzle)
+  uint8_t* sB = smem + NA * kABytes;  // ND x kG x 2 x BN x 128 B (16-bit, 128-byte swizzle)
+  SharedCtl* ctl = reinterpret_cast<SharedCtl*>(sB + ND * kBBytes);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&ctl->full[s], 1);
-      mbar_init(&ctl->empty[s], 4 + 1);  // 4 converter warps + 1 MMA commit
+    for (int s = 0; s < NA; ++s) {
+      mbar_init(&ctl->fullA[s], 1);
+      mbar_init(&ctl->emptyA[s], 4);  // the 4 warps of the converter group
     }
-    for (int s = 0; s < kAStages; ++s) {
+    for (int s = 0; s < ND; ++s) {
+      mbar_init(&ctl->fullB[s], 1);
       mbar_init(&ctl->afull[s], 4);
-      mbar_init(&ctl->afree[s], 1);
+      mbar_init(&ctl->stepfree[s], 1);  // MMA commit
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&ctl->accfull[s], 1);
@@ -263,13 +316,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int total = nb * p.MT * p.splits;
 
   if (warp == 0) {
-    // ------------------------------------------------ TMA producer ----
+    // ------------------------------------------ A producer (int8 weights) ----
     // The whole warp walks the schedule (so it stays converged); lane 0
-    // waits, issues the copies, and broadcasts the wait outcome.
-    if (lane == 0) {
-      tma_prefetch_desc(&tmA);
-      tma_prefetch_desc(&tmB);
-    }
+    // issues the copies.
+    if (lane == 0) tma_prefetch_desc(&tmA);
     int it = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
@@ -277,22 +327,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ks0 = w.split * p.ksteps / p.splits;
       const int ks1 = (w.split + 1) * p.ksteps / p.splits;
       for (int ks = ks0; ks < ks1; ++ks, ++it) {
-        const int s = it % STAGES;
-        const uint32_t ph = (it / STAGES) & 1;
-        ok = warp_wait(&ctl->empty[s], ph ^ 1, ctl, p.status, lane);
+        const int s = it % NA;
+        ok = warp_wait(&ctl->emptyA[s], ((it / NA) & 1) ^ 1, ctl, p.status, lane);
         if (!ok) break;
         if (lane == 0) {
-          mbar_arrive_expect_tx(&ctl->full[s], kABytes + kBBytes);
+          mbar_arrive_expect_tx(&ctl->fullA[s], kABytes);
           uint8_t* a = sA + s * kABytes;
           if (MODE == 1) {
             // {K, row in half, gate/up half, expert}: 64 gate rows then 64 up rows
-            tma_load_4d(a, &tmA, &ctl->full[s], ks * kBK, w.mt * 64, 0, w.e);
+            tma_load_4d(a, &tmA, &ctl->fullA[s], ks * kBK, w.mt * 64, 0, w.e);
           } else {
-            tma_load_2d(a, &tmA, &ctl->full[s], ks * kBK, w.e * p.H + w.mt * kTileM);
+            tma_load_2d(a, &tmA, &ctl->fullA[s], ks * kBK, w.e * p.H + w.mt * kTileM);
           }
-          uint8_t* b = sB + s * kBBytes;
-          tma_load_2d(b, &tmB, &ctl->full[s], ks * kBK, w.b * BN);
-          tma_load_2d(b + kBBytes / 2, &tmB, &ctl->full[s], ks * kBK + 64, w.b * BN);
         }
         __syncwarp();
       }
@@ -300,49 +346,80 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Never leave with copies in flight: wait for the last load issued into
     // each stage (iterations it-1, it-2, ...).
     if (lane == 0) {
-      const int n = it < STAGES ? it : STAGES;
+      const int n = it < NA ? it : NA;
       for (int d = 1; d <= n; ++d) {
         const int j = it - d;
-        wait_drain(&ctl->full[j % STAGES], (j / STAGES) & 1);
+        wait_drain(&ctl->fullA[j % NA], (j / NA) & 1);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ------------------------------------------ B producer (activations) ----
+    if (lane == 0) tma_prefetch_desc(&tmB);
+    int st = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+      const Unit w = decode_unit<BN>(p, u);
+      const int ks0 = w.split * p.ksteps / p.splits;
+      const int ks1 = (w.split + 1) * p.ksteps / p.splits;
+      for (int ks = ks0; ks < ks1; ks += kG, ++st) {
+        const int nk = min(kG, ks1 - ks);
+        const int d = st % ND;
+        ok = warp_wait(&ctl->stepfree[d], ((st / ND) & 1) ^ 1, ctl, p.status, lane);
+        if (!ok) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&ctl->fullB[d], nk * kBBytesK);
+          uint8_t* b = sB + d * kBBytes;
+          for (int j = 0; j < nk; ++j) {
+            const int kx = (ks + j) * kBK;
+            tma_load_2d(b + j * kBBytesK, &tmB, &ctl->fullB[d], kx, w.b * BN);
+            tma_load_2d(b + j * kBBytesK + kBBytesK / 2, &tmB, &ctl->fullB[d], kx + 64, w.b * BN);
+          }
+        }
+        __syncwarp();
+      }
+    }
+    if (lane == 0) {
+      const int n = st < ND ? st : ND;
+      for (int dd = 1; dd <= n; ++dd) {
+        const int j = st - dd;
+        wait_drain(&ctl->fullB[j % ND], (j / ND) & 1);
       }
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------- MMA issuer ----
-    int it = 0, t = 0;
+    int st = 0, t = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x, ++t) {
       const Unit w = decode_unit<BN>(p, u);
       const int ks0 = w.split * p.ksteps / p.splits;
       const int ks1 = (w.split + 1) * p.ksteps / p.splits;
       const int buf = t & 1;
-      const uint32_t bph = (t >> 1) & 1;
-      ok = warp_wait(&ctl->accempty[buf], bph ^ 1, ctl, p.status, lane);
+      ok = warp_wait(&ctl->accempty[buf], ((t >> 1) & 1) ^ 1, ctl, p.status, lane);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t d_tmem = tmem + buf * NKACC * BN;
-      for (int ks = ks0; ks < ks1; ++ks, ++it) {
-        const int s = it % STAGES;
-        const uint32_t ph = (it / STAGES) & 1;
-        const int as = it % kAStages;
-        const uint32_t aph = (it / kAStages) & 1;
-        ok = warp_wait(&ctl->afull[as], aph, ctl, p.status, lane) &&
-             warp_wait(&ctl->full[s], ph, ctl, p.status, lane);
+      const uint32_t d_tmem = tmem + buf * BN;
+      for (int ks = ks0; ks < ks1; ks += kG, ++st) {
+        const int nk = min(kG, ks1 - ks);
+        const int d = st % ND;
+        ok = warp_wait(&ctl->afull[d], (st / ND) & 1, ctl, p.status, lane);
         if (!ok) break;
         tc_fence_after();
         if (lane == 0) {
-          const uint32_t b_base = smem_addr(sB + s * kBBytes);
-          const uint32_t a_tmem = tmem + kACol0 + as * kAColsPerStage;
+          const uint32_t b_base = smem_addr(sB + d * kBBytes);
+          const uint32_t a_tmem = tmem + kACol0 + d * kAColsPerStep;
+          for (int j = 0; j < nk; ++j) {
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            // K slices 0-3 in the first 64-column box, 4-7 in the second
-            const uint32_t b_addr = b_base + (kk >> 2) * (kBBytes / 2) + (kk & 3) * 32;
-            const int acc = kk % NKACC;
-            mma_ts(d_tmem + acc * BN, a_tmem + kk * 8, smem_desc_k_sw128(b_addr), kIdesc,
-                   (ks > ks0 || kk >= NKACC) ? 1u : 0u);
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+              // K slices 0-3 in the first 64-column box, 4-7 in the second
+              const uint32_t b_addr =
+                  b_base + j * kBBytesK + (kk >> 2) * (kBBytesK / 2) + (kk & 3) * 32;
+              mma_ts(d_tmem, a_tmem + j * kAColsPerK + kk * 8, smem_desc_k_sw128(b_addr), kIdesc,
+                     (ks > ks0 || j > 0 || kk > 0) ? 1u : 0u);
+            }
           }
-          mma_commit(&ctl->empty[s]);
-          mma_commit(&ctl->afree[as]);
+          mma_commit(&ctl->stepfree[d]);
         }
         __syncwarp();
       }
@@ -358,8 +435,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp < kEpiWarp0) {
     // -------------------------------------------------- converters ----
-    const int grp = (warp - 2) >> 2;  // takes the K steps with it % kConvGroups == grp
-    const int q = warp & 3;           // tensor-memory lane quarter of this warp
+    // Per MMA step of this group: for each weight stage, wait for the int8
+    // tile, read this thread's row into registers and hand the shared-memory
+    // stage back at once; convert and write it into the step's tensor-memory
+    // A stage.  Then wait for the step's activations and tell the MMA issuer.
+    const int grp = (warp - kConvWarp0) >> 2;  // takes the steps with st % kConvGroups == grp
+    const int q = warp & 3;                    // tensor-memory lane quarter of this warp
     const int r = q * 32 + lane;
     int srow;
     int rot = 0;
@@ -367,100 +448,93 @@ __global__ void __launch_bounds__(kThreads, 1)
       // lanes (2i, 2i+1) hold gate row i and up row i of this tile
       const int i = q * 16 + (lane >> 1);
       srow = (lane & 1) ? 64 + i : i;
-      rot = (lane & 1) ? 2 : 0;  // rotated read order keeps the pair on distinct banks
+      rot = (lane & 1) ? 4 : 0;  // rotated read order keeps the pair on distinct banks
     } else {
       srow = r;
     }
     const uint32_t sw = srow & 7;  // 128-byte swizzle phase of this row
     const uint32_t tcol = ((uint32_t)(q * 32) << 16) + kACol0;
-    int it = 0;
+    const bool rt = rot != 0;
+    int it = 0, st = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
       const Unit w = decode_unit<BN>(p, u);
       const int ks0 = w.split * p.ksteps / p.splits;
       const int ks1 = (w.split + 1) * p.ksteps / p.splits;
-      for (int ks = ks0; ks < ks1; ++ks, ++it) {
-        if (it % kConvGroups != grp) continue;
-        const int s = it % STAGES;
-        const uint32_t ph = (it / STAGES) & 1;
-        const int as = it % kAStages;
-        const uint32_t aph = (it / kAStages) & 1;
-        ok = warp_wait(&ctl->full[s], ph, ctl, p.status, lane) &&
-             warp_wait(&ctl->afree[as], aph ^ 1, ctl, p.status, lane);
-        if (!ok) break;
-        tc_fence_after();
-        const uint8_t* row = sA + s * kABytes + srow * kBK;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          // x_j holds logical chunk 4h + ((j + rot) & 3)
-          const uint4 x0 = ld_chunk(row, 4 * h + ((0 + rot) & 3), sw);
-          const uint4 x1 = ld_chunk(row, 4 * h + ((1 + rot) & 3), sw);
-          const uint4 x2 = ld_chunk(row, 4 * h + ((2 + rot) & 3), sw);
-          const uint4 x3 = ld_chunk(row, 4 * h + ((3 + rot) & 3), sw);
-          const bool rt = rot != 0;
-          uint32_t words[32];
-          convert16(sel4(rt, x2, x0), &words[0]);
-          convert16(sel4(rt, x3, x1), &words[8]);
-          convert16(sel4(rt, x0, x2), &words[16]);
-          convert16(sel4(rt, x1, x3), &words[24]);
-          tmem_st32(tmem + tcol + as * kAColsPerStage + h * 32, words);
+      for (int ks = ks0; ks < ks1; ks += kG, ++st) {
+        const int nk = min(kG, ks1 - ks);
+        if (st % kConvGroups != grp) {
+          it += nk;
+          continue;
         }
+        const int d = st % ND;
+        for (int j = 0; j < nk && ok; ++j, ++it) {
+          const int sa = it % NA;
+          ok = warp_wait(&ctl->fullA[sa], (it / NA) & 1, ctl, p.status, lane);
+          if (!ok) break;
+          const uint8_t* row = sA + sa * kABytes + srow * kBK;
+          uint4 x[8];  // x[c] holds logical chunk (c + rot) & 7
+#pragma unroll
+          for (int c = 0; c < 8; ++c) x[c] = ld_chunk(row, (c + rot) & 7, sw);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl->emptyA[sa]);
+          if (j == 0) {
+            // the MMAs that last read this tensor-memory stage must be done
+            ok = warp_wait(&ctl->stepfree[d], ((st / ND) & 1) ^ 1, ctl, p.status, lane);
+            if (!ok) break;
+            tc_fence_after();
+          }
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t words[32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              // logical chunk 4h + c sits in x[4h + c] (rot 0) or x[(4h + c + 4) & 7] (rot 4)
+              convert16<kF16>(sel4(rt, x[(4 * h + c + 4) & 7], x[4 * h + c]), &words[c * 8]);
+            }
+            tmem_st32(tmem + tcol + d * kAColsPerStep + j * kAColsPerK + h * 32, words);
+          }
+        }
+        if (!ok) break;
+        ok = warp_wait(&ctl->fullB[d], (st / ND) & 1, ctl, p.status, lane);
+        if (!ok) break;
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&ctl->afull[as]);
-          mbar_arrive(&ctl->empty[s]);
-        }
+        if (lane == 0) mbar_arrive(&ctl->afull[d]);
       }
     }
   } else {
     // ---------------------------------------------------- epilogue ----
     const int q = warp & 3;
     const int r = q * 32 + lane;
-    // accumulator columns per tcgen05.ld (16 when several K accumulators are summed)
-    constexpr int CH = (BN < 32 || NKACC > 1) ? 16 : 32;
+    constexpr int CH = BN < 32 ? BN : 32;  // accumulator columns per tcgen05.ld
     int t = 0;
     for (int u = blockIdx.x; u < total; u += gridDim.x, ++t) {
       const Unit w = decode_unit<BN>(p, u);
       const int buf = t & 1;
-      const uint32_t bph = (t >> 1) & 1;
-      if (!warp_wait_sleepy(&ctl->accfull[buf], bph, ctl, p.status, lane)) break;
+      if (!warp_wait_sleepy(&ctl->accfull[buf], (t >> 1) & 1, ctl, p.status, lane)) break;
       tc_fence_after();
-      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + buf * NKACC * BN;
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + buf * BN;
       if (MODE == 1) {
         const int i = q * 16 + (lane >> 1);
         const int wrow = w.e * 2 * p.I + ((lane & 1) ? p.I : 0) + w.mt * 64 + i;
         const float sc = p.scale[wrow];
         const int col = w.mt * 64 + i;
         for (int c0 = 0; c0 < BN; c0 += CH) {
-          float acc[CH];
-          {
-            uint32_t v[CH];
-            tmem_ld_cols<CH>(taddr + c0, v);
-            tmem_ld_wait();
-#pragma unroll
-            for (int jj = 0; jj < CH; ++jj) acc[jj] = __uint_as_float(v[jj]);
-          }
-#pragma unroll
-          for (int a = 1; a < NKACC; ++a) {
-            uint32_t v[CH];
-            tmem_ld_cols<CH>(taddr + a * BN + c0, v);
-            tmem_ld_wait();
-#pragma unroll
-            for (int jj = 0; jj < CH; ++jj) acc[jj] += __uint_as_float(v[jj]);
-          }
+          uint32_t v[CH];
+          tmem_ld_cols<CH>(taddr + c0, v);
+          tmem_ld_wait();
 #pragma unroll
           for (int jj = 0; jj < CH; ++jj) {
-            const float own = acc[jj] * sc;
+            const int prow = w.b * BN + c0 + jj;
+            const float own = __uint_as_float(v[jj]) * sc * p.xinv[prow];
             const float other = __shfl_xor_sync(0xffffffffu, own, 1);
             const float g = (lane & 1) ? other : own;
             const float up = (lane & 1) ? own : other;
             // even lane stores the first half of the columns, odd lane the rest
-            if ((jj >= CH / 2) == ((lane & 1) != 0)) {
-              const int prow = w.b * BN + c0 + jj;
+            if ((jj >= CH / 2) == ((lane & 1) != 0))
               p.act[(int64_t)prow * p.I + col] = __float2bfloat16_rn(mq::silu_mul(g, up));
-            }
           }
         }
       } else {
@@ -468,26 +542,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float sc = p.scale[w.e * p.H + h];
         float* yp = p.ypart + (int64_t)w.split * p.S * p.H;
         for (int c0 = 0; c0 < BN; c0 += CH) {
-          float acc[CH];
-          {
-            uint32_t v[CH];
-            tmem_ld_cols<CH>(taddr + c0, v);
-            tmem_ld_wait();
-#pragma unroll
-            for (int jj = 0; jj < CH; ++jj) acc[jj] = __uint_as_float(v[jj]);
-          }
-#pragma unroll
-          for (int a = 1; a < NKACC; ++a) {
-            uint32_t v[CH];
-            tmem_ld_cols<CH>(taddr + a * BN + c0, v);
-            tmem_ld_wait();
-#pragma unroll
-            for (int jj = 0; jj < CH; ++jj) acc[jj] += __uint_as_float(v[jj]);
-          }
+          uint32_t v[CH];
+          tmem_ld_cols<CH>(taddr + c0, v);
+          tmem_ld_wait();
 #pragma unroll
           for (int jj = 0; jj < CH; ++jj) {
             const int slot = p.sorted[w.b * BN + c0 + jj];
-            if (slot < p.S) yp[(int64_t)slot * p.H + h] = acc[jj] * sc * p.topk_w[slot];
+            if (slot < p.S) yp[(int64_t)slot * p.H + h] = __uint_as_float(v[jj]) * sc * p.topk_w[slot];
           }
         }
       }
@@ -505,22 +566,55 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Rows of x gathered into expert-sorted order (zeros for padding slots).
-__global__ void __launch_bounds__(128) gather_rows(const __nv_bfloat16* __restrict__ x,
-                                                   const int32_t* __restrict__ sorted,
-                                                   const int32_t* __restrict__ num_padded, int k,
-                                                   int S, int H, __nv_bfloat16* __restrict__ xs) {
+// Rows of x gathered into expert-sorted order as f16, each scaled by a power
+// of two 2^e chosen so that the row's largest magnitude lands in
+// [2^14, 2^15): bf16 -> f16 is then exact except for elements below 2^-28
+// of the row maximum (f16 subnormals).  xinv[p] = 2^-e undoes it in the
+// epilogue.  Padding rows are zeros.
+__global__ void __launch_bounds__(128) gather_rows_f16(const __nv_bfloat16* __restrict__ x,
+                                                       const int32_t* __restrict__ sorted,
+                                                       const int32_t* __restrict__ num_padded,
+                                                       int k, int S, int H,
+                                                       __half* __restrict__ xs,
+                                                       float* __restrict__ xinv) {
+  __shared__ float wmax[4];
   const int p = blockIdx.x;
   if (p >= *num_padded) return;
   const int s = sorted[p];
-  uint4* dst = reinterpret_cast<uint4*>(xs + (int64_t)p * H);
-  const int n = H / 8;
-  if (s < S) {
-    const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)(s / k) * H);
-    for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = src[i];
-  } else {
-    for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = make_uint4(0, 0, 0, 0);
+  uint2* dst = reinterpret_cast<uint2*>(xs + (int64_t)p * H);  // 4 halves per uint2
+  const int n = H / 4;
+  if (s >= S) {
+    for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = make_uint2(0, 0);
+    if (threadIdx.x == 0) xinv[p] = 1.0f;
+    return;
   }
+  const uint2* src = reinterpret_cast<const uint2*>(x + (int64_t)(s / k) * H);
+  float m = 0.0f;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const uint2 v = src[i];
+    m = fmaxf(m, fmaxf(fmaxf(fabsf(mq::bf16_lo(v.x)), fabsf(mq::bf16_hi(v.x))),
+                       fmaxf(fabsf(mq::bf16_lo(v.y)), fabsf(mq::bf16_hi(v.y)))));
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
+  __syncthreads();
+  m = fmaxf(fmaxf(wmax[0], wmax[1]), fmaxf(wmax[2], wmax[3]));
+  int ex = 0;
+  if (m > 0.0f) frexpf(m, &ex);  // m = f * 2^ex, f in [0.5, 1)
+  int e = 15 - ex;               // m * 2^e in [2^14, 2^15)
+  e = max(-120, min(120, e));
+  const float scale = ldexpf(1.0f, e);
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const uint2 v = src[i];
+    const __half2 a = __floats2half2_rn(mq::bf16_lo(v.x) * scale, mq::bf16_hi(v.x) * scale);
+    const __half2 b = __floats2half2_rn(mq::bf16_lo(v.y) * scale, mq::bf16_hi(v.y) * scale);
+    uint2 o;
+    o.x = *reinterpret_cast<const uint32_t*>(&a);
+    o.y = *reinterpret_cast<const uint32_t*>(&b);
+    dst[i] = o;
+  }
+  if (threadIdx.x == 0) xinv[p] = ldexpf(1.0f, -e);
 }
 
 // out[t, :] = sum over valid slots j and K splits of ypart[split, t*k + j, :].
@@ -589,7 +683,8 @@ cudaError_t make_map(CUtensorMap* map, CUtensorMapDataType dt, int rank, const v
 template <int BN>
 constexpr size_t smem_for() {
   using C = TileCfg<BN>;
-  const size_t need = 1024 + (size_t)C::kStages * (kABytes + C::kBBytes) + sizeof(SharedCtl);
+  const size_t need = 1024 + (size_t)C::kAStagesSmem * kABytes + (size_t)C::kSteps * C::kBBytes +
+                      sizeof(SharedCtl);
   return need < 120 * 1024 ? 120 * 1024 : need;
 }
 
@@ -652,14 +747,15 @@ int tc_num_sms() {
   return g_num_sms > 0 ? g_num_sms : 148;
 }
 
-cudaError_t launch_gather_rows(const MoeArgs& a, __nv_bfloat16* xs, cudaStream_t st) {
+cudaError_t launch_gather_rows(const MoeArgs& a, void* xs, float* xinv, cudaStream_t st) {
   if (a.cap == 0) return cudaSuccess;
-  gather_rows<<<(unsigned)a.cap, 128, 0, st>>>(a.x, a.sorted, a.num_padded, a.k, a.T * a.k, a.H, xs);
+  gather_rows_f16<<<(unsigned)a.cap, 128, 0, st>>>(a.x, a.sorted, a.num_padded, a.k, a.T * a.k,
+                                                   a.H, static_cast<__half*>(xs), xinv);
   return cudaGetLastError();
 }
 
-cudaError_t launch_gemm1_tc(const MoeArgs& a, const TcPlan& pl, const __nv_bfloat16* xs,
-                            cudaStream_t st) {
+cudaError_t launch_gemm1_tc(const MoeArgs& a, const TcPlan& pl, const void* xs,
+                            const float* xinv, cudaStream_t st) {
   cudaError_t err = get_encoder();
   if (err != cudaSuccess) return err;
   CUtensorMap ta, tb;
@@ -676,7 +772,7 @@ cudaError_t launch_gemm1_tc(const MoeArgs& a, const TcPlan& pl, const __nv_bfloa
     const cuuint64_t dims[2] = {(cuuint64_t)a.H, (cuuint64_t)a.cap};
     const cuuint64_t strides[1] = {(cuuint64_t)a.H * 2};
     const cuuint32_t box[2] = {64, (cuuint32_t)pl.bn};
-    err = make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, xs, dims, strides, box,
+    err = make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, xs, dims, strides, box,
                    CU_TENSOR_MAP_SWIZZLE_128B);
     if (err != cudaSuccess) return err;
   }
@@ -691,6 +787,7 @@ cudaError_t launch_gemm1_tc(const MoeArgs& a, const TcPlan& pl, const __nv_bfloa
   p.topk_w = a.topk_w;
   p.act = a.act;
   p.ypart = nullptr;
+  p.xinv = xinv;
   p.status = a.status;
   const int64_t units = (a.cap / pl.bn) * (int64_t)p.MT;
   return launch_gemm_bn<1>(pl.bn, ta, tb, p, (int)(units < (1 << 30) ? units : (1 << 30)), st);
@@ -727,6 +824,7 @@ cudaError_t launch_gemm2_tc(const MoeArgs& a, const TcPlan& pl, float* ypart, cu
   p.topk_w = a.topk_w;
   p.act = nullptr;
   p.ypart = ypart;
+  p.xinv = nullptr;
   p.status = a.status;
   const int64_t units = (a.cap / pl.bn) * (int64_t)p.MT * p.splits;
   return launch_gemm_bn<2>(pl.bn, ta, tb, p, (int)(units < (1 << 30) ? units : (1 << 30)), st);

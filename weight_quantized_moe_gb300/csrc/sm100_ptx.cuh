@@ -192,5 +192,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
          | ((uint32_t)(M >> 4) << 24);  // M / 16
 }
 
+// Instruction descriptor, kind::f16: f16 x f16 -> f32, A and B K-major.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+  return (1u << 4)                      // D format: f32
+         | ((uint32_t)(N >> 3) << 17)   // N / 8   (A, B formats 0 = f16)
+         | ((uint32_t)(M >> 4) << 24);  // M / 16
+}
+
 }  // namespace ptx
 }  // namespace mq
