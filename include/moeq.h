@@ -194,6 +194,37 @@ int moe_quant_forward(const void* x, int T, int H, int I, int E, int k,
                       void* out, void* stream);
 
 /*
+ * moe_quant_forward_noalloc -- moe_quant_forward without a workspace
+ * argument.  (The pages have no counterpart: their forward allocates its
+ * intermediates through torch.)
+ *
+ * For callers that cannot allocate device memory or hand over a workspace:
+ * e.g. a plugin inside a host application that owns all device memory
+ * through its own allocator and passes the plugin only its input and output
+ * buffers, or a path on which an allocation (a synchronising call that may
+ * fail) is not allowed.  The scratch the forward needs lives in a fixed
+ * 32 MiB array inside libmoeq.so, held on every GPU that loads the library
+ * until the process exits.  Nothing is allocated per call.
+ *
+ * Arguments, layouts and results are those of moe_quant_forward.  Sizes whose
+ * scratch (moe_quant_forward_workspace) exceeds 32 MiB are rejected with
+ * MQ_ERR_UNSUPPORTED and a message naming both sizes; nothing is launched.
+ * The first call on each device looks up that device's address of the array
+ * (a CUDA runtime query, no allocation), so make that first call before any
+ * stream capture.  All calls on a device share the one array, which keeps
+ * the previous call's contents (nothing in it needs to start at zero): calls
+ * whose GPU work overlaps -- on different streams, or from several host
+ * threads -- race on it and must be serialised by the caller.
+ */
+int moe_quant_forward_noalloc(const void* x, int T, int H, int I, int E, int k,
+                              int bits, int group_size, int has_zp,
+                              const void* w13, const void* w2,
+                              const void* s13, const void* s2,
+                              const uint8_t* z13, const uint8_t* z2,
+                              const float* topk_w, const int32_t* topk_ids,
+                              void* out, void* stream);
+
+/*
  * Instrumentation (no counterpart on the pages; used by the benchmark).
  *
  * mq_kernel_launch_count: kernels this library has launched in this process.

@@ -34,6 +34,8 @@ _SIGNATURES = {
     "moe_quant_forward_workspace": (_sz, [_i32] * 7),
     "moe_quant_forward": (_i32, [_vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
                                  _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _vp]),
+    "moe_quant_forward_noalloc": (_i32, [_vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
+                                         _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "mq_kernel_launch_count": (ctypes.c_longlong, []),
     "mq_profile_enable": (_i32, [_i32]),
     "mq_profile_read": (_i32, [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_longlong), _i32]),
@@ -239,4 +241,25 @@ def moe_quant_forward(x, w13, w2, s13, s2, topk_w, topk_ids, bits=8, group_size=
         _ptr(w13), _ptr(w2), _ptr(s13), _ptr(s2), _ptr(z13 if has_zp else None),
         _ptr(z2 if has_zp else None), _ptr(topk_w), _ptr(topk_ids),
         _ptr(workspace), workspace.numel(), _ptr(out), _stream(stream)))
+    return out
+
+
+def moe_quant_forward_noalloc(x, w13, w2, s13, s2, topk_w, topk_ids, bits=8, group_size=-1,
+                              has_zp=False, z13=None, z2=None, out=None, stream=None):
+    """moe_quant_forward with the library's fixed scratch instead of a
+    workspace (for callers that cannot allocate; see include/moeq.h)."""
+    _need(x, torch.bfloat16, "x", 2)
+    T, H = x.shape
+    E = w13.shape[0]
+    I = w13.shape[1] // 2
+    k = topk_ids.shape[-1] if topk_ids.dim() == 2 else 1
+    _need(topk_w, torch.float32, "topk_w")
+    _need(topk_ids, torch.int32, "topk_ids")
+    if out is None:
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=x.device)
+    _need(out, torch.bfloat16, "out", 2)
+    _check(lib().moe_quant_forward_noalloc(
+        _ptr(x), T, H, I, E, k, bits, group_size, int(bool(has_zp)),
+        _ptr(w13), _ptr(w2), _ptr(s13), _ptr(s2), _ptr(z13 if has_zp else None),
+        _ptr(z2 if has_zp else None), _ptr(topk_w), _ptr(topk_ids), _ptr(out), _stream(stream)))
     return out

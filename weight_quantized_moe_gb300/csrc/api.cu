@@ -139,6 +139,8 @@ bool fmt_ok(int bits, int group_size, int has_zp) {
 
 }  // namespace
 
+int mq_set_error(int status, const char* msg) { return fail(status, "%s", msg); }
+
 MQ_EXPORT const char* mq_status_string(int status) {
   switch (status) {
     case MQ_OK: return "ok";

@@ -94,6 +94,8 @@ MQ_HIDDEN cudaError_t launch_combine_splits(const MoeArgs& a, const float* ypart
                                             cudaStream_t st);
 
 MQ_HIDDEN int simple_block_m();
+// Records `msg` as the calling thread's mq_last_error_message(); returns status.
+MQ_HIDDEN int mq_set_error(int status, const char* msg);
 MQ_HIDDEN cudaError_t launch_gemm1_simple(const MoeArgs& a, cudaStream_t st);
 MQ_HIDDEN cudaError_t launch_gemm2_simple(const MoeArgs& a, cudaStream_t st);
 MQ_HIDDEN cudaError_t launch_combine(const MoeArgs& a, cudaStream_t st);
