@@ -9,20 +9,18 @@
 //   shared memory, one 16 KB box (128 rows x 128 bytes) per K step; for the
 //   gate/up GEMM a 4-D tensor map fetches the 64 gate rows and the matching
 //   64 up rows in that one box.  Converter warpgroups turn the codes into
-//   bf16 (exact: every int8 value is a bf16) and write them straight into
-//   tensor memory with tcgen05.st, so shared memory never holds bf16
-//   weights.  The per-channel scale is applied once per output in the
+//   f16 (gate/up) or bf16 (down) -- exact, every int8 value is both -- and
+//   write them straight into tensor memory with tcgen05.st, so shared
+//   memory never holds 16-bit weights.  The per-channel scale is applied once per output in the
 //   epilogue (sum_k x*(q*s) = s * sum_k x*q).
 // * The activations (token rows gathered per expert block) are the B
-//   operand: TMA tiles with the 128-byte swizzle, read by tcgen05.mma from
-//   shared memory.
+//   operand: TMA tiles with the 128-byte swizzle in a second, short ring,
+//   read by tcgen05.mma from shared memory.
 // * Accumulators live in tensor memory, double-buffered across work units.
-//   For small BN the K steps are spread round-robin over NKACC independent
-//   accumulators (summed in the epilogue) so that consecutive MMAs do not
-//   wait on each other's results.
 // * One persistent CTA per SM walks the work units (expert block, weight
-//   tile, K split).  Warp roles: 0 TMA producer, 1 MMA issuer, 2-9 two
-//   converter warpgroups taking alternate K steps, 10-13 epilogue.
+//   tile, K split).  Warp roles: 0 weight producer (TMA), 1 MMA issuer,
+//   2 activation producer (TMA), 3-10 two converter warpgroups taking
+//   alternate MMA steps, 11-14 epilogue.
 // * Every mbarrier wait is bounded: after kWaitNs the CTA flags
 //   MQ_DEV_WAIT_TIMEOUT, stops issuing work, drains its own copies and MMAs
 //   (with a bound again), frees its tensor memory and exits.
@@ -52,6 +50,7 @@ constexpr int kRasterGroup = 8;           // weight tiles per raster group
 constexpr uint32_t kTmemCols = 512;
 constexpr int kSmemBudget = 212 * 1024;   // A ring + B ring
 constexpr int kMaxSteps = 4;              // MMA-step ring depth (max)
+constexpr int kUnitList = 512;            // work units per CTA decoded once into shared memory
 
 // Pipeline shape per token-tile width BN.
 //
@@ -125,7 +124,23 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
   return out;
 }
 
-struct SharedCtl {
+// Unit number i of this CTA (u = blockIdx.x + i * gridDim.x): from the list
+// decoded in the prologue, or decoded on the spot past its end.
+template <int BN>
+__device__ __forceinline__ Unit cta_unit(const TcParams& p, const int4* ulist, int i, int u) {
+  if (i < kUnitList) {
+    const int4 v = ulist[i];
+    Unit w;
+    w.e = v.x;
+    w.b = v.y;
+    w.mt = v.z;
+    w.split = v.w;
+    return w;
+  }
+  return decode_unit<BN>(p, u);
+}
+
+struct alignas(16) SharedCtl {
   uint64_t fullA[16];
   uint64_t emptyA[16];
   uint64_t fullB[kMaxSteps];
@@ -307,13 +322,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(&ctl->tmem_base, kTmemCols);
     tmem_relinquish();
   }
+  // Decode this CTA's work units once, all threads in parallel, so that no
+  // role waits on the schedule's global loads at a unit boundary.
+  const int nb = *p.num_padded / BN;
+  const int total = nb * p.MT * p.splits;
+  int4* ulist = reinterpret_cast<int4*>(ctl + 1);
+  for (int i = threadIdx.x; i < kUnitList; i += kThreads) {
+    const int u = blockIdx.x + i * gridDim.x;
+    if (u >= total) break;
+    const Unit w = decode_unit<BN>(p, u);
+    ulist[i] = make_int4(w.e, w.b, w.mt, w.split);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
-
-  const int nb = *p.num_padded / BN;
-  const int total = nb * p.MT * p.splits;
 
   if (warp == 0) {
     // ------------------------------------------ A producer (int8 weights) ----
@@ -322,8 +345,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) tma_prefetch_desc(&tmA);
     int it = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-      const Unit w = decode_unit<BN>(p, u);
+    for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
+      const Unit w = cta_unit<BN>(p, ulist, ui, u);
       const int ks0 = w.split * p.ksteps / p.splits;
       const int ks1 = (w.split + 1) * p.ksteps / p.splits;
       for (int ks = ks0; ks < ks1; ++ks, ++it) {
@@ -358,8 +381,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) tma_prefetch_desc(&tmB);
     int st = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-      const Unit w = decode_unit<BN>(p, u);
+    for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
+      const Unit w = cta_unit<BN>(p, ulist, ui, u);
       const int ks0 = w.split * p.ksteps / p.splits;
       const int ks1 = (w.split + 1) * p.ksteps / p.splits;
       for (int ks = ks0; ks < ks1; ks += kG, ++st) {
@@ -392,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int st = 0, t = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x, ++t) {
-      const Unit w = decode_unit<BN>(p, u);
+      const Unit w = cta_unit<BN>(p, ulist, t, u);
       const int ks0 = w.split * p.ksteps / p.splits;
       const int ks1 = (w.split + 1) * p.ksteps / p.splits;
       const int buf = t & 1;
@@ -457,8 +480,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool rt = rot != 0;
     int it = 0, st = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-      const Unit w = decode_unit<BN>(p, u);
+    for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
+      const Unit w = cta_unit<BN>(p, ulist, ui, u);
       const int ks0 = w.split * p.ksteps / p.splits;
       const int ks1 = (w.split + 1) * p.ksteps / p.splits;
       for (int ks = ks0; ks < ks1; ks += kG, ++st) {
@@ -511,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int CH = BN < 32 ? BN : 32;  // accumulator columns per tcgen05.ld
     int t = 0;
     for (int u = blockIdx.x; u < total; u += gridDim.x, ++t) {
-      const Unit w = decode_unit<BN>(p, u);
+      const Unit w = cta_unit<BN>(p, ulist, t, u);
       const int buf = t & 1;
       if (!warp_wait_sleepy(&ctl->accfull[buf], (t >> 1) & 1, ctl, p.status, lane)) break;
       tc_fence_after();
@@ -684,7 +707,7 @@ template <int BN>
 constexpr size_t smem_for() {
   using C = TileCfg<BN>;
   const size_t need = 1024 + (size_t)C::kAStagesSmem * kABytes + (size_t)C::kSteps * C::kBBytes +
-                      sizeof(SharedCtl);
+                      sizeof(SharedCtl) + kUnitList * sizeof(int4);
   return need < 120 * 1024 ? 120 * 1024 : need;
 }
 
