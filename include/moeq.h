@@ -243,6 +243,7 @@ int moe_quant_forward_noalloc(const void* x, int T, int H, int I, int E, int k,
 #define MQ_PROF_GEMM2   4
 #define MQ_PROF_COMBINE 5
 #define MQ_PROF_GATHER  6
+#define MQ_PROF_ACTF16  7
 #define MQ_PROF_SLOTS   8
 
 long long mq_kernel_launch_count(void);

@@ -107,6 +107,17 @@ def test_forward_w4a16():
     assert _run(layer, 24, seed=2) <= FWD_TOL
 
 
+@pytest.mark.parametrize("gs,zp,H,I", [(64, False, 256, 384), (32, True, 128, 256),
+                                       (256, True, 512, 256), (128, True, 384, 640)])
+def test_forward_w4a16_group_sizes(gs, zp, H, I):
+    """Group sizes 32..256, implicit zero point (8), and K not a multiple of
+    256 (a half-filled last weight stage)."""
+    wl = synth.Workload(f"w4a16_gs{gs}", E=6, k=2, H=H, I=I, Ts=(20,), bits=4, group_size=gs,
+                        has_zp=zp)
+    layer = Layer(wl, seed=gs)
+    assert _run(layer, 20, seed=gs) <= FWD_TOL
+
+
 def test_forward_w4a16_full_sampled():
     """The full W4A16 layer (E=64, k=6, H=2048, I=1408, gs=128) at T=32."""
     layer = Layer(W["w4a16"], seed=0)

@@ -41,7 +41,7 @@ _SIGNATURES = {
     "mq_profile_read": (_i32, [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_longlong), _i32]),
 }
 
-PROF_SLOTS = ("quant", "route", "align", "gemm1", "gemm2", "combine", "gather", "slot7")
+PROF_SLOTS = ("quant", "route", "align", "gemm1", "gemm2", "combine", "gather", "act_f16")
 
 _lib = None
 

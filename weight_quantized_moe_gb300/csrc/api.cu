@@ -99,19 +99,18 @@ unsigned* status_ptr() {
 
 inline size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
 
-// Workspace layout of moe_quant_forward.  W8A16 runs the tensor-core path
-// (gathered activations, split-K partial outputs); W4A16 the CUDA-core path.
+// Workspace layout of moe_quant_forward: align arrays, gathered activations
+// (f16) and their row scales, act (bf16, then f16 in place) and its row
+// scales, split-K partial outputs (fp32).
 struct WsLayout {
-  size_t sorted, block_expert, offsets, num_padded, xs, xinv, act, y, total;
+  size_t sorted, block_expert, offsets, num_padded, xs, xinv, act, act_inv, y, total;
   int64_t cap;
   TcPlan plan;
-  bool tc;
 };
 
 WsLayout ws_layout(int T, int H, int I, int E, int k, int bits) {
   WsLayout L;
-  L.tc = (bits == 8);
-  L.plan = L.tc ? tc_plan(T, H, I, E, k) : TcPlan{simple_block_m(), 1};
+  L.plan = tc_plan(T, H, I, E, k, bits);
   const int bm = L.plan.bn;
   const int64_t S = (int64_t)T * k;
   const int64_t cap = moe_align_capacity(T, k, E, bm);
@@ -121,9 +120,10 @@ WsLayout ws_layout(int T, int H, int I, int E, int k, int bits) {
   L.block_expert = off; off += align256(sizeof(int32_t) * (size_t)(cap / bm));
   L.offsets = off;      off += align256(sizeof(int32_t) * (size_t)(E + 1));
   L.num_padded = off;   off += align256(sizeof(int32_t));
-  L.xs = off;           off += L.tc ? align256(sizeof(__half) * (size_t)cap * (size_t)H) : 0;
-  L.xinv = off;         off += L.tc ? align256(sizeof(float) * (size_t)cap) : 0;
+  L.xs = off;           off += align256(sizeof(__half) * (size_t)cap * (size_t)H);
+  L.xinv = off;         off += align256(sizeof(float) * (size_t)cap);
   L.act = off;          off += align256(sizeof(__nv_bfloat16) * (size_t)cap * (size_t)I);
+  L.act_inv = off;      off += align256(sizeof(float) * (size_t)cap);
   L.y = off;            off += align256(sizeof(float) * (size_t)L.plan.splits * (size_t)S * (size_t)H);
   L.total = off;
   return L;
@@ -347,43 +347,32 @@ MQ_EXPORT int moe_quant_forward(const void* x, int T, int H, int I, int E, int k
                        a.status, st);
   }
   if (err != cudaSuccess) return cuda_fail(err, "forward: align launch");
-  if (L.tc) {
-    void* xs = ws + L.xs;
-    float* xinv = reinterpret_cast<float*>(ws + L.xinv);
-    {
-      LaunchScope ls(MQ_PROF_GATHER, st);
-      err = launch_gather_rows(a, xs, xinv, st);
-    }
-    if (err != cudaSuccess) return cuda_fail(err, "forward: gather launch");
-    {
-      LaunchScope ls(MQ_PROF_GEMM1, st);
-      err = launch_gemm1_tc(a, L.plan, xs, xinv, st);
-    }
-    if (err != cudaSuccess) return cuda_fail(err, "forward: gate/up GEMM launch");
-    {
-      LaunchScope ls(MQ_PROF_GEMM2, st);
-      err = launch_gemm2_tc(a, L.plan, a.y, st);
-    }
-    if (err != cudaSuccess) return cuda_fail(err, "forward: down GEMM launch");
-    {
-      LaunchScope ls(MQ_PROF_COMBINE, st);
-      err = launch_combine_splits(a, a.y, L.plan.splits, st);
-    }
-  } else {
-    {
-      LaunchScope ls(MQ_PROF_GEMM1, st);
-      err = launch_gemm1_simple(a, st);
-    }
-    if (err != cudaSuccess) return cuda_fail(err, "forward: gate/up GEMM launch");
-    {
-      LaunchScope ls(MQ_PROF_GEMM2, st);
-      err = launch_gemm2_simple(a, st);
-    }
-    if (err != cudaSuccess) return cuda_fail(err, "forward: down GEMM launch");
-    {
-      LaunchScope ls(MQ_PROF_COMBINE, st);
-      err = launch_combine(a, st);
-    }
+  void* xs = ws + L.xs;
+  float* xinv = reinterpret_cast<float*>(ws + L.xinv);
+  {
+    LaunchScope ls(MQ_PROF_GATHER, st);
+    err = launch_gather_rows(a, xs, xinv, st);
+  }
+  if (err != cudaSuccess) return cuda_fail(err, "forward: gather launch");
+  {
+    LaunchScope ls(MQ_PROF_GEMM1, st);
+    err = launch_gemm1_tc(a, L.plan, xs, xinv, st);
+  }
+  if (err != cudaSuccess) return cuda_fail(err, "forward: gate/up GEMM launch");
+  float* act_inv = reinterpret_cast<float*>(ws + L.act_inv);
+  {
+    LaunchScope ls(MQ_PROF_ACTF16, st);
+    err = launch_act_to_f16(a, act_inv, st);
+  }
+  if (err != cudaSuccess) return cuda_fail(err, "forward: act conversion launch");
+  {
+    LaunchScope ls(MQ_PROF_GEMM2, st);
+    err = launch_gemm2_tc(a, L.plan, act_inv, a.y, st);
+  }
+  if (err != cudaSuccess) return cuda_fail(err, "forward: down GEMM launch");
+  {
+    LaunchScope ls(MQ_PROF_COMBINE, st);
+    err = launch_combine_splits(a, a.y, L.plan.splits, st);
   }
   if (err != cudaSuccess) return cuda_fail(err, "forward: combine launch");
   return MQ_OK;

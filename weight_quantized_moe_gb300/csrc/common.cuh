@@ -83,19 +83,16 @@ struct TcPlan {
   int bn;      // token-slots per aligned block (MMA N)
   int splits;  // K splits of the down GEMM
 };
-MQ_HIDDEN TcPlan tc_plan(int T, int H, int I, int E, int k);
+MQ_HIDDEN TcPlan tc_plan(int T, int H, int I, int E, int k, int bits);
 MQ_HIDDEN int tc_num_sms();
 MQ_HIDDEN cudaError_t launch_gather_rows(const MoeArgs& a, void* xs, float* xinv, cudaStream_t st);
 MQ_HIDDEN cudaError_t launch_gemm1_tc(const MoeArgs& a, const TcPlan& pl, const void* xs,
                                       const float* xinv, cudaStream_t st);
-MQ_HIDDEN cudaError_t launch_gemm2_tc(const MoeArgs& a, const TcPlan& pl, float* ypart,
-                                      cudaStream_t st);
+MQ_HIDDEN cudaError_t launch_act_to_f16(const MoeArgs& a, float* act_inv, cudaStream_t st);
+MQ_HIDDEN cudaError_t launch_gemm2_tc(const MoeArgs& a, const TcPlan& pl, const float* act_inv,
+                                      float* ypart, cudaStream_t st);
 MQ_HIDDEN cudaError_t launch_combine_splits(const MoeArgs& a, const float* ypart, int splits,
                                             cudaStream_t st);
 
-MQ_HIDDEN int simple_block_m();
 // Records `msg` as the calling thread's mq_last_error_message(); returns status.
 MQ_HIDDEN int mq_set_error(int status, const char* msg);
-MQ_HIDDEN cudaError_t launch_gemm1_simple(const MoeArgs& a, cudaStream_t st);
-MQ_HIDDEN cudaError_t launch_gemm2_simple(const MoeArgs& a, cudaStream_t st);
-MQ_HIDDEN cudaError_t launch_combine(const MoeArgs& a, cudaStream_t st);

@@ -80,14 +80,19 @@ struct TileCfg {
 
 struct TcParams {
   int H, I, E, k, S;
-  int ksteps;        // K / kBK
+  int ksteps;        // weight stages per row: ceil(K / stage K)
   int MT;            // weight tiles per expert
   int splits;        // K splits
   const int32_t* sorted;
   const int32_t* block_expert;
   const int32_t* offsets;
   const int32_t* num_padded;
-  const float* scale;     // fp32 per-output-row scales of this GEMM's weights
+  const float* scale;     // int8: fp32 per-output-row scales of this GEMM's weights
+  const __half* gscale;   // uint4: f16 group scales [rows, G]
+  const uint8_t* gzero;   // uint4: zero points [rows / 2, G], even row in the low nibble
+  int G;                  // uint4: groups per row (K / group_size)
+  int gs;                 // uint4: group size
+  int has_zp;             // uint4: 0 -> implicit zero 8
   const float* topk_w;
   __nv_bfloat16* act;     // gate/up output [cap, I]
   float* ypart;           // down output [splits, S, H]
@@ -216,23 +221,6 @@ __device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity) {
   }
 }
 
-// int8 x4 (one 32-bit word) -> two bf16x2 words, exact.
-// Each byte b is placed in the low byte of a bf16 whose high byte is 0x43:
-// for b < 128 that bf16 is 128 + b, for b >= 128 (negative x = b - 256) it
-// is 256 + 2 * (b - 128) = 512 + 2x.  One bf16x2 FMA with per-half
-// coefficients (1, -128) or (0.5, -256), chosen by the byte's top bit,
-// returns x exactly.
-__device__ __forceinline__ void int8x4_to_bf16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  const uint32_t v0 = __byte_perm(w, 0x43u, 0x4140);  // [b0, 0x43, b1, 0x43]
-  const uint32_t v1 = __byte_perm(w, 0x43u, 0x4342);  // [b2, 0x43, b3, 0x43]
-  const uint32_t t0 = v0 & 0x00800080u;
-  const uint32_t t1 = v1 & 0x00800080u;
-  const uint32_t a0 = t0 ^ 0x3F803F80u, c0 = t0 | 0xC300C300u;
-  const uint32_t a1 = t1 ^ 0x3F803F80u, c1 = t1 | 0xC300C300u;
-  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(lo) : "r"(v0), "r"(a0), "r"(c0));
-  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(hi) : "r"(v1), "r"(a1), "r"(c1));
-}
-
 // int8 x4 -> two f16x2 words, exact.  Flipping the sign bit gives u = x + 128
 // in [0, 255]; the half with bits 0x64uu is 1024 + u; subtracting 1152
 // leaves x.
@@ -244,20 +232,19 @@ __device__ __forceinline__ void int8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32
   asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(v1), "r"(0x64806480u));
 }
 
-// 16 int8 -> 8 words of 16-bit pairs (f16 when F16, else bf16).
-template <bool F16>
+// 16 int8 -> 8 words of f16 pairs.
 __device__ __forceinline__ void convert16(const uint4& v, uint32_t* w) {
-  if constexpr (F16) {
-    int8x4_to_f16x4(v.x, w[0], w[1]);
-    int8x4_to_f16x4(v.y, w[2], w[3]);
-    int8x4_to_f16x4(v.z, w[4], w[5]);
-    int8x4_to_f16x4(v.w, w[6], w[7]);
-  } else {
-    int8x4_to_bf16x4(v.x, w[0], w[1]);
-    int8x4_to_bf16x4(v.y, w[2], w[3]);
-    int8x4_to_bf16x4(v.z, w[4], w[5]);
-    int8x4_to_bf16x4(v.w, w[6], w[7]);
-  }
+  int8x4_to_f16x4(v.x, w[0], w[1]);
+  int8x4_to_f16x4(v.y, w[2], w[3]);
+  int8x4_to_f16x4(v.z, w[4], w[5]);
+  int8x4_to_f16x4(v.w, w[6], w[7]);
+}
+
+// Position of K index i inside its octet under the order [0,4,1,5,2,6,3,7]
+// (index c < 4 at 2c, index c + 4 at 2c + 1).
+__host__ __device__ __forceinline__ int permute_octet(int i) {
+  const int o = i & 7;
+  return (i & ~7) | (o < 4 ? 2 * o : 2 * (o - 4) + 1);
 }
 
 // 16-byte chunk c of a 128-byte swizzled shared-memory row.
@@ -269,25 +256,62 @@ __device__ __forceinline__ uint4 sel4(bool p, const uint4& a, const uint4& b) {
   return make_uint4(p ? a.x : b.x, p ? a.y : b.y, p ? a.z : b.z, p ? a.w : b.w);
 }
 
-// MODE 1: gate/up GEMM (f16 operands: activations pre-scaled per row by a
-//         power of two), SiLU-and-mul epilogue -> act (bf16).
-// MODE 2: down GEMM (bf16 operands), router-weighted epilogue -> ypart.
+// uint4 -> f16, one 32-bit word w = 8 codes k0..k7 of one K octet (two per
+// byte, even index in the low nibble).  Word j of the result holds codes
+// (k_j, k_{j+4}): one mask places both under the f16 exponent of 1024, so
+// within every K octet the tensor-memory order is [0,4,1,5,2,6,3,7]; the
+// activations are laid out in the same order, which leaves the dot product
+// unchanged.  Each half becomes 1024 + q (exact); subtracting zz = 1024 + z
+// gives q - z exactly; multiplying by the f16 group scale ss rounds once.
+__device__ __forceinline__ void uint4x8_to_f16(uint32_t w, uint32_t zz, uint32_t ss, uint32_t* o) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t v = ((w >> (4 * j)) & 0x000F000Fu) | 0x64006400u;
+    uint32_t d;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(v), "r"(zz));
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[j]) : "r"(d), "r"(ss));
+  }
+}
+
+// Zero point and scale of one weight row at K position k (uint4), each
+// broadcast to both f16 halves.
+__device__ __forceinline__ void group_words(const TcParams& p, int wrow, int k, uint32_t& zz,
+                                            uint32_t& ss) {
+  const int g = k / p.gs;
+  uint32_t z = 8, sb = 0;  // past the row's end: scale 0 (the activations there are 0 too)
+  if (g < p.G) {
+    sb = __half_as_ushort(p.gscale[(int64_t)wrow * p.G + g]);
+    if (p.has_zp) z = (p.gzero[(int64_t)(wrow >> 1) * p.G + g] >> (4 * (wrow & 1))) & 15u;
+  }
+  zz = (0x6400u | z) * 0x00010001u;
+  ss = sb * 0x00010001u;
+}
+
+// Both GEMMs run f16 operands; their activation rows carry an exact
+// power-of-two scale (xinv undoes it in the epilogue).
+// MODE 1: gate/up GEMM, SiLU-and-mul epilogue -> act (bf16).
+// MODE 2: down GEMM on act (converted in place to scaled f16 in between),
+//         router-weighted epilogue -> ypart.
 //
-// Counters shared by all roles: `it` numbers weight stages (16 KB, kBK of K)
-// in schedule order, `st` numbers MMA steps (up to kG weight stages of one
-// work unit).  Ring slots are it % NA and st % ND.
-template <int MODE, int BN>
+// Counters shared by all roles: `it` numbers weight stages (16 KB: 128 K of
+// int8 or 256 K of uint4) in schedule order, `st` numbers MMA steps (256 K,
+// i.e. kGA weight stages, of one work unit).  Ring slots are it % NA and
+// st % ND.
+template <int MODE, int BITS, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const TcParams p) {
   using C = TileCfg<BN>;
+  // one weight stage = 128 rows x 128 bytes: 128 K of int8 or 256 K of uint4
+  constexpr int kEntryK = BITS == 8 ? 128 : 256;
+  constexpr int kGA = 256 / kEntryK;  // weight stages per MMA step (256 K)
+  constexpr int kEntryCols = kEntryK / 2;
   constexpr int NA = C::kAStagesSmem;
   constexpr int ND = C::kSteps;
   constexpr int kBBytesK = C::kBBytesK;
   constexpr int kBBytes = C::kBBytes;
   constexpr int kACol0 = C::kACol0;
-  constexpr bool kF16 = (MODE == 1);
-  constexpr uint32_t kIdesc = kF16 ? idesc_f16_f32(kTileM, BN) : idesc_bf16_f32(kTileM, BN);
+  constexpr uint32_t kIdesc = idesc_f16_f32(kTileM, BN);
   static_assert(NA <= 16, "ring sizes");
 
   extern __shared__ uint8_t smem_raw[];
@@ -358,9 +382,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* a = sA + s * kABytes;
           if (MODE == 1) {
             // {K, row in half, gate/up half, expert}: 64 gate rows then 64 up rows
-            tma_load_4d(a, &tmA, &ctl->fullA[s], ks * kBK, w.mt * 64, 0, w.e);
+            tma_load_4d(a, &tmA, &ctl->fullA[s], ks * 128, w.mt * 64, 0, w.e);
           } else {
-            tma_load_2d(a, &tmA, &ctl->fullA[s], ks * kBK, w.e * p.H + w.mt * kTileM);
+            tma_load_2d(a, &tmA, &ctl->fullA[s], ks * 128, w.e * p.H + w.mt * kTileM);
           }
         }
         __syncwarp();
@@ -385,19 +409,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Unit w = cta_unit<BN>(p, ulist, ui, u);
       const int ks0 = w.split * p.ksteps / p.splits;
       const int ks1 = (w.split + 1) * p.ksteps / p.splits;
-      for (int ks = ks0; ks < ks1; ks += kG, ++st) {
-        const int nk = min(kG, ks1 - ks);
+      for (int ks = ks0; ks < ks1; ks += kGA, ++st) {
+        const int nboxes = min(kGA, ks1 - ks) * kEntryK / 64;  // 64-K activation boxes
         const int d = st % ND;
         ok = warp_wait(&ctl->stepfree[d], ((st / ND) & 1) ^ 1, ctl, p.status, lane);
         if (!ok) break;
         if (lane == 0) {
-          mbar_arrive_expect_tx(&ctl->fullB[d], nk * kBBytesK);
+          mbar_arrive_expect_tx(&ctl->fullB[d], nboxes * (kBBytesK / 2));
           uint8_t* b = sB + d * kBBytes;
-          for (int j = 0; j < nk; ++j) {
-            const int kx = (ks + j) * kBK;
-            tma_load_2d(b + j * kBBytesK, &tmB, &ctl->fullB[d], kx, w.b * BN);
-            tma_load_2d(b + j * kBBytesK + kBBytesK / 2, &tmB, &ctl->fullB[d], kx + 64, w.b * BN);
-          }
+          for (int j = 0; j < nboxes; ++j)  // past K the box reads the fill value 0
+            tma_load_2d(b + j * (kBBytesK / 2), &tmB, &ctl->fullB[d], ks * kEntryK + 64 * j,
+                        w.b * BN);
         }
         __syncwarp();
       }
@@ -423,23 +445,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem + buf * BN;
-      for (int ks = ks0; ks < ks1; ks += kG, ++st) {
-        const int nk = min(kG, ks1 - ks);
+      for (int ks = ks0; ks < ks1; ks += kGA, ++st) {
+        const int nmma = min(kGA, ks1 - ks) * kEntryK / 16;  // K = 16 per MMA
         const int d = st % ND;
         ok = warp_wait(&ctl->afull[d], (st / ND) & 1, ctl, p.status, lane);
         if (!ok) break;
         tc_fence_after();
         if (lane == 0) {
-          const uint32_t b_base = smem_addr(sB + d * kBBytes);
+          // descriptor of the step's first K slice; the others differ only in
+          // the start-address field (address >> 4, no carry below 256 KB)
+          const uint64_t b_desc = smem_desc_k_sw128(smem_addr(sB + d * kBBytes));
           const uint32_t a_tmem = tmem + kACol0 + d * kAColsPerStep;
-          for (int j = 0; j < nk; ++j) {
+          const uint32_t acc0 = ks > ks0 ? 1u : 0u;
 #pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk) {
-              // K slices 0-3 in the first 64-column box, 4-7 in the second
-              const uint32_t b_addr =
-                  b_base + j * kBBytesK + (kk >> 2) * (kBBytesK / 2) + (kk & 3) * 32;
-              mma_ts(d_tmem, a_tmem + j * kAColsPerK + kk * 8, smem_desc_k_sw128(b_addr), kIdesc,
-                     (ks > ks0 || j > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 16; ++kk) {
+            if (kk < nmma) {
+              // four K slices of 16 per 64-K activation box
+              constexpr uint32_t kBox = kBBytesK / 2;
+              const uint64_t off = (uint64_t)(((kk >> 2) * kBox + (kk & 3) * 32) >> 4);
+              mma_ts(d_tmem, a_tmem + kk * 8, b_desc + off, kIdesc, kk > 0 ? 1u : acc0);
             }
           }
           mma_commit(&ctl->stepfree[d]);
@@ -458,10 +482,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp < kEpiWarp0) {
     // -------------------------------------------------- converters ----
-    // Per MMA step of this group: for each weight stage, wait for the int8
-    // tile, read this thread's row into registers and hand the shared-memory
-    // stage back at once; convert and write it into the step's tensor-memory
-    // A stage.  Then wait for the step's activations and tell the MMA issuer.
+    // Per MMA step of this group: for each weight stage, wait for the tile,
+    // read this thread's row into registers and hand the shared-memory stage
+    // back at once; convert (int8: exact; uint4: (q - z) * s per group) and
+    // write it into the step's tensor-memory A stage.  Then wait for the
+    // step's activations and tell the MMA issuer.
     const int grp = (warp - kConvWarp0) >> 2;  // takes the steps with st % kConvGroups == grp
     const int q = warp & 3;                    // tensor-memory lane quarter of this warp
     const int r = q * 32 + lane;
@@ -484,8 +509,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Unit w = cta_unit<BN>(p, ulist, ui, u);
       const int ks0 = w.split * p.ksteps / p.splits;
       const int ks1 = (w.split + 1) * p.ksteps / p.splits;
-      for (int ks = ks0; ks < ks1; ks += kG, ++st) {
-        const int nk = min(kG, ks1 - ks);
+      // this thread's weight row (uint4 group scales and zero points)
+      const int wrow = MODE == 1 ? w.e * 2 * p.I + ((lane & 1) ? p.I : 0) + w.mt * 64 + q * 16 + (lane >> 1)
+                                 : w.e * p.H + w.mt * kTileM + r;
+      for (int ks = ks0; ks < ks1; ks += kGA, ++st) {
+        const int nk = min(kGA, ks1 - ks);
         if (st % kConvGroups != grp) {
           it += nk;
           continue;
@@ -493,9 +521,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int d = st % ND;
         for (int j = 0; j < nk && ok; ++j, ++it) {
           const int sa = it % NA;
+          uint32_t zz[8], ss[8];  // uint4: per 32-K chunk, issued before the tile wait
+          if constexpr (BITS == 4) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) group_words(p, wrow, (ks + j) * kEntryK + 32 * c, zz[c], ss[c]);
+          }
           ok = warp_wait(&ctl->fullA[sa], (it / NA) & 1, ctl, p.status, lane);
           if (!ok) break;
-          const uint8_t* row = sA + sa * kABytes + srow * kBK;
+          const uint8_t* row = sA + sa * kABytes + srow * 128;
           uint4 x[8];  // x[c] holds logical chunk (c + rot) & 7
 #pragma unroll
           for (int c = 0; c < 8; ++c) x[c] = ld_chunk(row, (c + rot) & 7, sw);
@@ -507,15 +540,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after();
           }
+          const uint32_t tbase = tmem + tcol + d * kAColsPerStep + j * kEntryCols;
+          if constexpr (BITS == 8) {
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            uint32_t words[32];
+            for (int h = 0; h < 2; ++h) {
+              uint32_t words[32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              // logical chunk 4h + c sits in x[4h + c] (rot 0) or x[(4h + c + 4) & 7] (rot 4)
-              convert16<kF16>(sel4(rt, x[(4 * h + c + 4) & 7], x[4 * h + c]), &words[c * 8]);
+              for (int c = 0; c < 4; ++c) {
+                // logical chunk 4h + c sits in x[4h + c] (rot 0) or x[(4h + c + 4) & 7] (rot 4)
+                convert16(sel4(rt, x[(4 * h + c + 4) & 7], x[4 * h + c]), &words[c * 8]);
+              }
+              tmem_st32(tbase + h * 32, words);
             }
-            tmem_st32(tmem + tcol + d * kAColsPerStep + j * kAColsPerK + h * 32, words);
+          } else {
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              uint32_t words[32];
+#pragma unroll
+              for (int c2 = 0; c2 < 2; ++c2) {
+                const int c = 2 * h + c2;  // logical 16-byte chunk = 32 codes
+                const uint4 v = sel4(rt, x[(c + 4) & 7], x[c]);
+                uint4x8_to_f16(v.x, zz[c], ss[c], &words[c2 * 16 + 0]);
+                uint4x8_to_f16(v.y, zz[c], ss[c], &words[c2 * 16 + 4]);
+                uint4x8_to_f16(v.z, zz[c], ss[c], &words[c2 * 16 + 8]);
+                uint4x8_to_f16(v.w, zz[c], ss[c], &words[c2 * 16 + 12]);
+              }
+              tmem_st32(tbase + h * 32, words);
+            }
           }
         }
         if (!ok) break;
@@ -542,8 +593,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (MODE == 1) {
         const int i = q * 16 + (lane >> 1);
         const int wrow = w.e * 2 * p.I + ((lane & 1) ? p.I : 0) + w.mt * 64 + i;
-        const float sc = p.scale[wrow];
-        const int col = w.mt * 64 + i;
+        // int8: per-channel scale here; uint4: group scales were applied to A
+        const float sc = BITS == 8 ? p.scale[wrow] : 1.0f;
+        // uint4 runs the down GEMM in the K order [0,4,1,5,2,6,3,7] per octet
+        const int col = BITS == 8 ? w.mt * 64 + i : w.mt * 64 + permute_octet(i);
         for (int c0 = 0; c0 < BN; c0 += CH) {
           uint32_t v[CH];
           tmem_ld_cols<CH>(taddr + c0, v);
@@ -562,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         const int h = w.mt * kTileM + r;
-        const float sc = p.scale[w.e * p.H + h];
+        const float sc = BITS == 8 ? p.scale[w.e * p.H + h] : 1.0f;
         float* yp = p.ypart + (int64_t)w.split * p.S * p.H;
         for (int c0 = 0; c0 < BN; c0 += CH) {
           uint32_t v[CH];
@@ -571,7 +624,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int jj = 0; jj < CH; ++jj) {
             const int slot = p.sorted[w.b * BN + c0 + jj];
-            if (slot < p.S) yp[(int64_t)slot * p.H + h] = __uint_as_float(v[jj]) * sc * p.topk_w[slot];
+            if (slot < p.S)
+              yp[(int64_t)slot * p.H + h] =
+                  __uint_as_float(v[jj]) * sc * p.xinv[w.b * BN + c0 + jj] * p.topk_w[slot];
           }
         }
       }
@@ -594,6 +649,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // [2^14, 2^15): bf16 -> f16 is then exact except for elements below 2^-28
 // of the row maximum (f16 subnormals).  xinv[p] = 2^-e undoes it in the
 // epilogue.  Padding rows are zeros.
+template <bool PERM>
 __global__ void __launch_bounds__(128) gather_rows_f16(const __nv_bfloat16* __restrict__ x,
                                                        const int32_t* __restrict__ sorted,
                                                        const int32_t* __restrict__ num_padded,
@@ -604,19 +660,20 @@ __global__ void __launch_bounds__(128) gather_rows_f16(const __nv_bfloat16* __re
   const int p = blockIdx.x;
   if (p >= *num_padded) return;
   const int s = sorted[p];
-  uint2* dst = reinterpret_cast<uint2*>(xs + (int64_t)p * H);  // 4 halves per uint2
-  const int n = H / 4;
+  uint4* dst = reinterpret_cast<uint4*>(xs + (int64_t)p * H);  // one K octet per uint4
+  const int n = H / 8;
   if (s >= S) {
-    for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = make_uint2(0, 0);
+    for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = make_uint4(0, 0, 0, 0);
     if (threadIdx.x == 0) xinv[p] = 1.0f;
     return;
   }
-  const uint2* src = reinterpret_cast<const uint2*>(x + (int64_t)(s / k) * H);
+  const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)(s / k) * H);
   float m = 0.0f;
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    const uint2 v = src[i];
-    m = fmaxf(m, fmaxf(fmaxf(fabsf(mq::bf16_lo(v.x)), fabsf(mq::bf16_hi(v.x))),
-                       fmaxf(fabsf(mq::bf16_lo(v.y)), fabsf(mq::bf16_hi(v.y)))));
+    const uint4 v = src[i];
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) m = fmaxf(m, fmaxf(fabsf(mq::bf16_lo(u[j])), fabsf(mq::bf16_hi(u[j]))));
   }
 #pragma unroll
   for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -629,13 +686,66 @@ __global__ void __launch_bounds__(128) gather_rows_f16(const __nv_bfloat16* __re
   e = max(-120, min(120, e));
   const float scale = ldexpf(1.0f, e);
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    const uint2 v = src[i];
-    const __half2 a = __floats2half2_rn(mq::bf16_lo(v.x) * scale, mq::bf16_hi(v.x) * scale);
-    const __half2 b = __floats2half2_rn(mq::bf16_lo(v.y) * scale, mq::bf16_hi(v.y) * scale);
-    uint2 o;
-    o.x = *reinterpret_cast<const uint32_t*>(&a);
-    o.y = *reinterpret_cast<const uint32_t*>(&b);
-    dst[i] = o;
+    const uint4 v = src[i];
+    float f[8];
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      f[2 * j] = mq::bf16_lo(u[j]) * scale;
+      f[2 * j + 1] = mq::bf16_hi(u[j]) * scale;
+    }
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      // natural order: pair (2j, 2j+1); octet order [0,4,1,5,2,6,3,7]: pair (j, j+4)
+      const __half2 h = PERM ? __floats2half2_rn(f[j], f[j + 4]) : __floats2half2_rn(f[2 * j], f[2 * j + 1]);
+      o[j] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  if (threadIdx.x == 0) xinv[p] = ldexpf(1.0f, -e);
+}
+
+// act rows [0, num_padded) converted in place from bf16 to f16, each row
+// scaled by a power of two 2^e so that its largest magnitude lands in
+// [2^14, 2^15) (exact, as in gather_rows_f16); xinv[p] = 2^-e.
+__global__ void __launch_bounds__(256) act_rows_to_f16(uint16_t* act, const int32_t* num_padded,
+                                                       int I, float* __restrict__ xinv) {
+  __shared__ float wmax[8];
+  const int p = blockIdx.x;
+  if (p >= *num_padded) return;
+  uint4* row = reinterpret_cast<uint4*>(act + (int64_t)p * I);
+  const int n = I / 8;
+  float m = 0.0f;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const uint4 v = row[i];
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) m = fmaxf(m, fmaxf(fabsf(mq::bf16_lo(u[j])), fabsf(mq::bf16_hi(u[j]))));
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
+  __syncthreads();
+  m = 0.0f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) m = fmaxf(m, wmax[w]);
+  int ex = 0;
+  if (m > 0.0f) frexpf(m, &ex);
+  int e = 15 - ex;
+  e = max(-120, min(120, e));
+  const float scale = ldexpf(1.0f, e);
+  // each thread rewrites exactly the vectors it read: in place is safe
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const uint4 v = row[i];
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const __half2 h = __floats2half2_rn(mq::bf16_lo(u[j]) * scale, mq::bf16_hi(u[j]) * scale);
+      o[j] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    row[i] = make_uint4(o[0], o[1], o[2], o[3]);
   }
   if (threadIdx.x == 0) xinv[p] = ldexpf(1.0f, -e);
 }
@@ -711,11 +821,11 @@ constexpr size_t smem_for() {
   return need < 120 * 1024 ? 120 * 1024 : need;
 }
 
-template <int MODE, int BN>
+template <int MODE, int BITS, int BN>
 cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const TcParams& p,
                         int max_units, cudaStream_t st) {
   constexpr size_t smem = smem_for<BN>();
-  auto kern = moe_gemm_tc<MODE, BN>;
+  auto kern = moe_gemm_tc<MODE, BITS, BN>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   const int sms = tc_num_sms();
@@ -725,21 +835,25 @@ cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const TcPa
   return cudaGetLastError();
 }
 
-template <int MODE>
+template <int MODE, int BITS>
 cudaError_t launch_gemm_bn(int bn, const CUtensorMap& ta, const CUtensorMap& tb,
                            const TcParams& p, int max_units, cudaStream_t st) {
   switch (bn) {
-    case 16: return launch_gemm<MODE, 16>(ta, tb, p, max_units, st);
-    case 32: return launch_gemm<MODE, 32>(ta, tb, p, max_units, st);
-    case 64: return launch_gemm<MODE, 64>(ta, tb, p, max_units, st);
-    case 128: return launch_gemm<MODE, 128>(ta, tb, p, max_units, st);
+    case 16: return launch_gemm<MODE, BITS, 16>(ta, tb, p, max_units, st);
+    case 32: return launch_gemm<MODE, BITS, 32>(ta, tb, p, max_units, st);
+    case 64: return launch_gemm<MODE, BITS, 64>(ta, tb, p, max_units, st);
+    case 128: return launch_gemm<MODE, BITS, 128>(ta, tb, p, max_units, st);
     default: return cudaErrorInvalidValue;
   }
 }
 
+// K elements per 16 KB weight stage, and stages per row of length K.
+inline int entry_k(int bits) { return bits == 8 ? 128 : 256; }
+inline int entries(int K, int bits) { return (K + entry_k(bits) - 1) / entry_k(bits); }
+
 }  // namespace
 
-TcPlan tc_plan(int T, int H, int I, int E, int k) {
+TcPlan tc_plan(int T, int H, int I, int E, int k, int bits) {
   TcPlan pl;
   const int64_t S = (int64_t)T * k;
   const int64_t per_expert = (S + E - 1) / E;
@@ -749,14 +863,15 @@ TcPlan tc_plan(int T, int H, int I, int E, int k) {
   pl.bn = bn;
   // K splits of the down GEMM: enough work units (about 600, four per SM)
   // to keep every SM streaming weights; a fixed target keeps the workspace
-  // size independent of the device.
+  // size independent of the device.  A split keeps at least two MMA steps.
   const int64_t live = S < E ? S : E;
   const int64_t blocks = live > S / bn ? live : S / bn;
   const int mt2 = H / kTileM;
-  const int ksteps2 = I / kBK;
+  const int steps2 = (I + 255) / 256;
   int splits = 1;
-  while (splits < 8 && blocks * mt2 * splits < 600 && ksteps2 / (splits * 2) >= 2) splits *= 2;
+  while (splits < 8 && blocks * mt2 * splits < 600 && steps2 / (splits * 2) >= 2) splits *= 2;
   pl.splits = splits;
+  (void)bits;
   return pl;
 }
 
@@ -772,21 +887,48 @@ int tc_num_sms() {
 
 cudaError_t launch_gather_rows(const MoeArgs& a, void* xs, float* xinv, cudaStream_t st) {
   if (a.cap == 0) return cudaSuccess;
-  gather_rows_f16<<<(unsigned)a.cap, 128, 0, st>>>(a.x, a.sorted, a.num_padded, a.k, a.T * a.k,
-                                                   a.H, static_cast<__half*>(xs), xinv);
+  if (a.bits == 8)
+    gather_rows_f16<false><<<(unsigned)a.cap, 128, 0, st>>>(
+        a.x, a.sorted, a.num_padded, a.k, a.T * a.k, a.H, static_cast<__half*>(xs), xinv);
+  else
+    gather_rows_f16<true><<<(unsigned)a.cap, 128, 0, st>>>(
+        a.x, a.sorted, a.num_padded, a.k, a.T * a.k, a.H, static_cast<__half*>(xs), xinv);
   return cudaGetLastError();
 }
+
+namespace {
+
+void common_params(TcParams& p, const MoeArgs& a) {
+  p.H = a.H; p.I = a.I; p.E = a.E; p.k = a.k; p.S = a.T * a.k;
+  p.sorted = a.sorted; p.block_expert = a.block_expert; p.offsets = a.offsets;
+  p.num_padded = a.num_padded;
+  p.topk_w = a.topk_w;
+  p.status = a.status;
+  p.gs = a.bits == 8 ? 0 : a.group_size;
+  p.has_zp = a.has_zp;
+  p.act = nullptr;
+  p.ypart = nullptr;
+  p.xinv = nullptr;
+  p.scale = nullptr;
+  p.gscale = nullptr;
+  p.gzero = nullptr;
+  p.G = 0;
+}
+
+}  // namespace
 
 cudaError_t launch_gemm1_tc(const MoeArgs& a, const TcPlan& pl, const void* xs,
                             const float* xinv, cudaStream_t st) {
   cudaError_t err = get_encoder();
   if (err != cudaSuccess) return err;
+  // weight rows in bytes: H int8 codes or H/2 bytes of packed uint4 codes
+  const uint64_t rb = a.bits == 8 ? (uint64_t)a.H : (uint64_t)a.H / 2;
   CUtensorMap ta, tb;
   {
-    // w13 int8 [E, 2, I, H] viewed as {H, I, 2, E}: one box = 64 gate rows + 64 up rows
-    const cuuint64_t dims[4] = {(cuuint64_t)a.H, (cuuint64_t)a.I, 2, (cuuint64_t)a.E};
-    const cuuint64_t strides[3] = {(cuuint64_t)a.H, (cuuint64_t)a.I * a.H, (cuuint64_t)2 * a.I * a.H};
-    const cuuint32_t box[4] = {kBK, 64, 2, 1};
+    // w13 [E, 2, I, rb] viewed as {rb, I, 2, E}: one box = 64 gate rows + 64 up rows
+    const cuuint64_t dims[4] = {rb, (cuuint64_t)a.I, 2, (cuuint64_t)a.E};
+    const cuuint64_t strides[3] = {rb, (cuuint64_t)a.I * rb, (cuuint64_t)2 * a.I * rb};
+    const cuuint32_t box[4] = {128, 64, 2, 1};
     err = make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, a.w13, dims, strides, box,
                    CU_TENSOR_MAP_SWIZZLE_128B);
     if (err != cudaSuccess) return err;
@@ -800,30 +942,42 @@ cudaError_t launch_gemm1_tc(const MoeArgs& a, const TcPlan& pl, const void* xs,
     if (err != cudaSuccess) return err;
   }
   TcParams p;
-  p.H = a.H; p.I = a.I; p.E = a.E; p.k = a.k; p.S = a.T * a.k;
-  p.ksteps = a.H / kBK;
+  common_params(p, a);
+  p.ksteps = entries(a.H, a.bits);
   p.MT = a.I / 64;
   p.splits = 1;
-  p.sorted = a.sorted; p.block_expert = a.block_expert; p.offsets = a.offsets;
-  p.num_padded = a.num_padded;
-  p.scale = static_cast<const float*>(a.s13);
-  p.topk_w = a.topk_w;
+  if (a.bits == 8) {
+    p.scale = static_cast<const float*>(a.s13);
+  } else {
+    p.gscale = static_cast<const __half*>(a.s13);
+    p.gzero = a.z13;
+    p.G = a.H / a.group_size;
+  }
   p.act = a.act;
-  p.ypart = nullptr;
   p.xinv = xinv;
-  p.status = a.status;
   const int64_t units = (a.cap / pl.bn) * (int64_t)p.MT;
-  return launch_gemm_bn<1>(pl.bn, ta, tb, p, (int)(units < (1 << 30) ? units : (1 << 30)), st);
+  const int mu = (int)(units < (1 << 30) ? units : (1 << 30));
+  return a.bits == 8 ? launch_gemm_bn<1, 8>(pl.bn, ta, tb, p, mu, st)
+                     : launch_gemm_bn<1, 4>(pl.bn, ta, tb, p, mu, st);
 }
 
-cudaError_t launch_gemm2_tc(const MoeArgs& a, const TcPlan& pl, float* ypart, cudaStream_t st) {
+cudaError_t launch_act_to_f16(const MoeArgs& a, float* act_inv, cudaStream_t st) {
+  if (a.cap == 0) return cudaSuccess;
+  act_rows_to_f16<<<(unsigned)a.cap, 256, 0, st>>>(reinterpret_cast<uint16_t*>(a.act), a.num_padded,
+                                                    a.I, act_inv);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm2_tc(const MoeArgs& a, const TcPlan& pl, const float* act_inv,
+                            float* ypart, cudaStream_t st) {
   cudaError_t err = get_encoder();
   if (err != cudaSuccess) return err;
+  const uint64_t rb = a.bits == 8 ? (uint64_t)a.I : (uint64_t)a.I / 2;
   CUtensorMap ta, tb;
   {
-    const cuuint64_t dims[2] = {(cuuint64_t)a.I, (cuuint64_t)a.E * a.H};
-    const cuuint64_t strides[1] = {(cuuint64_t)a.I};
-    const cuuint32_t box[2] = {kBK, kTileM};
+    const cuuint64_t dims[2] = {rb, (cuuint64_t)a.E * a.H};
+    const cuuint64_t strides[1] = {rb};
+    const cuuint32_t box[2] = {128, kTileM};
     err = make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.w2, dims, strides, box,
                    CU_TENSOR_MAP_SWIZZLE_128B);
     if (err != cudaSuccess) return err;
@@ -832,25 +986,28 @@ cudaError_t launch_gemm2_tc(const MoeArgs& a, const TcPlan& pl, float* ypart, cu
     const cuuint64_t dims[2] = {(cuuint64_t)a.I, (cuuint64_t)a.cap};
     const cuuint64_t strides[1] = {(cuuint64_t)a.I * 2};
     const cuuint32_t box[2] = {64, (cuuint32_t)pl.bn};
-    err = make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.act, dims, strides, box,
+    err = make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.act, dims, strides, box,
                    CU_TENSOR_MAP_SWIZZLE_128B);
     if (err != cudaSuccess) return err;
   }
   TcParams p;
-  p.H = a.H; p.I = a.I; p.E = a.E; p.k = a.k; p.S = a.T * a.k;
-  p.ksteps = a.I / kBK;
+  common_params(p, a);
+  p.ksteps = entries(a.I, a.bits);
   p.MT = a.H / kTileM;
   p.splits = pl.splits;
-  p.sorted = a.sorted; p.block_expert = a.block_expert; p.offsets = a.offsets;
-  p.num_padded = a.num_padded;
-  p.scale = static_cast<const float*>(a.s2);
-  p.topk_w = a.topk_w;
-  p.act = nullptr;
+  if (a.bits == 8) {
+    p.scale = static_cast<const float*>(a.s2);
+  } else {
+    p.gscale = static_cast<const __half*>(a.s2);
+    p.gzero = a.z2;
+    p.G = a.I / a.group_size;
+  }
   p.ypart = ypart;
-  p.xinv = nullptr;
-  p.status = a.status;
+  p.xinv = act_inv;
   const int64_t units = (a.cap / pl.bn) * (int64_t)p.MT * p.splits;
-  return launch_gemm_bn<2>(pl.bn, ta, tb, p, (int)(units < (1 << 30) ? units : (1 << 30)), st);
+  const int mu = (int)(units < (1 << 30) ? units : (1 << 30));
+  return a.bits == 8 ? launch_gemm_bn<2, 8>(pl.bn, ta, tb, p, mu, st)
+                     : launch_gemm_bn<2, 4>(pl.bn, ta, tb, p, mu, st);
 }
 
 cudaError_t launch_combine_splits(const MoeArgs& a, const float* ypart, int splits,
