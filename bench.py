@@ -74,22 +74,32 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(x, world):
+def _reduce(x, world, op, device):
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=op)
     return float(t.item())
 
 
-def sum_over_ranks(x, world):
-    if world == 1:
-        return x
+def max_over_ranks(x, world, device="cuda"):
+    """Slowest rank's value (the job's time is the slowest replica's)."""
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.SUM)
-    return float(t.item())
+    return _reduce(x, world, dist.ReduceOp.MAX, device)
+
+
+def sum_over_ranks(x, world, device="cuda"):
+    """Whole-job total (tokens processed by all replicas)."""
+    import torch.distributed as dist
+    return _reduce(x, world, dist.ReduceOp.SUM, device)
+
+
+def job_throughput(local_tokens, local_ms, world, device="cuda"):
+    """Weak-scaling throughput of N independent replicas: all ranks' tokens
+    over the slowest rank's time."""
+    ms = max_over_ranks(local_ms, world, device)
+    return sum_over_ranks(local_tokens, world, device) / (ms / 1e3), ms
 
 
 def measured_peaks():
@@ -394,9 +404,8 @@ def main():
     clk = clocks.stop()
     assert mq.mq_device_status() == 0, "device status flagged during the timed run"
 
-    ms_max = max_over_ranks(ms, world)
+    value, ms_max = job_throughput(T * args.steps, ms, world)
     tokens_all = sum_over_ranks(T * args.steps, world)
-    value = tokens_all / (ms_max / 1e3)
 
     # per-kernel device times (separate pass of the same steps, events on the
     # launching stream)
