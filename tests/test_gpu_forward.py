@@ -124,6 +124,42 @@ def test_forward_w4a16_full_sampled():
     assert _run(layer, 32, seed=3, tokens=[0, 7, 31]) <= FWD_TOL
 
 
+@pytest.mark.parametrize("name,T", [("mixtral_decode", 64), ("fine", 64), ("w4a16", 32),
+                                    ("mixtral_prefill", 1024)])
+def test_forward_is_deterministic(name, T):
+    """No atomics anywhere: repeated calls give bitwise identical outputs
+    (a check that no kernel reads data before it has landed)."""
+    layer = Layer(W[name], seed=0)
+    layer.free_bf16()
+    x, lg = inputs(layer.wl, T, seed=4)
+    tw, tid = mq.moe_topk_route(lg, layer.k, True)
+    outs = [layer.forward(x, tw, tid).clone() for _ in range(4)]
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+
+
+@pytest.mark.parametrize("name,T", [("mixtral_decode", 64), ("fine", 256), ("w4a16", 256),
+                                    ("mixtral_prefill", 1024)])
+def test_forward_token_permutation_is_exact(name, T):
+    """Each token's output depends only on its own row: every GEMM column is
+    an independent dot product in a fixed K order, and the combine sums a
+    token's slots in a fixed order.  Permuting the batch therefore permutes
+    the output bitwise, although the tokens land in other blocks and block
+    positions.  (Any read of a stage before its data landed breaks this.)"""
+    layer = Layer(W[name], seed=0)
+    layer.free_bf16()
+    x, lg = inputs(layer.wl, T, seed=6)
+    perm = torch.from_numpy(np.random.default_rng(T).permutation(T)).cuda()
+    tw, tid = mq.moe_topk_route(lg, layer.k, True)
+    out = layer.forward(x, tw, tid)
+    tw_p, tid_p = mq.moe_topk_route(lg[perm].contiguous(), layer.k, True)
+    out_p = layer.forward(x[perm].contiguous(), tw_p, tid_p)
+    torch.cuda.synchronize()
+    assert mq.mq_device_status() == 0
+    assert torch.equal(out_p, out[perm])
+
+
 def test_forward_mixtral_decode_sampled():
     """Mixtral-shaped layer at T=64, the benchmarked decode size: two sampled
     tokens, 512 sampled output columns."""

@@ -293,10 +293,15 @@ __device__ __forceinline__ void group_words(const TcParams& p, int wrow, int k, 
 // MODE 2: down GEMM on act (converted in place to scaled f16 in between),
 //         router-weighted epilogue -> ypart.
 //
-// Counters shared by all roles: `it` numbers weight stages (16 KB: 128 K of
-// int8 or 256 K of uint4) in schedule order, `st` numbers MMA steps (256 K,
-// i.e. kGA weight stages, of one work unit).  Ring slots are it % NA and
-// st % ND.
+// `st` numbers MMA steps (256 K, i.e. kGA weight stages of 16 KB, of one
+// work unit) in schedule order; step st belongs to converter group
+// st % kConvGroups and uses tensor-memory / activation slot st % ND.  The
+// weight ring is split into one half per converter group, each with its own
+// count of weight stages, so that every mbarrier of a ring slot is waited on
+// by one sequential consumer only.  (A slot shared by two consumers breaks
+// the phase-parity wait: a consumer can reach the slot's next use while the
+// other consumer's fill is still in flight, and then sees the barrier one
+// phase behind, which has the parity it waits for.)
 template <int MODE, int BITS, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -307,6 +312,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kGA = 256 / kEntryK;  // weight stages per MMA step (256 K)
   constexpr int kEntryCols = kEntryK / 2;
   constexpr int NA = C::kAStagesSmem;
+  constexpr int NAG = NA / kConvGroups;  // weight-ring slots per converter group
+  static_assert(kConvGroups == 2 && NAG >= 2, "two converter groups, two slots each");
   constexpr int ND = C::kSteps;
   constexpr int kBBytesK = C::kBBytesK;
   constexpr int kBBytes = C::kBBytes;
@@ -367,36 +374,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The whole warp walks the schedule (so it stays converged); lane 0
     // issues the copies.
     if (lane == 0) tma_prefetch_desc(&tmA);
-    int it = 0;
+    int st = 0;
+    int lit0 = 0, lit1 = 0;  // weight stages issued into each group's half of the ring
     bool ok = true;
     for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
       const Unit w = cta_unit<BN>(p, ulist, ui, u);
       const int ks0 = w.split * p.ksteps / p.splits;
       const int ks1 = (w.split + 1) * p.ksteps / p.splits;
-      for (int ks = ks0; ks < ks1; ++ks, ++it) {
-        const int s = it % NA;
-        ok = warp_wait(&ctl->emptyA[s], ((it / NA) & 1) ^ 1, ctl, p.status, lane);
-        if (!ok) break;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&ctl->fullA[s], kABytes);
-          uint8_t* a = sA + s * kABytes;
-          if (MODE == 1) {
-            // {K, row in half, gate/up half, expert}: 64 gate rows then 64 up rows
-            tma_load_4d(a, &tmA, &ctl->fullA[s], ks * 128, w.mt * 64, 0, w.e);
-          } else {
-            tma_load_2d(a, &tmA, &ctl->fullA[s], ks * 128, w.e * p.H + w.mt * kTileM);
+      for (int ks = ks0; ks < ks1 && ok; ks += kGA, ++st) {
+        const int g = st % kConvGroups;
+        const int nk = min(kGA, ks1 - ks);
+        for (int j = 0; j < nk; ++j) {
+          const int n = g ? lit1 : lit0;
+          const int s = g * NAG + n % NAG;
+          ok = warp_wait(&ctl->emptyA[s], ((n / NAG) & 1) ^ 1, ctl, p.status, lane);
+          if (!ok) break;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&ctl->fullA[s], kABytes);
+            uint8_t* a = sA + s * kABytes;
+            if (MODE == 1) {
+              // {K, row in half, gate/up half, expert}: 64 gate rows then 64 up rows
+              tma_load_4d(a, &tmA, &ctl->fullA[s], (ks + j) * 128, w.mt * 64, 0, w.e);
+            } else {
+              tma_load_2d(a, &tmA, &ctl->fullA[s], (ks + j) * 128, w.e * p.H + w.mt * kTileM);
+            }
           }
+          __syncwarp();
+          if (g) ++lit1; else ++lit0;
         }
-        __syncwarp();
       }
     }
     // Never leave with copies in flight: wait for the last load issued into
-    // each stage (iterations it-1, it-2, ...).
+    // each slot of both halves.
     if (lane == 0) {
-      const int n = it < NA ? it : NA;
-      for (int d = 1; d <= n; ++d) {
-        const int j = it - d;
-        wait_drain(&ctl->fullA[j % NA], (j / NA) & 1);
+      for (int g = 0; g < kConvGroups; ++g) {
+        const int n = g ? lit1 : lit0;
+        for (int d = 1; d <= (n < NAG ? n : NAG); ++d) {
+          const int j = n - d;
+          wait_drain(&ctl->fullA[g * NAG + j % NAG], (j / NAG) & 1);
+        }
       }
     }
     __syncwarp();
@@ -448,7 +464,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int ks = ks0; ks < ks1; ks += kGA, ++st) {
         const int nmma = min(kGA, ks1 - ks) * kEntryK / 16;  // K = 16 per MMA
         const int d = st % ND;
-        ok = warp_wait(&ctl->afull[d], (st / ND) & 1, ctl, p.status, lane);
+        ok = warp_wait(&ctl->afull[d], (st / ND) & 1, ctl, p.status, lane) &&
+             warp_wait(&ctl->fullB[d], (st / ND) & 1, ctl, p.status, lane);
         if (!ok) break;
         tc_fence_after();
         if (lane == 0) {
@@ -482,11 +499,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp < kEpiWarp0) {
     // -------------------------------------------------- converters ----
-    // Per MMA step of this group: for each weight stage, wait for the tile,
-    // read this thread's row into registers and hand the shared-memory stage
-    // back at once; convert (int8: exact; uint4: (q - z) * s per group) and
-    // write it into the step's tensor-memory A stage.  Then wait for the
-    // step's activations and tell the MMA issuer.
+    // Per MMA step of this group: for each weight stage, wait for the tile
+    // in this group's half of the ring, read this thread's row into
+    // registers, convert it (int8: exact; uint4: (q - z) * s per group),
+    // write it into the step's tensor-memory A stage and hand the slot back.
+    // Then tell the MMA issuer.
     const int grp = (warp - kConvWarp0) >> 2;  // takes the steps with st % kConvGroups == grp
     const int q = warp & 3;                    // tensor-memory lane quarter of this warp
     const int r = q * 32 + lane;
@@ -503,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sw = srow & 7;  // 128-byte swizzle phase of this row
     const uint32_t tcol = ((uint32_t)(q * 32) << 16) + kACol0;
     const bool rt = rot != 0;
-    int it = 0, st = 0;
+    int lit = 0, st = 0;  // lit: weight stages consumed by this group
     bool ok = true;
     for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
       const Unit w = cta_unit<BN>(p, ulist, ui, u);
@@ -514,26 +531,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  : w.e * p.H + w.mt * kTileM + r;
       for (int ks = ks0; ks < ks1; ks += kGA, ++st) {
         const int nk = min(kGA, ks1 - ks);
-        if (st % kConvGroups != grp) {
-          it += nk;
-          continue;
-        }
+        if (st % kConvGroups != grp) continue;
         const int d = st % ND;
-        for (int j = 0; j < nk && ok; ++j, ++it) {
-          const int sa = it % NA;
+        for (int j = 0; j < nk && ok; ++j, ++lit) {
+          const int sa = grp * NAG + lit % NAG;
           uint32_t zz[8], ss[8];  // uint4: per 32-K chunk, issued before the tile wait
           if constexpr (BITS == 4) {
 #pragma unroll
             for (int c = 0; c < 8; ++c) group_words(p, wrow, (ks + j) * kEntryK + 32 * c, zz[c], ss[c]);
           }
-          ok = warp_wait(&ctl->fullA[sa], (it / NA) & 1, ctl, p.status, lane);
+          ok = warp_wait(&ctl->fullA[sa], (lit / NAG) & 1, ctl, p.status, lane);
           if (!ok) break;
           const uint8_t* row = sA + sa * kABytes + srow * 128;
           uint4 x[8];  // x[c] holds logical chunk (c + rot) & 7
 #pragma unroll
           for (int c = 0; c < 8; ++c) x[c] = ld_chunk(row, (c + rot) & 7, sw);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&ctl->emptyA[sa]);
           if (j == 0) {
             // the MMAs that last read this tensor-memory stage must be done
             ok = warp_wait(&ctl->stepfree[d], ((st / ND) & 1) ^ 1, ctl, p.status, lane);
@@ -568,9 +580,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               tmem_st32(tbase + h * 32, words);
             }
           }
+          // The slot goes back only now that the loaded registers have been
+          // consumed: a shared-memory load that has issued may still be
+          // reading, and the next fill of the slot (TMA) would overtake it.
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl->emptyA[sa]);
         }
-        if (!ok) break;
-        ok = warp_wait(&ctl->fullB[d], (st / ND) & 1, ctl, p.status, lane);
         if (!ok) break;
         tmem_st_wait();
         tc_fence_before();
@@ -582,7 +597,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------- epilogue ----
     const int q = warp & 3;
     const int r = q * 32 + lane;
+    const bool odd = (lane & 1) != 0;
     constexpr int CH = BN < 32 ? BN : 32;  // accumulator columns per tcgen05.ld
+    constexpr int HALF = CH / 2;
     int t = 0;
     for (int u = blockIdx.x; u < total; u += gridDim.x, ++t) {
       const Unit w = cta_unit<BN>(p, ulist, t, u);
@@ -591,26 +608,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + buf * BN;
       if (MODE == 1) {
+        // lanes (2i, 2i+1) hold gate row i and up row i; per pair of
+        // columns (jj, jj + HALF) the even lane finishes column jj and the
+        // odd lane column jj + HALF, after one exchange
         const int i = q * 16 + (lane >> 1);
-        const int wrow = w.e * 2 * p.I + ((lane & 1) ? p.I : 0) + w.mt * 64 + i;
+        const int wrow = w.e * 2 * p.I + (odd ? p.I : 0) + w.mt * 64 + i;
         // int8: per-channel scale here; uint4: group scales were applied to A
         const float sc = BITS == 8 ? p.scale[wrow] : 1.0f;
         // uint4 runs the down GEMM in the K order [0,4,1,5,2,6,3,7] per octet
-        const int col = BITS == 8 ? w.mt * 64 + i : w.mt * 64 + permute_octet(i);
+        const int col = w.mt * 64 + q * 16 + (BITS == 8 ? (lane >> 1) : permute_octet(lane >> 1));
         for (int c0 = 0; c0 < BN; c0 += CH) {
           uint32_t v[CH];
-          tmem_ld_cols<CH>(taddr + c0, v);
-          tmem_ld_wait();
+          const float xv = lane < CH ? p.xinv[w.b * BN + c0 + lane] : 1.0f;
+          tmem_ld_cols_sync<CH>(taddr + c0, v);
 #pragma unroll
-          for (int jj = 0; jj < CH; ++jj) {
-            const int prow = w.b * BN + c0 + jj;
-            const float own = __uint_as_float(v[jj]) * sc * p.xinv[prow];
-            const float other = __shfl_xor_sync(0xffffffffu, own, 1);
-            const float g = (lane & 1) ? other : own;
-            const float up = (lane & 1) ? own : other;
-            // even lane stores the first half of the columns, odd lane the rest
-            if ((jj >= CH / 2) == ((lane & 1) != 0))
-              p.act[(int64_t)prow * p.I + col] = __float2bfloat16_rn(mq::silu_mul(g, up));
+          for (int jj = 0; jj < HALF; ++jj) {
+            const float lo = __uint_as_float(v[jj]) * sc;         // own row, column jj
+            const float hi = __uint_as_float(v[jj + HALF]) * sc;  // own row, column jj + HALF
+            const float got = __shfl_xor_sync(0xffffffffu, odd ? lo : hi, 1);
+            const int cj = odd ? jj + HALF : jj;
+            const float xs = __shfl_sync(0xffffffffu, xv, cj);
+            const float g = (odd ? got : lo) * xs;
+            const float up = (odd ? hi : got) * xs;
+            const float a = __fdividef(g * up, 1.0f + __expf(-g));  // silu(g) * up
+            p.act[(int64_t)(w.b * BN + c0 + cj) * p.I + col] = __float2bfloat16_rn(a);
           }
         }
       } else {
@@ -619,14 +640,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         float* yp = p.ypart + (int64_t)w.split * p.S * p.H;
         for (int c0 = 0; c0 < BN; c0 += CH) {
           uint32_t v[CH];
-          tmem_ld_cols<CH>(taddr + c0, v);
-          tmem_ld_wait();
+          // per column: its slot and the factor (act row scale x router weight)
+          int slot = p.S;
+          float f = 0.0f;
+          if (lane < CH) {
+            const int prow = w.b * BN + c0 + lane;
+            slot = p.sorted[prow];
+            if (slot < p.S) f = p.xinv[prow] * p.topk_w[slot];
+          }
+          tmem_ld_cols_sync<CH>(taddr + c0, v);
 #pragma unroll
           for (int jj = 0; jj < CH; ++jj) {
-            const int slot = p.sorted[w.b * BN + c0 + jj];
-            if (slot < p.S)
-              yp[(int64_t)slot * p.H + h] =
-                  __uint_as_float(v[jj]) * sc * p.xinv[w.b * BN + c0 + jj] * p.topk_w[slot];
+            const int sj = __shfl_sync(0xffffffffu, slot, jj);
+            const float fj = __shfl_sync(0xffffffffu, f, jj);
+            if (sj < p.S) yp[(int64_t)sj * p.H + h] = __uint_as_float(v[jj]) * sc * fj;
           }
         }
       }
