@@ -295,13 +295,14 @@ __device__ __forceinline__ void group_words(const TcParams& p, int wrow, int k, 
 //
 // `st` numbers MMA steps (256 K, i.e. kGA weight stages of 16 KB, of one
 // work unit) in schedule order; step st belongs to converter group
-// st % kConvGroups and uses tensor-memory / activation slot st % ND.  The
-// weight ring is split into one half per converter group, each with its own
-// count of weight stages, so that every mbarrier of a ring slot is waited on
-// by one sequential consumer only.  (A slot shared by two consumers breaks
-// the phase-parity wait: a consumer can reach the slot's next use while the
-// other consumer's fill is still in flight, and then sees the barrier one
-// phase behind, which has the parity it waits for.)
+// st % kConvGroups and uses tensor-memory / activation slot st % ND.
+//
+// A phase-parity wait is exact only if the waiter knows that the barrier's
+// previous phase has completed (a barrier two phases behind shows the parity
+// being waited for).  Hence: the weight ring is split into one half per
+// converter group, each with its own count of weight stages (one sequential
+// consumer per slot); a converter waits for its step's activations only
+// after it has seen the MMAs of the slot's previous use complete.
 template <int MODE, int BITS, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -450,49 +451,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------- MMA issuer ----
-    int st = 0, t = 0;
-    bool ok = true;
-    for (int u = blockIdx.x; u < total && ok; u += gridDim.x, ++t) {
-      const Unit w = cta_unit<BN>(p, ulist, t, u);
-      const int ks0 = w.split * p.ksteps / p.splits;
-      const int ks1 = (w.split + 1) * p.ksteps / p.splits;
-      const int buf = t & 1;
-      ok = warp_wait(&ctl->accempty[buf], ((t >> 1) & 1) ^ 1, ctl, p.status, lane);
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t d_tmem = tmem + buf * BN;
-      for (int ks = ks0; ks < ks1; ks += kGA, ++st) {
-        const int nmma = min(kGA, ks1 - ks) * kEntryK / 16;  // K = 16 per MMA
-        const int d = st % ND;
-        ok = warp_wait(&ctl->afull[d], (st / ND) & 1, ctl, p.status, lane) &&
-             warp_wait(&ctl->fullB[d], (st / ND) & 1, ctl, p.status, lane);
+    // One thread runs this loop: it alone waits, issues and commits, so the
+    // rest of the warp has nothing to agree on.  Per 256-K step: one wait
+    // (the converted A stage; the converters have also seen the step's
+    // activations land), the 16 MMAs from one asm statement, one commit.
+    if (lane == 0) {
+      constexpr uint32_t kBoxD = (uint32_t)(kBBytesK / 2) >> 4;  // one 64-K activation box
+      int st = 0, t = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < total && ok; u += gridDim.x, ++t) {
+        const Unit w = cta_unit<BN>(p, ulist, t, u);
+        const int ks0 = w.split * p.ksteps / p.splits;
+        const int ks1 = (w.split + 1) * p.ksteps / p.splits;
+        const int buf = t & 1;
+        ok = wait_bounded(&ctl->accempty[buf], ((t >> 1) & 1) ^ 1, ctl, p.status);
         if (!ok) break;
         tc_fence_after();
-        if (lane == 0) {
+        const uint32_t d_tmem = tmem + buf * BN;
+        for (int ks = ks0; ks < ks1; ks += kGA, ++st) {
+          const int nmma = min(kGA, ks1 - ks) * kEntryK / 16;  // K = 16 per MMA
+          const int d = st % ND;
+          ok = wait_bounded(&ctl->afull[d], (st / ND) & 1, ctl, p.status);
+          if (!ok) break;
+          tc_fence_after();
           // descriptor of the step's first K slice; the others differ only in
-          // the start-address field (address >> 4, no carry below 256 KB)
+          // the start-address field (address >> 4, no carry below 256 KB):
+          // four K slices of 16 (32 bytes) per 64-K activation box
           const uint64_t b_desc = smem_desc_k_sw128(smem_addr(sB + d * kBBytes));
           const uint32_t a_tmem = tmem + kACol0 + d * kAColsPerStep;
           const uint32_t acc0 = ks > ks0 ? 1u : 0u;
-#pragma unroll
-          for (int kk = 0; kk < 16; ++kk) {
-            if (kk < nmma) {
-              // four K slices of 16 per 64-K activation box
-              constexpr uint32_t kBox = kBBytesK / 2;
-              const uint64_t off = (uint64_t)(((kk >> 2) * kBox + (kk & 3) * 32) >> 4);
-              mma_ts(d_tmem, a_tmem + kk * 8, b_desc + off, kIdesc, kk > 0 ? 1u : acc0);
-            }
+          if (nmma == 16) {
+            mma_ts_x16<2, 4, 6, kBoxD, kBoxD + 2, kBoxD + 4, kBoxD + 6, 2 * kBoxD, 2 * kBoxD + 2,
+                       2 * kBoxD + 4, 2 * kBoxD + 6, 3 * kBoxD, 3 * kBoxD + 2, 3 * kBoxD + 4,
+                       3 * kBoxD + 6>(d_tmem, a_tmem, b_desc, kIdesc, acc0);
+          } else {
+            for (int kk = 0; kk < nmma; ++kk)
+              mma_ts(d_tmem, a_tmem + kk * 8, b_desc + (uint64_t)((kk >> 2) * kBoxD + (kk & 3) * 2),
+                     kIdesc, kk > 0 ? 1u : acc0);
           }
           mma_commit(&ctl->stepfree[d]);
         }
-        __syncwarp();
+        if (!ok) break;
+        mma_commit(&ctl->accfull[buf]);
       }
-      if (!ok) break;
-      if (lane == 0) mma_commit(&ctl->accfull[buf]);
-      __syncwarp();
-    }
-    // every MMA issued here must finish before tensor memory is freed
-    if (lane == 0) {
+      // every MMA issued here must finish before tensor memory is freed
       mma_commit(&ctl->drain);
       wait_drain(&ctl->drain, 0);
     }
@@ -503,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // in this group's half of the ring, read this thread's row into
     // registers, convert it (int8: exact; uint4: (q - z) * s per group),
     // write it into the step's tensor-memory A stage and hand the slot back.
-    // Then tell the MMA issuer.
+    // Then wait for the step's activations and tell the MMA issuer.
     const int grp = (warp - kConvWarp0) >> 2;  // takes the steps with st % kConvGroups == grp
     const int q = warp & 3;                    // tensor-memory lane quarter of this warp
     const int r = q * 32 + lane;
@@ -586,6 +588,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&ctl->emptyA[sa]);
         }
+        if (!ok) break;
+        // the step's activations (exact: the MMAs that read this slot's
+        // previous fill are done, so its barrier is at most this phase behind)
+        ok = warp_wait(&ctl->fullB[d], (st / ND) & 1, ctl, p.status, lane);
         if (!ok) break;
         tmem_st_wait();
         tc_fence_before();

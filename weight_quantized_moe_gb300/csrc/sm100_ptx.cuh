@@ -105,6 +105,58 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
+// One MMA step: 16 MMAs of K = 16 into the same accumulator, A from 16
+// consecutive 8-column slices of tensor memory, B slice kk at descriptor
+// b_desc + Okk (a start-address offset in 16-byte units).  The first MMA
+// accumulates only if `accumulate` is nonzero, the others always.  All 16 are
+// issued from one asm statement, with no instruction of the compiler's
+// between them.
+template <uint32_t O1, uint32_t O2, uint32_t O3, uint32_t O4, uint32_t O5, uint32_t O6,
+          uint32_t O7, uint32_t O8, uint32_t O9, uint32_t O10, uint32_t O11, uint32_t O12,
+          uint32_t O13, uint32_t O14, uint32_t O15>
+__device__ __forceinline__ void mma_ts_x16(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred pa;\n\t.reg .b64 bd;\n\t.reg .b32 ta;\n\t"
+      "setp.ne.b32 pa, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, pa;\n\t"
+      "setp.eq.b32 pa, %3, %3;\n\t"
+      "add.s32 ta, %1, 8;\n\tadd.s64 bd, %2, %5;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, pa;\n\t"
+      "add.s32 ta, %1, 16;\n\tadd.s64 bd, %2, %6;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, pa;\n\t"
+      "add.s32 ta, %1, 24;\n\tadd.s64 bd, %2, %7;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, pa;\n\t"
+      "add.s32 ta, %1, 32;\n\tadd.s64 bd, %2, %8;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, pa;\n\t"
+      "add.s32 ta, %1, 40;\n\tadd.s64 bd, %2, %9;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, pa;\n\t"
+      "add.s32 ta, %1, 48;\n\tadd.s64 bd, %2, %10;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, pa;\n\t"
+      "add.s32 ta, %1, 56;\n\tadd.s64 bd, %2, %11;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, pa;\n\t"
+      "add.s32 ta, %1, 64;\n\tadd.s64 bd, %2, %12;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, pa;\n\t"
+      "add.s32 ta, %1, 72;\n\tadd.s64 bd, %2, %13;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, pa;\n\t"
+      "add.s32 ta, %1, 80;\n\tadd.s64 bd, %2, %14;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, pa;\n\t"
+      "add.s32 ta, %1, 88;\n\tadd.s64 bd, %2, %15;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, pa;\n\t"
+      "add.s32 ta, %1, 96;\n\tadd.s64 bd, %2, %16;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, pa;\n\t"
+      "add.s32 ta, %1, 104;\n\tadd.s64 bd, %2, %17;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, pa;\n\t"
+      "add.s32 ta, %1, 112;\n\tadd.s64 bd, %2, %18;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, pa;\n\t"
+      "add.s32 ta, %1, 120;\n\tadd.s64 bd, %2, %19;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %3, pa;\n\t"
+      "}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate),
+      "n"(O1), "n"(O2), "n"(O3), "n"(O4), "n"(O5), "n"(O6), "n"(O7), "n"(O8), "n"(O9), "n"(O10), "n"(O11), "n"(O12), "n"(O13), "n"(O14), "n"(O15)
+      : "memory");
+}
+
 // Arrives once on `bar` when every tcgen05.mma issued so far by this thread
 // has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
