@@ -3,7 +3,7 @@
 // performs before its grouped GEMMs).
 //
 // One CTA of 32 warps.  Warp w owns the contiguous slot range
-// [w * chunk, (w + 1) * chunk).
+// [w * per_warp, (w + 1) * per_warp).
 //   1. per-warp histograms hist[w][e] (shared-memory atomics);
 //   2. per expert: count, pad, block-wide exclusive scan -> segment starts;
 //      hist[w][e] becomes the first position of warp w's slots of expert e;
@@ -11,6 +11,11 @@
 //      hist[w][e] + (rank among equal experts in this 32-slot step), found
 //      with __match_any_sync; the rank order is lane order, i.e. slot order.
 // The result is therefore deterministic and identical to a stable sort.
+//
+// Optionally (chunk > 0) it also cuts each expert's padded segment into
+// chunks of at most `chunk` slots, the token tiles of the expert GEMMs:
+// chunk_start[e] = index of expert e's first chunk (chunk_start[E] = the
+// number of chunks) and chunk_expert[c] = the expert of chunk c.
 #include "common.cuh"
 
 namespace {
@@ -21,10 +26,12 @@ constexpr int kThreads = kWarps * 32;
 __global__ void __launch_bounds__(kThreads, 1)
     align_kernel(const int32_t* __restrict__ ids, int S, int E, int bm, int32_t* __restrict__ sorted,
                  int32_t* __restrict__ block_expert, int32_t* __restrict__ offsets,
-                 int32_t* __restrict__ num_padded, unsigned* status) {
+                 int32_t* __restrict__ num_padded, int chunk, int32_t* __restrict__ chunk_expert,
+                 int32_t* __restrict__ chunk_start, unsigned* status) {
   extern __shared__ int smem[];
   int* hist = smem;                   // [kWarps][E]
   int* warp_tot = smem + kWarps * E;  // [kWarps] scan scratch
+  int* warp_tot2 = warp_tot + kWarps; // [kWarps] scan scratch (chunks)
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
@@ -32,9 +39,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int i = tid; i < kWarps * E; i += kThreads) hist[i] = 0;
   __syncthreads();
 
-  const int chunk = (S + kWarps - 1) / kWarps;
-  const int begin = warp * chunk;
-  const int end = min(S, begin + chunk);
+  const int per_warp = (S + kWarps - 1) / kWarps;
+  const int begin = warp * per_warp;
+  const int end = min(S, begin + per_warp);
   bool bad = false;
   for (int base = begin; base < end; base += 32) {
     const int s = base + lane;
@@ -88,6 +95,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     offsets[E] = total;
     num_padded[0] = total;
   }
+  if (chunk > 0) {
+    // exclusive scan of the chunk counts, the same way as the padded sizes
+    const int nch = e < E ? (padded + chunk - 1) / chunk : 0;
+    int cincl = nch;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, cincl, o);
+      if (lane >= o) cincl += n;
+    }
+    if (lane == 31) warp_tot2[warp] = cincl;
+    __syncthreads();
+    if (warp == 0) {
+      int t2 = warp_tot2[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, t2, o);
+        if (lane >= o) t2 += n;
+      }
+      warp_tot2[lane] = t2;
+    }
+    __syncthreads();
+    const int cstart = cincl - nch + (warp ? warp_tot2[warp - 1] : 0);
+    if (e < E) {
+      chunk_start[e] = cstart;
+      for (int c = 0; c < nch; ++c) chunk_expert[cstart + c] = e;
+    }
+    if (tid == 0) chunk_start[E] = warp_tot2[kWarps - 1];
+  }
   __syncthreads();
 
   // ---- stable placement ---------------------------------------------------
@@ -111,14 +146,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int bm, int32_t* sorted,
                          int32_t* block_expert, int32_t* offsets, int32_t* num_padded,
-                         unsigned* status, cudaStream_t st) {
-  const size_t smem = (size_t)(kWarps * E + kWarps) * sizeof(int);
+                         unsigned* status, cudaStream_t st, int chunk, int32_t* chunk_expert,
+                         int32_t* chunk_start) {
+  const size_t smem = (size_t)(kWarps * E + 2 * kWarps) * sizeof(int);
   if (smem > 48 * 1024) {
     cudaError_t err =
         cudaFuncSetAttribute(align_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
   }
   align_kernel<<<1, kThreads, smem, st>>>(ids, T * k, E, bm, sorted, block_expert, offsets,
-                                          num_padded, status);
+                                          num_padded, chunk, chunk_expert, chunk_start, status);
   return cudaGetLastError();
 }

@@ -99,11 +99,15 @@ unsigned* status_ptr() {
 
 inline size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
 
-// Workspace layout of moe_quant_forward: align arrays, gathered activations
-// (f16) and their row scales, act (bf16, then f16 in place) and its row
-// scales, split-K partial outputs (fp32).
+// Workspace layout of moe_quant_forward: align arrays (16-slot blocks) and
+// the chunk table of the GEMMs' token tiles, gathered activations (f16) and
+// their row scales, act (bf16, then f16 in place) and its row scales,
+// split-K partial outputs (fp32).
+constexpr int kAlignBlock = 16;
+
 struct WsLayout {
-  size_t sorted, block_expert, offsets, num_padded, xs, xinv, act, act_inv, y, total;
+  size_t sorted, block_expert, offsets, num_padded, chunk_expert, chunk_start, xs, xinv, act,
+      act_inv, y, total;
   int64_t cap;
   TcPlan plan;
 };
@@ -111,7 +115,7 @@ struct WsLayout {
 WsLayout ws_layout(int T, int H, int I, int E, int k, int bits) {
   WsLayout L;
   L.plan = tc_plan(T, H, I, E, k, bits);
-  const int bm = L.plan.bn;
+  const int bm = kAlignBlock;
   const int64_t S = (int64_t)T * k;
   const int64_t cap = moe_align_capacity(T, k, E, bm);
   L.cap = cap;
@@ -120,6 +124,8 @@ WsLayout ws_layout(int T, int H, int I, int E, int k, int bits) {
   L.block_expert = off; off += align256(sizeof(int32_t) * (size_t)(cap / bm));
   L.offsets = off;      off += align256(sizeof(int32_t) * (size_t)(E + 1));
   L.num_padded = off;   off += align256(sizeof(int32_t));
+  L.chunk_expert = off; off += align256(sizeof(int32_t) * (size_t)(cap / bm));
+  L.chunk_start = off;  off += align256(sizeof(int32_t) * (size_t)(E + 1));
   L.xs = off;           off += align256(sizeof(__half) * (size_t)cap * (size_t)H);
   L.xinv = off;         off += align256(sizeof(float) * (size_t)cap);
   L.act = off;          off += align256(sizeof(__nv_bfloat16) * (size_t)cap * (size_t)I);
@@ -317,7 +323,7 @@ MQ_EXPORT int moe_quant_forward(const void* x, int T, int H, int I, int E, int k
     if (ob < xb + nb && xb < ob + nb) return fail(MQ_ERR_INVALID_ARG, "out overlaps x");
   }
   const WsLayout L = ws_layout(T, H, I, E, k, bits);
-  const int bm = L.plan.bn;
+  const int bm = kAlignBlock;
   if (ws_bytes < L.total)
     return fail(MQ_ERR_WORKSPACE, "workspace %zu bytes, need %zu", ws_bytes, L.total);
 
@@ -335,6 +341,8 @@ MQ_EXPORT int moe_quant_forward(const void* x, int T, int H, int I, int E, int k
   a.block_expert = reinterpret_cast<int32_t*>(ws + L.block_expert);
   a.offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
   a.num_padded = reinterpret_cast<int32_t*>(ws + L.num_padded);
+  a.chunk_expert = reinterpret_cast<int32_t*>(ws + L.chunk_expert);
+  a.chunk_start = reinterpret_cast<int32_t*>(ws + L.chunk_start);
   a.act = reinterpret_cast<__nv_bfloat16*>(ws + L.act);
   a.y = reinterpret_cast<float*>(ws + L.y);
   a.bm = bm;
@@ -344,7 +352,7 @@ MQ_EXPORT int moe_quant_forward(const void* x, int T, int H, int I, int E, int k
   {
     LaunchScope ls(MQ_PROF_ALIGN, st);
     err = launch_align(topk_ids, T, k, E, bm, a.sorted, a.block_expert, a.offsets, a.num_padded,
-                       a.status, st);
+                       a.status, st, L.plan.bn, a.chunk_expert, a.chunk_start);
   }
   if (err != cudaSuccess) return cuda_fail(err, "forward: align launch");
   void* xs = ws + L.xs;

@@ -49,9 +49,13 @@ MQ_HIDDEN cudaError_t launch_quant_uint4(const void* w, int64_t rows, int64_t co
                                          uint8_t* qw, uint16_t* sc, uint8_t* qz, cudaStream_t st);
 MQ_HIDDEN cudaError_t launch_route(const float* logits, int T, int E, int k, int renorm,
                                    float* topk_w, int32_t* topk_ids, cudaStream_t st);
+// chunk > 0 also writes the chunk table of the expert GEMMs' token tiles
+// (chunk_expert [cap / bm], chunk_start [E + 1]).
 MQ_HIDDEN cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int bm,
                                    int32_t* sorted, int32_t* block_expert, int32_t* offsets,
-                                   int32_t* num_padded, unsigned* status, cudaStream_t st);
+                                   int32_t* num_padded, unsigned* status, cudaStream_t st,
+                                   int chunk = 0, int32_t* chunk_expert = nullptr,
+                                   int32_t* chunk_start = nullptr);
 
 struct MoeArgs {
   const __nv_bfloat16* x;
@@ -72,6 +76,8 @@ struct MoeArgs {
   int32_t* block_expert;  // [cap / bm]
   int32_t* offsets;       // [E + 1]
   int32_t* num_padded;    // [1]
+  int32_t* chunk_expert;  // [cap / bm]: expert of each token tile (chunk)
+  int32_t* chunk_start;   // [E + 1]: first chunk of each expert; [E] = number of chunks
   __nv_bfloat16* act;     // [cap, I]
   float* y;               // [S, H]
   int bm;
@@ -80,7 +86,7 @@ struct MoeArgs {
 
 // Tensor-core path (tcgen05): tile plan and launchers.
 struct TcPlan {
-  int bn;      // token-slots per aligned block (MMA N)
+  int bn;      // token-slots per tile at most (MMA N <= bn); the align block is 16
   int splits;  // K splits of the down GEMM
 };
 MQ_HIDDEN TcPlan tc_plan(int T, int H, int I, int E, int k, int bits);

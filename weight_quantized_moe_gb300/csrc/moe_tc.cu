@@ -44,7 +44,7 @@ constexpr int kABytes = kTileM * kBK;     // int8 A tile per weight stage (16 KB
 constexpr int kConvGroups = 2;            // converter warpgroups (alternate MMA steps)
 constexpr int kConvWarp0 = 3;             // warps 0: A producer, 1: MMA, 2: B producer
 constexpr int kEpiWarp0 = kConvWarp0 + 4 * kConvGroups;  // first epilogue warp
-constexpr int kThreads = (kEpiWarp0 + 4) * 32;
+constexpr int kIssuer2Warp = kEpiWarp0 + 4;  // second MMA issuer (16-token tiles)
 constexpr unsigned long long kWaitNs = 1000000000ull;
 constexpr int kRasterGroup = 8;           // weight tiles per raster group
 constexpr uint32_t kTmemCols = 512;
@@ -61,20 +61,30 @@ constexpr int kUnitList = 512;            // work units per CTA decoded once int
 //   cycles for any N <= 64, and each wait or commit costs about as much as
 //   an MMA, so batching keeps the issuing thread below the time HBM needs to
 //   deliver the weights.
-// * Tensor memory holds two BN-column accumulators and kSteps converted-A
+// * Tensor memory holds two accumulator buffers and kSteps converted-A
 //   stages of kG * 64 columns; the activation ring has the same depth, and
 //   one MMA commit per step frees both.
+// * One tcgen05.mma takes about 80 cycles to issue whatever N is, and the
+//   issuing thread's wait and commit around each 16-MMA step add about a
+//   third to that.  For 16-token tiles a second issuer thread takes
+//   every other step, so that one thread's wait and commit overlap the
+//   other's MMAs; each issuer accumulates its steps into its own half of the
+//   accumulator (kNI = 2 halves, added in a fixed order by the epilogue),
+//   and step st uses tensor-memory stage st % 2 (kSteps = 2).
 template <int BN>
 struct TileCfg {
-  static constexpr int kACol0 = 2 * BN;  // two accumulator buffers
+  static constexpr int kNI = BN == 16 ? 2 : 1;  // MMA issuer threads
+  static constexpr int kACol0 = 2 * kNI * BN;   // two accumulator buffers of kNI halves
   static constexpr int kStepFit = ((int)kTmemCols - kACol0) / kAColsPerStep;
-  static constexpr int kSteps = kStepFit > kMaxSteps ? kMaxSteps : kStepFit;
+  static constexpr int kSteps = kNI == 2 ? 2 : (kStepFit > kMaxSteps ? kMaxSteps : kStepFit);
+  static constexpr int kThreads = (kEpiWarp0 + 4 + (kNI - 1)) * 32;
   static constexpr int kBBytesK = BN * kBK * 2;     // activations per weight stage
   static constexpr int kBBytes = kG * kBBytesK;     // activations per MMA step
   static constexpr int kAFit = (kSmemBudget - kSteps * kBBytes) / kABytes;
   static constexpr int kAStagesSmem = kAFit > 12 ? 12 : kAFit;
   static_assert(kACol0 + kSteps * kAColsPerStep <= (int)kTmemCols, "tensor memory budget");
   static_assert(kSteps >= 2, "MMA-step depth");
+  static_assert(kNI == 1 || (kSteps == 2 && kStepFit >= 2), "two issuers: one stage each");
   static_assert(kAStagesSmem >= 3, "weight ring depth");
 };
 
@@ -84,9 +94,9 @@ struct TcParams {
   int MT;            // weight tiles per expert
   int splits;        // K splits
   const int32_t* sorted;
-  const int32_t* block_expert;
-  const int32_t* offsets;
-  const int32_t* num_padded;
+  const int32_t* offsets;       // [E + 1] padded expert segments (16-slot blocks)
+  const int32_t* chunk_expert;  // expert of each token tile
+  const int32_t* chunk_start;   // [E + 1] first token tile of each expert
   const float* scale;     // int8: fp32 per-output-row scales of this GEMM's weights
   const __half* gscale;   // uint4: f16 group scales [rows, G]
   const uint8_t* gzero;   // uint4: zero points [rows / 2, G], even row in the low nibble
@@ -100,33 +110,47 @@ struct TcParams {
   unsigned* status;
 };
 
+// Work unit: token tile (rows [row0, row0 + n) of the expert-sorted
+// activations, n <= BN a multiple of 16, all of expert e), weight tile mt
+// and K split.
 struct Unit {
-  int e, b, mt, split;
+  int e, row0, n, mt, split;
 };
 
-// Work unit u -> (expert, block, weight tile, K split).  Units of one expert
-// are contiguous; inside an expert, groups of kRasterGroup weight tiles sweep
-// all of its token blocks, so a weight tile is reused from L2 by the blocks
-// that run at the same time.
+template <int N>
+struct IC {
+  static constexpr int value = N;
+};
+
+// Work unit u -> Unit.  Each expert's segment is cut into token tiles of at
+// most BN rows (its chunks); units of one expert are contiguous, and inside
+// an expert groups of kRasterGroup weight tiles sweep all of its token
+// tiles, so a weight tile is reused from L2 by the tiles that run at the
+// same time.
 template <int BN>
 __device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
   const int V = p.MT * p.splits;
-  const int b0 = u / V;
-  const int e = p.block_expert[b0];
-  const int bs = p.offsets[e] / BN;
-  const int nbe = p.offsets[e + 1] / BN - bs;
-  const int ue = u - bs * V;
-  const int g = ue / (kRasterGroup * nbe);
-  const int r = ue - g * kRasterGroup * nbe;
+  const int c0 = u / V;
+  const int e = p.chunk_expert[c0];
+  const int cs = p.chunk_start[e];
+  const int nce = p.chunk_start[e + 1] - cs;
+  const int ue = u - cs * V;
+  const int g = ue / (kRasterGroup * nce);
+  const int r = ue - g * kRasterGroup * nce;
   const int gsz = min(kRasterGroup, V - g * kRasterGroup);
   const int bl = r / gsz;
   const int v = g * kRasterGroup + (r - bl * gsz);
   Unit out;
   out.e = e;
-  out.b = bs + bl;
+  out.row0 = p.offsets[e] + bl * BN;
+  out.n = min(BN, p.offsets[e + 1] - out.row0);
   out.mt = v % p.MT;
   out.split = v / p.MT;
   return out;
+}
+
+__device__ __forceinline__ int4 pack_unit(const Unit& w) {
+  return make_int4(w.e, w.row0, w.mt | (w.split << 20), w.n);
 }
 
 // Unit number i of this CTA (u = blockIdx.x + i * gridDim.x): from the list
@@ -137,9 +161,10 @@ __device__ __forceinline__ Unit cta_unit(const TcParams& p, const int4* ulist, i
     const int4 v = ulist[i];
     Unit w;
     w.e = v.x;
-    w.b = v.y;
-    w.mt = v.z;
-    w.split = v.w;
+    w.row0 = v.y;
+    w.mt = v.z & 0xfffff;
+    w.split = v.z >> 20;
+    w.n = v.w;
     return w;
   }
   return decode_unit<BN>(p, u);
@@ -304,7 +329,7 @@ __device__ __forceinline__ void group_words(const TcParams& p, int wrow, int k, 
 // consumer per slot); a converter waits for its step's activations only
 // after it has seen the MMAs of the slot's previous use complete.
 template <int MODE, int BITS, int BN>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(TileCfg<BN>::kThreads, 1)
     moe_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const TcParams p) {
   using C = TileCfg<BN>;
@@ -319,6 +344,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kBBytesK = C::kBBytesK;
   constexpr int kBBytes = C::kBBytes;
   constexpr int kACol0 = C::kACol0;
+  // MMAs always run N = BN: a token tile's rows past its n belong to other
+  // tiles (or are zero fill), and the accumulator columns they produce are
+  // never read.  A compile-time descriptor keeps the issue loop short.
   constexpr uint32_t kIdesc = idesc_f16_f32(kTileM, BN);
   static_assert(NA <= 16, "ring sizes");
 
@@ -343,10 +371,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&ctl->stepfree[s], 1);  // MMA commit
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&ctl->accfull[s], 1);
+      mbar_init(&ctl->accfull[s], C::kNI);  // one commit per issuer
       mbar_init(&ctl->accempty[s], 4);
     }
-    mbar_init(&ctl->drain, 1);
+    mbar_init(&ctl->drain, C::kNI);
     ctl->abort_flag = 0;
     fence_mbar_init();
   }
@@ -356,14 +384,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   // Decode this CTA's work units once, all threads in parallel, so that no
   // role waits on the schedule's global loads at a unit boundary.
-  const int nb = *p.num_padded / BN;
-  const int total = nb * p.MT * p.splits;
+  const int total = p.chunk_start[p.E] * p.MT * p.splits;
   int4* ulist = reinterpret_cast<int4*>(ctl + 1);
-  for (int i = threadIdx.x; i < kUnitList; i += kThreads) {
+  for (int i = threadIdx.x; i < kUnitList; i += C::kThreads) {
     const int u = blockIdx.x + i * gridDim.x;
     if (u >= total) break;
-    const Unit w = decode_unit<BN>(p, u);
-    ulist[i] = make_int4(w.e, w.b, w.mt, w.split);
+    ulist[i] = pack_unit(decode_unit<BN>(p, u));
   }
   tc_fence_before();
   __syncthreads();
@@ -436,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* b = sB + d * kBBytes;
           for (int j = 0; j < nboxes; ++j)  // past K the box reads the fill value 0
             tma_load_2d(b + j * (kBBytesK / 2), &tmB, &ctl->fullB[d], ks * kEntryK + 64 * j,
-                        w.b * BN);
+                        w.row0);
         }
         __syncwarp();
       }
@@ -449,14 +475,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp == 1 || (C::kNI == 2 && warp == kIssuer2Warp)) {
     // ------------------------------------------------- MMA issuer ----
     // One thread runs this loop: it alone waits, issues and commits, so the
     // rest of the warp has nothing to agree on.  Per 256-K step: one wait
     // (the converted A stage; the converters have also seen the step's
     // activations land), the 16 MMAs from one asm statement, one commit.
+    // With two issuers, issuer ip takes the steps st with st % 2 == ip and
+    // accumulates them into half ip of the unit's accumulator buffer.
     if (lane == 0) {
       constexpr uint32_t kBoxD = (uint32_t)(kBBytesK / 2) >> 4;  // one 64-K activation box
+      const int ip = warp == 1 ? 0 : 1;
       int st = 0, t = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < total && ok; u += gridDim.x, ++t) {
@@ -467,8 +496,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = wait_bounded(&ctl->accempty[buf], ((t >> 1) & 1) ^ 1, ctl, p.status);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem + buf * BN;
+        const uint32_t d_tmem = tmem + (buf * C::kNI + ip) * BN;
+        uint32_t acc = 0;  // the first step of this issuer in the unit overwrites
         for (int ks = ks0; ks < ks1; ks += kGA, ++st) {
+          if (C::kNI == 2 && (st & 1) != ip) continue;
           const int nmma = min(kGA, ks1 - ks) * kEntryK / 16;  // K = 16 per MMA
           const int d = st % ND;
           ok = wait_bounded(&ctl->afull[d], (st / ND) & 1, ctl, p.status);
@@ -479,16 +510,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           // four K slices of 16 (32 bytes) per 64-K activation box
           const uint64_t b_desc = smem_desc_k_sw128(smem_addr(sB + d * kBBytes));
           const uint32_t a_tmem = tmem + kACol0 + d * kAColsPerStep;
-          const uint32_t acc0 = ks > ks0 ? 1u : 0u;
           if (nmma == 16) {
             mma_ts_x16<2, 4, 6, kBoxD, kBoxD + 2, kBoxD + 4, kBoxD + 6, 2 * kBoxD, 2 * kBoxD + 2,
                        2 * kBoxD + 4, 2 * kBoxD + 6, 3 * kBoxD, 3 * kBoxD + 2, 3 * kBoxD + 4,
-                       3 * kBoxD + 6>(d_tmem, a_tmem, b_desc, kIdesc, acc0);
+                       3 * kBoxD + 6>(d_tmem, a_tmem, b_desc, kIdesc, acc);
           } else {
             for (int kk = 0; kk < nmma; ++kk)
               mma_ts(d_tmem, a_tmem + kk * 8, b_desc + (uint64_t)((kk >> 2) * kBoxD + (kk & 3) * 2),
-                     kIdesc, kk > 0 ? 1u : acc0);
+                     kIdesc, kk > 0 ? 1u : acc);
           }
+          acc = 1;
           mma_commit(&ctl->stepfree[d]);
         }
         if (!ok) break;
@@ -604,15 +635,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;
     const int r = q * 32 + lane;
     const bool odd = (lane & 1) != 0;
-    constexpr int CH = BN < 32 ? BN : 32;  // accumulator columns per tcgen05.ld
-    constexpr int HALF = CH / 2;
+    // accumulator columns per tcgen05.ld (two issuers: two halves are loaded)
+    constexpr int CH = C::kNI == 2 ? 16 : (BN < 32 ? BN : 32);
     int t = 0;
+    int est = 0;  // schedule index of the unit's first MMA step
     for (int u = blockIdx.x; u < total; u += gridDim.x, ++t) {
       const Unit w = cta_unit<BN>(p, ulist, t, u);
       const int buf = t & 1;
+      const int nsteps = ((w.split + 1) * p.ksteps / p.splits - w.split * p.ksteps / p.splits + kGA - 1) / kGA;
+      // two issuers: both halves hold partial sums when the unit has two or
+      // more steps; with one step only half (first step % 2) was written
+      const bool both = C::kNI == 2 && nsteps >= 2;
+      const int half0 = (C::kNI == 2 && !both) ? (est & 1) : 0;
+      est += nsteps;
       if (!warp_wait_sleepy(&ctl->accfull[buf], (t >> 1) & 1, ctl, p.status, lane)) break;
       tc_fence_after();
-      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + buf * BN;
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (buf * C::kNI + half0) * BN;
+      // accumulator columns [c0, c0 + W) into v: half 0 (+ half 1), in that order
+      auto load_acc = [&](auto wtag, int c0, auto& v) {
+        constexpr int W = decltype(wtag)::value;
+        tmem_ld_cols_sync<W>(taddr + c0, v);
+        if (C::kNI == 2 && both) {
+          uint32_t v2[W];
+          tmem_ld_cols_sync<W>(taddr + BN + c0, v2);
+#pragma unroll
+          for (int j = 0; j < W; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(v2[j]));
+        }
+      };
       if (MODE == 1) {
         // lanes (2i, 2i+1) hold gate row i and up row i; per pair of
         // columns (jj, jj + HALF) the even lane finishes column jj and the
@@ -623,45 +672,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float sc = BITS == 8 ? p.scale[wrow] : 1.0f;
         // uint4 runs the down GEMM in the K order [0,4,1,5,2,6,3,7] per octet
         const int col = w.mt * 64 + q * 16 + (BITS == 8 ? (lane >> 1) : permute_octet(lane >> 1));
-        for (int c0 = 0; c0 < BN; c0 += CH) {
-          uint32_t v[CH];
-          const float xv = lane < CH ? p.xinv[w.b * BN + c0 + lane] : 1.0f;
-          tmem_ld_cols_sync<CH>(taddr + c0, v);
+        auto body = [&](auto wtag, int c0) {
+          constexpr int W = decltype(wtag)::value;
+          constexpr int HW = W / 2;
+          uint32_t v[W];
+          const float xv = lane < W ? p.xinv[w.row0 + c0 + lane] : 1.0f;
+          load_acc(wtag, c0, v);
 #pragma unroll
-          for (int jj = 0; jj < HALF; ++jj) {
-            const float lo = __uint_as_float(v[jj]) * sc;         // own row, column jj
-            const float hi = __uint_as_float(v[jj + HALF]) * sc;  // own row, column jj + HALF
+          for (int jj = 0; jj < HW; ++jj) {
+            const float lo = __uint_as_float(v[jj]) * sc;       // own row, column jj
+            const float hi = __uint_as_float(v[jj + HW]) * sc;  // own row, column jj + HW
             const float got = __shfl_xor_sync(0xffffffffu, odd ? lo : hi, 1);
-            const int cj = odd ? jj + HALF : jj;
+            const int cj = odd ? jj + HW : jj;
             const float xs = __shfl_sync(0xffffffffu, xv, cj);
             const float g = (odd ? got : lo) * xs;
             const float up = (odd ? hi : got) * xs;
             const float a = __fdividef(g * up, 1.0f + __expf(-g));  // silu(g) * up
-            p.act[(int64_t)(w.b * BN + c0 + cj) * p.I + col] = __float2bfloat16_rn(a);
+            p.act[(int64_t)(w.row0 + c0 + cj) * p.I + col] = __float2bfloat16_rn(a);
           }
-        }
+        };
+        int c0 = 0;
+        for (; c0 + CH <= w.n; c0 += CH) body(IC<CH>{}, c0);
+        if (CH > 16 && c0 < w.n) body(IC<16>{}, c0);  // n is a multiple of 16
       } else {
         const int h = w.mt * kTileM + r;
         const float sc = BITS == 8 ? p.scale[w.e * p.H + h] : 1.0f;
         float* yp = p.ypart + (int64_t)w.split * p.S * p.H;
-        for (int c0 = 0; c0 < BN; c0 += CH) {
-          uint32_t v[CH];
+        auto body = [&](auto wtag, int c0) {
+          constexpr int W = decltype(wtag)::value;
+          uint32_t v[W];
           // per column: its slot and the factor (act row scale x router weight)
           int slot = p.S;
           float f = 0.0f;
-          if (lane < CH) {
-            const int prow = w.b * BN + c0 + lane;
+          if (lane < W) {
+            const int prow = w.row0 + c0 + lane;
             slot = p.sorted[prow];
             if (slot < p.S) f = p.xinv[prow] * p.topk_w[slot];
           }
-          tmem_ld_cols_sync<CH>(taddr + c0, v);
+          load_acc(wtag, c0, v);
 #pragma unroll
-          for (int jj = 0; jj < CH; ++jj) {
+          for (int jj = 0; jj < W; ++jj) {
             const int sj = __shfl_sync(0xffffffffu, slot, jj);
             const float fj = __shfl_sync(0xffffffffu, f, jj);
             if (sj < p.S) yp[(int64_t)sj * p.H + h] = __uint_as_float(v[jj]) * sc * fj;
           }
-        }
+        };
+        int c0 = 0;
+        for (; c0 + CH <= w.n; c0 += CH) body(IC<CH>{}, c0);
+        if (CH > 16 && c0 < w.n) body(IC<16>{}, c0);  // n is a multiple of 16
       }
       tc_fence_before();
       __syncwarp();
@@ -864,7 +922,7 @@ cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const TcPa
   const int sms = tc_num_sms();
   const int grid = max_units < sms ? max_units : sms;
   if (grid <= 0) return cudaSuccess;
-  kern<<<grid, kThreads, smem, st>>>(ta, tb, p);
+  kern<<<grid, TileCfg<BN>::kThreads, smem, st>>>(ta, tb, p);
   return cudaGetLastError();
 }
 
@@ -889,10 +947,14 @@ inline int entries(int K, int bits) { return (K + entry_k(bits) - 1) / entry_k(b
 TcPlan tc_plan(int T, int H, int I, int E, int k, int bits) {
   TcPlan pl;
   const int64_t S = (int64_t)T * k;
-  const int64_t per_expert = (S + E - 1) / E;
-  // token-slots per block: cover an average expert's load with some slack
-  int bn = 16;
-  while (bn < 128 && bn < per_expert + per_expert / 2) bn *= 2;
+  // Token-slots per tile at most (the MMA's N).  A tile is cut from one
+  // expert's segment with the rows it has, so a larger bound only costs
+  // shared memory for the activation ring, while a smaller one streams an
+  // expert's weights once per tile.  Up to 32 tokens: 16 (with two MMA
+  // issuers, the fastest tile for small loads); up to 64 tokens: 64, which
+  // covers any expert even if it receives the whole batch (an expert gets at
+  // most one slot per token); beyond that, 128.
+  const int bn = T > 64 ? 128 : (T > 32 ? 64 : 16);
   pl.bn = bn;
   // K splits of the down GEMM: enough work units (about 600, four per SM)
   // to keep every SM streaming weights; a fixed target keeps the workspace
@@ -933,8 +995,8 @@ namespace {
 
 void common_params(TcParams& p, const MoeArgs& a) {
   p.H = a.H; p.I = a.I; p.E = a.E; p.k = a.k; p.S = a.T * a.k;
-  p.sorted = a.sorted; p.block_expert = a.block_expert; p.offsets = a.offsets;
-  p.num_padded = a.num_padded;
+  p.sorted = a.sorted; p.offsets = a.offsets;
+  p.chunk_expert = a.chunk_expert; p.chunk_start = a.chunk_start;
   p.topk_w = a.topk_w;
   p.status = a.status;
   p.gs = a.bits == 8 ? 0 : a.group_size;
@@ -988,7 +1050,7 @@ cudaError_t launch_gemm1_tc(const MoeArgs& a, const TcPlan& pl, const void* xs,
   }
   p.act = a.act;
   p.xinv = xinv;
-  const int64_t units = (a.cap / pl.bn) * (int64_t)p.MT;
+  const int64_t units = (a.cap / a.bm) * (int64_t)p.MT;  // token tiles <= 16-slot blocks
   const int mu = (int)(units < (1 << 30) ? units : (1 << 30));
   return a.bits == 8 ? launch_gemm_bn<1, 8>(pl.bn, ta, tb, p, mu, st)
                      : launch_gemm_bn<1, 4>(pl.bn, ta, tb, p, mu, st);
@@ -1037,7 +1099,7 @@ cudaError_t launch_gemm2_tc(const MoeArgs& a, const TcPlan& pl, const float* act
   }
   p.ypart = ypart;
   p.xinv = act_inv;
-  const int64_t units = (a.cap / pl.bn) * (int64_t)p.MT * p.splits;
+  const int64_t units = (a.cap / a.bm) * (int64_t)p.MT * p.splits;
   const int mu = (int)(units < (1 << 30) ? units : (1 << 30));
   return a.bits == 8 ? launch_gemm_bn<2, 8>(pl.bn, ta, tb, p, mu, st)
                      : launch_gemm_bn<2, 4>(pl.bn, ta, tb, p, mu, st);
