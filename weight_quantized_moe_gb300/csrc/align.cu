@@ -37,6 +37,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = tid & 31;
 
   for (int i = tid; i < kWarps * E; i += kThreads) hist[i] = 0;
+  mq::pdl_wait();  // the ids come from the previous kernel
+  mq::pdl_trigger();
   __syncthreads();
 
   const int per_warp = (S + kWarps - 1) / kWarps;
@@ -154,7 +156,8 @@ cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int bm, int32_
         cudaFuncSetAttribute(align_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
   }
-  align_kernel<<<1, kThreads, smem, st>>>(ids, T * k, E, bm, sorted, block_expert, offsets,
-                                          num_padded, chunk, chunk_expert, chunk_start, status);
-  return cudaGetLastError();
+  const cudaError_t err =
+      launch_pdl(align_kernel, dim3(1), dim3(kThreads), smem, st, ids, T * k, E, bm, sorted,
+                 block_expert, offsets, num_padded, chunk, chunk_expert, chunk_start, status);
+  return err != cudaSuccess ? err : cudaGetLastError();
 }

@@ -33,12 +33,41 @@ __device__ __forceinline__ unsigned long long global_timer_ns() {
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
+// Programmatic dependent launch.  The forward's kernels are launched so that
+// each may start while its predecessor in the stream is still running.
+// pdl_wait() blocks until the predecessor has completed and its writes are
+// visible; pdl_trigger() lets the successor begin launching.  Every kernel
+// triggers only after its own wait, so when a kernel starts, all kernels
+// before its predecessor have completed: only the predecessor's outputs need
+// the wait.  Without the launch attribute both are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // silu(u) * v in float32; silu(u) = u / (1 + exp(-u)).
 __device__ __forceinline__ float silu_mul(float u, float v) {
   return u / (1.0f + expf(-u)) * v;
 }
 
 }  // namespace mq
+
+// Launch with the programmatic-stream-serialization attribute (see pdl_wait).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
 
 // ---------------------------------------------------------------------------
 // Internal launchers (one translation unit each, not exported).

@@ -395,6 +395,11 @@ __global__ void __launch_bounds__(TileCfg<BN>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
+  // The unit list (from the align kernel, two or more launches back) and the
+  // weights do not depend on the previous kernel: the weight stream starts
+  // at once.  The activations (and, in the epilogue, their row scales) come
+  // from the previous kernel: the roles that read them wait for it first.
+  mq::pdl_trigger();
 
   if (warp == 0) {
     // ------------------------------------------ A producer (int8 weights) ----
@@ -446,6 +451,7 @@ __global__ void __launch_bounds__(TileCfg<BN>::kThreads, 1)
   } else if (warp == 2) {
     // ------------------------------------------ B producer (activations) ----
     if (lane == 0) tma_prefetch_desc(&tmB);
+    mq::pdl_wait();
     int st = 0;
     bool ok = true;
     for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
@@ -637,6 +643,7 @@ __global__ void __launch_bounds__(TileCfg<BN>::kThreads, 1)
     const bool odd = (lane & 1) != 0;
     // accumulator columns per tcgen05.ld (two issuers: two halves are loaded)
     constexpr int CH = C::kNI == 2 ? 16 : (BN < 32 ? BN : 32);
+    mq::pdl_wait();
     int t = 0;
     int est = 0;  // schedule index of the unit's first MMA step
     for (int u = blockIdx.x; u < total; u += gridDim.x, ++t) {
@@ -749,6 +756,8 @@ __global__ void __launch_bounds__(128) gather_rows_f16(const __nv_bfloat16* __re
                                                        float* __restrict__ xinv) {
   __shared__ float wmax[4];
   const int p = blockIdx.x;
+  mq::pdl_wait();  // sorted and num_padded come from the previous kernel
+  mq::pdl_trigger();
   if (p >= *num_padded) return;
   const int s = sorted[p];
   uint4* dst = reinterpret_cast<uint4*>(xs + (int64_t)p * H);  // one K octet per uint4
@@ -804,6 +813,8 @@ __global__ void __launch_bounds__(256) act_rows_to_f16(uint16_t* act, const int3
                                                        int I, float* __restrict__ xinv) {
   __shared__ float wmax[8];
   const int p = blockIdx.x;
+  mq::pdl_wait();  // act comes from the previous kernel
+  mq::pdl_trigger();
   if (p >= *num_padded) return;
   uint4* row = reinterpret_cast<uint4*>(act + (int64_t)p * I);
   const int n = I / 8;
@@ -848,6 +859,8 @@ __global__ void __launch_bounds__(256) combine_splits(const float* __restrict__ 
                                                       __nv_bfloat16* __restrict__ out) {
   const int64_t i4 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int H4 = H / 4;
+  mq::pdl_wait();  // ypart comes from the previous kernel
+  mq::pdl_trigger();
   if (i4 >= (int64_t)T * H4) return;
   const int t = (int)(i4 / H4);
   const int c = (int)(i4 % H4) * 4;
@@ -922,8 +935,8 @@ cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const TcPa
   const int sms = tc_num_sms();
   const int grid = max_units < sms ? max_units : sms;
   if (grid <= 0) return cudaSuccess;
-  kern<<<grid, TileCfg<BN>::kThreads, smem, st>>>(ta, tb, p);
-  return cudaGetLastError();
+  err = launch_pdl(kern, dim3(grid), dim3(TileCfg<BN>::kThreads), smem, st, ta, tb, p);
+  return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 template <int MODE, int BITS>
@@ -982,13 +995,11 @@ int tc_num_sms() {
 
 cudaError_t launch_gather_rows(const MoeArgs& a, void* xs, float* xinv, cudaStream_t st) {
   if (a.cap == 0) return cudaSuccess;
-  if (a.bits == 8)
-    gather_rows_f16<false><<<(unsigned)a.cap, 128, 0, st>>>(
-        a.x, a.sorted, a.num_padded, a.k, a.T * a.k, a.H, static_cast<__half*>(xs), xinv);
-  else
-    gather_rows_f16<true><<<(unsigned)a.cap, 128, 0, st>>>(
-        a.x, a.sorted, a.num_padded, a.k, a.T * a.k, a.H, static_cast<__half*>(xs), xinv);
-  return cudaGetLastError();
+  const cudaError_t err = launch_pdl(
+      a.bits == 8 ? gather_rows_f16<false> : gather_rows_f16<true>, dim3((unsigned)a.cap),
+      dim3(128), 0, st, a.x, a.sorted, a.num_padded, a.k, a.T * a.k, a.H,
+      static_cast<__half*>(xs), xinv);
+  return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 namespace {
@@ -1058,9 +1069,10 @@ cudaError_t launch_gemm1_tc(const MoeArgs& a, const TcPlan& pl, const void* xs,
 
 cudaError_t launch_act_to_f16(const MoeArgs& a, float* act_inv, cudaStream_t st) {
   if (a.cap == 0) return cudaSuccess;
-  act_rows_to_f16<<<(unsigned)a.cap, 256, 0, st>>>(reinterpret_cast<uint16_t*>(a.act), a.num_padded,
-                                                    a.I, act_inv);
-  return cudaGetLastError();
+  const cudaError_t err =
+      launch_pdl(act_rows_to_f16, dim3((unsigned)a.cap), dim3(256), 0, st,
+                 reinterpret_cast<uint16_t*>(a.act), a.num_padded, a.I, act_inv);
+  return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 cudaError_t launch_gemm2_tc(const MoeArgs& a, const TcPlan& pl, const float* act_inv,
@@ -1109,7 +1121,8 @@ cudaError_t launch_combine_splits(const MoeArgs& a, const float* ypart, int spli
                                   cudaStream_t st) {
   const int64_t n = (int64_t)a.T * (a.H / 4);
   if (n == 0) return cudaSuccess;
-  combine_splits<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(ypart, a.topk_ids, a.T, a.k, a.E,
-                                                              a.H, splits, a.out);
-  return cudaGetLastError();
+  const cudaError_t err =
+      launch_pdl(combine_splits, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, ypart,
+                 a.topk_ids, a.T, a.k, a.E, a.H, splits, a.out);
+  return err != cudaSuccess ? err : cudaGetLastError();
 }

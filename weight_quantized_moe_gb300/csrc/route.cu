@@ -29,6 +29,8 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ lo
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
+  mq::pdl_wait();  // the logits come from the previous kernel
+  mq::pdl_trigger();
   if (t >= T) return;
   const float* row = logits + (int64_t)t * E;
   float v[PER];
@@ -99,8 +101,10 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int renorm, f
   if (T == 0) return cudaSuccess;
   const unsigned blocks = (unsigned)((T + 7) / 8);
   const int per = (E + 31) / 32;
-#define MQ_ROUTE(P)                                                                            \
-  route_kernel<P><<<blocks, 256, 0, st>>>(logits, T, E, k, renorm, topk_w, topk_ids);          \
+  cudaError_t err = cudaSuccess;
+#define MQ_ROUTE(P)                                                                           \
+  err = launch_pdl(route_kernel<P>, dim3(blocks), dim3(256), 0, st, logits, T, E, k, renorm, \
+                   topk_w, topk_ids);                                                         \
   break;
   switch (per) {
     case 1: MQ_ROUTE(1)
@@ -112,5 +116,5 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int renorm, f
     default: MQ_ROUTE(32)
   }
 #undef MQ_ROUTE
-  return cudaGetLastError();
+  return err != cudaSuccess ? err : cudaGetLastError();
 }
