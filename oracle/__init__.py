@@ -13,7 +13,10 @@ it restates:
   ``quantizing_weight_loader`` and ``quantize_in_place_and_get_scales``);
 * "vllm.model_executor.layers.quantization.moe_wna16" -- the W4A16
   group-quantised storage (``MoeWNA16Method.create_weights`` and the AWQ/GPTQ
-  conversions inside ``get_weight_loader``).
+  conversions inside ``get_weight_loader``) and its 8-bit form (uint8 codes,
+  per-row scales and zeros);
+* "vllm.model_executor.layers.fused_moe.oracle.int8" -- the per-tensor
+  ("tensor" strategy) int8 scale.
 
 Precision: the forward runs in float64.  The two quantisers take their
 integer decisions in float32 (the precision the GPU kernels use), because a
@@ -34,6 +37,7 @@ from .moe_oracle import (  # noqa: F401
     pack_uint4_along_n,
     unpack_uint4_along_n,
     dequantize_uint4_group,
+    dequantize_uint8_per_channel,
     topk_route,
     align_capacity,
     align_block,
@@ -41,4 +45,6 @@ from .moe_oracle import (  # noqa: F401
     moe_forward,
     Int8Experts,
     Uint4Experts,
+    Uint8Experts,
+    Int8TensorExperts,
 )

@@ -22,6 +22,17 @@ Sources (vLLM API documentation pages):
       byte, the even index in the low nibble.
     - ``get_weight_loader.convert_gptq_int4_qzeros``: GPTQ stores z-1, the
       loader adds 1, so the stored zero is the true zero point.
+    - ``MoeWNA16Method`` with ``num_bits == 8``: ``group_size == -1`` (one
+      group per output row), qweight uint8 [E, N, K] (``bit8_pack_factor``
+      1), scales [E, N, 1] in the parameter dtype, optional qzeros uint8
+      [E, N, 1] (for 8 bits the loader also adds 1 to GPTQ zeros).
+* P-ct = "vllm.model_executor.layers.fused_moe.oracle.int8" (compressed-
+  tensors int8 config): strategy "channel", or "tensor" when the weight
+  scale has fewer elements than experts x output rows -- one scale per
+  expert.
+* P-int8 ``ExpertsInt8MoEMethod.apply`` passes ``apply_router_weight_on_input``
+  through to ``fused_experts``; the supported activation dtypes are bf16 and
+  fp16.
 
 Readings taken where the pages are silent are marked "Reading:" in place.
 """
@@ -277,6 +288,71 @@ class Int8Experts:
         return dequantize_int8_per_channel(self.w2[e][rows], self.s2[e][rows])
 
 
+# --------------------------------------------------------------------------
+# W8A16 stored the moe_wna16 way (P-wna16, num_bits == 8): uint8 codes,
+# one scale (and optionally one zero point) per output row
+# --------------------------------------------------------------------------
+def dequantize_uint8_per_channel(q, scales, zeros=None):
+    """w[n, k] = (q[n, k] - z[n]) * s[n] in float64.
+
+    Reading: without stored zero points the zero is 2^(bits-1) = 128, the
+    same convention as the implicit zero 8 of the 4-bit format, so that a
+    symmetric int8 code c is stored as c + 128.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    s = np.asarray(scales, dtype=np.float64).reshape(q.shape[0], 1)
+    z = 128.0 if zeros is None else np.asarray(zeros, dtype=np.float64).reshape(q.shape[0], 1)
+    return (q - z) * s
+
+
+@dataclass
+class Uint8Experts:
+    """W8A16 in the P-wna16 8-bit layout: uint8 qweight, per-row scales (the
+    parameter dtype's values, held as float64 here) and optional zeros."""
+    qw13: np.ndarray          # uint8 [E, 2I, H]
+    sc13: np.ndarray          # [E, 2I] (stored [E, 2I, 1])
+    qw2: np.ndarray           # uint8 [E, H, I]
+    sc2: np.ndarray           # [E, H]
+    qz13: np.ndarray = None   # uint8 [E, 2I] or None (zero 128)
+    qz2: np.ndarray = None    # uint8 [E, H] or None
+
+    @property
+    def shape(self):
+        E, N2, H = self.qw13.shape
+        return E, H, N2 // 2
+
+    def deq13(self, e):
+        return dequantize_uint8_per_channel(self.qw13[e], self.sc13[e],
+                                            None if self.qz13 is None else self.qz13[e])
+
+    def deq2(self, e, rows=None):
+        z = None if self.qz2 is None else self.qz2[e]
+        full = dequantize_uint8_per_channel(self.qw2[e], self.sc2[e], z)
+        return full if rows is None else full[rows]
+
+
+@dataclass
+class Int8TensorExperts:
+    """Int8 codes with one scale per expert and weight tensor (P-ct strategy
+    "tensor"): w = q * s[e]."""
+    w13: np.ndarray   # int8 [E, 2I, H]
+    s13: np.ndarray   # [E]
+    w2: np.ndarray    # int8 [E, H, I]
+    s2: np.ndarray    # [E]
+
+    @property
+    def shape(self):
+        E, N2, H = self.w13.shape
+        return E, H, N2 // 2
+
+    def deq13(self, e):
+        return self.w13[e].astype(np.float64) * float(self.s13[e])
+
+    def deq2(self, e, rows=None):
+        w = self.w2[e] if rows is None else self.w2[e][rows]
+        return w.astype(np.float64) * float(self.s2[e])
+
+
 @dataclass
 class Uint4Experts:
     """W4A16 expert weights in the P-wna16 layout (create_weights)."""
@@ -304,12 +380,19 @@ class Uint4Experts:
         return full if rows is None else full[rows]
 
 
-def moe_forward(x, experts, topk_w, topk_ids, tokens=None, out_cols=None):
+def moe_forward(x, experts, topk_w, topk_ids, tokens=None, out_cols=None,
+                apply_router_weight_on_input=False):
     """out[t] = sum_j topk_w[t, j] * W2(e_j) . (silu(g) * u), in float64.
 
     g = W13(e_j)[0:I] . x[t] and u = W13(e_j)[I:2I] . x[t] use the
-    dequantised weights (per-channel int8 or per-group uint4).  The gate half
-    comes first in w13, which fixes the SiLU-and-mul pairing.
+    dequantised weights (per-channel int8 or uint8, per-tensor int8 or
+    per-group uint4).  The gate half comes first in w13, which fixes the
+    SiLU-and-mul pairing.
+
+    Reading of ``apply_router_weight_on_input`` (a name only, on the pages):
+    the router weight scales the expert's input instead of its output,
+    out[t] = sum_j W2(e_j) . (silu(g') * u') with g', u' computed from
+    topk_w[t, j] * x[t].
 
     ``tokens`` restricts the computation to those rows (rows are independent
     once the routing is fixed); ``out_cols`` restricts the output columns
@@ -333,8 +416,14 @@ def moe_forward(x, experts, topk_w, topk_ids, tokens=None, out_cols=None):
         rr, jj = np.nonzero(sub_ids == e)
         W13 = experts.deq13(int(e))
         W2 = experts.deq2(int(e), None if out_cols is None else cols)
-        h = x[tokens[rr]] @ W13.T
+        xin = x[tokens[rr]]
+        if apply_router_weight_on_input:
+            xin = sub_w[rr, jj][:, None] * xin
+        h = xin @ W13.T
         a = silu(h[:, :I]) * h[:, I:]
         y = a @ W2.T
-        np.add.at(out, rr, sub_w[rr, jj][:, None] * y)
+        if apply_router_weight_on_input:
+            np.add.at(out, rr, y)
+        else:
+            np.add.at(out, rr, sub_w[rr, jj][:, None] * y)
     return out
