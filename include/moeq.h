@@ -194,6 +194,54 @@ int moe_quant_forward(const void* x, int T, int H, int I, int E, int k,
                       void* out, void* stream);
 
 /*
+ * Option flags of moe_quant_forward_ex (0 gives moe_quant_forward).
+ *
+ * MQ_FWD_W8_UINT8 (bits = 8): w13 / w2 hold uint8 codes u, the 8-bit form of
+ *     "vllm.model_executor.layers.quantization.moe_wna16" (MoeWNA16Method
+ *     with num_bits 8, group_size -1: qweight uint8 [E, N, K], scales
+ *     [E, N, 1], optional qzeros uint8 [E, N, 1]).  dequant = (u - z) * s
+ *     with z = 128, or with has_zp = 1 z13 uint8 [E, 2I] / z2 uint8 [E, H]
+ *     (one zero point per output row).
+ * MQ_FWD_SCALE_F16, MQ_FWD_SCALE_BF16 (bits = 8, at most one): the scales
+ *     are float16 / bfloat16 (the moe_wna16 parameter dtype) instead of
+ *     float32.
+ * MQ_FWD_SCALE_PER_TENSOR (bits = 8): one scale per expert and weight
+ *     tensor, s13 [E] and s2 [E] -- the "tensor" strategy of the
+ *     compressed-tensors int8 MoE config, chosen there when the weight scale
+ *     has fewer elements than experts x output rows.
+ * MQ_FWD_ACT_F16: x and out are float16 instead of bfloat16 (experts_int8
+ *     lists both as supported activation dtypes).
+ * MQ_FWD_ROUTER_WEIGHT_ON_INPUT: fused_experts' apply_router_weight_on_input
+ *     (a name only on the pages; read as): the router weight scales each
+ *     expert's input, h = dequant(w13[e]) . (topk_w[t,j] * x[t]), and the
+ *     expert's output is added unweighted, out[t] += y.
+ */
+#define MQ_FWD_W8_UINT8 0x1u
+#define MQ_FWD_SCALE_F16 0x2u
+#define MQ_FWD_SCALE_BF16 0x4u
+#define MQ_FWD_SCALE_PER_TENSOR 0x8u
+#define MQ_FWD_ACT_F16 0x10u
+#define MQ_FWD_ROUTER_WEIGHT_ON_INPUT 0x20u
+
+/*
+ * moe_quant_forward_ex -- moe_quant_forward with option flags (above).
+ * Arguments are those of moe_quant_forward, with x / out in the activation
+ * dtype the flags select.  out may be x itself (fused_experts' inplace =
+ * True: x is read only before out is written); any other overlap is
+ * rejected.  has_zp = 1 with bits = 8 requires MQ_FWD_W8_UINT8.
+ * Errors: as moe_quant_forward; flags that do not apply to the format (or
+ * unknown bits) give MQ_ERR_UNSUPPORTED.
+ */
+int moe_quant_forward_ex(const void* x, int T, int H, int I, int E, int k,
+                         int bits, int group_size, int has_zp,
+                         const void* w13, const void* w2,
+                         const void* s13, const void* s2,
+                         const uint8_t* z13, const uint8_t* z2,
+                         const float* topk_w, const int32_t* topk_ids,
+                         void* workspace, size_t ws_bytes,
+                         void* out, unsigned flags, void* stream);
+
+/*
  * moe_quant_forward_noalloc -- moe_quant_forward without a workspace
  * argument.  (The pages have no counterpart: their forward allocates its
  * intermediates through torch.)

@@ -42,6 +42,7 @@ from .moe_oracle import (  # noqa: F401
     align_capacity,
     align_block,
     silu,
+    round_to_bf16,
     moe_forward,
     Int8Experts,
     Uint4Experts,

@@ -259,6 +259,20 @@ def align_block(topk_ids, E, block_m):
 # --------------------------------------------------------------------------
 # Expert weights and the forward (P-int8 apply -> fused_experts)
 # --------------------------------------------------------------------------
+def round_to_bf16(a):
+    """Round to the nearest bfloat16 (ties to even), returned as float64.
+
+    A bfloat16 is the top 16 bits of a float32; the value is first rounded
+    to float32, then the low 16 bits are rounded away.  (NaN/inf are not
+    expected here.)
+    """
+    f = np.asarray(a, dtype=np.float64).astype(np.float32)
+    bits = f.view(np.uint32).astype(np.uint64)
+    lsb = (bits >> 16) & 1
+    bits = ((bits + 0x7FFF + lsb) >> 16) << 16
+    return bits.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
 def silu(u):
     """silu(u) = u / (1 + exp(-u)), the "silu" activation of apply()."""
     u = np.asarray(u, dtype=np.float64)
@@ -381,7 +395,7 @@ class Uint4Experts:
 
 
 def moe_forward(x, experts, topk_w, topk_ids, tokens=None, out_cols=None,
-                apply_router_weight_on_input=False):
+                apply_router_weight_on_input=False, intermediate="exact"):
     """out[t] = sum_j topk_w[t, j] * W2(e_j) . (silu(g) * u), in float64.
 
     g = W13(e_j)[0:I] . x[t] and u = W13(e_j)[I:2I] . x[t] use the
@@ -393,6 +407,12 @@ def moe_forward(x, experts, topk_w, topk_ids, tokens=None, out_cols=None,
     the router weight scales the expert's input instead of its output,
     out[t] = sum_j W2(e_j) . (silu(g') * u') with g', u' computed from
     topk_w[t, j] * x[t].
+
+    ``intermediate="bf16"`` rounds silu(g) * u to bfloat16 before the down
+    projection.  Reading: the pages do not state the intermediate's
+    precision; the GPU path holds it in bfloat16, the activation dtype, and
+    tests of variants whose error budget that rounding dominates compare
+    against this form.  The default keeps it exact.
 
     ``tokens`` restricts the computation to those rows (rows are independent
     once the routing is fixed); ``out_cols`` restricts the output columns
@@ -421,6 +441,8 @@ def moe_forward(x, experts, topk_w, topk_ids, tokens=None, out_cols=None,
             xin = sub_w[rr, jj][:, None] * xin
         h = xin @ W13.T
         a = silu(h[:, :I]) * h[:, I:]
+        if intermediate == "bf16":
+            a = round_to_bf16(a)
         y = a @ W2.T
         if apply_router_weight_on_input:
             np.add.at(out, rr, y)

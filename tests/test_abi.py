@@ -46,6 +46,7 @@ def test_align_capacity(lib):
 
 
 def test_host_side_rejections(lib):
+    from weight_quantized_moe_gb300 import binding
     vp = ctypes.c_void_p
     fake = vp(0x1000)  # never dereferenced: every case fails validation first
     # unsupported format (bits=8 with a group size)
@@ -64,6 +65,21 @@ def test_host_side_rejections(lib):
     assert lib.moe_quant_forward(fake, 4, 128, 128, 8, 2, 8, -1, 0, fake, fake, fake, fake,
                                  None, None, fake, fake, fake, 1 << 30, vp(0x1100), None) == 1
     assert b"overlap" in lib.mq_last_error_message()
+    # moe_quant_forward_ex: options that do not fit the format, unknown bits,
+    # both scale dtypes, zeros with int8 codes; out == x (in place) passes
+    # validation up to the workspace check
+    ex = lib.moe_quant_forward_ex
+    args = lambda bits, gs, zp, z, flags, out=vp(0x9000), ws=1 << 30: (
+        fake, 4, 128, 128, 8, 2, bits, gs, zp, fake, fake, fake, fake, z, z, fake, fake, fake,
+        ws, out, flags, None)
+    assert ex(*args(4, 128, 0, None, binding.MQ_FWD_W8_UINT8)) == 2
+    assert ex(*args(4, 128, 0, None, binding.MQ_FWD_SCALE_PER_TENSOR)) == 2
+    assert ex(*args(8, -1, 0, None, 0x400)) == 2
+    assert ex(*args(8, -1, 0, None, binding.MQ_FWD_SCALE_F16 | binding.MQ_FWD_SCALE_BF16)) == 2
+    assert ex(*args(8, -1, 1, fake, 0)) == 2
+    assert ex(*args(8, -1, 1, None, binding.MQ_FWD_W8_UINT8)) == 1
+    assert ex(*args(8, -1, 0, None, 0, out=vp(0x1100))) == 1
+    assert ex(*args(8, -1, 0, None, binding.MQ_FWD_ACT_F16, out=fake, ws=16)) == 4
     # null pointers, odd rows, bad group size, k > 32
     assert lib.moe_quantize_int8_per_channel(None, 4, 8, fake, fake, None) == 1
     assert lib.moe_quantize_int8_per_channel(fake, 4, 12, fake, fake, None) == 1

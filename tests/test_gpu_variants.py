@@ -1,0 +1,153 @@
+"""GPU parity of the forward's format and API variants (moe_quant_forward_ex)
+against the oracle: moe_wna16 8-bit storage (uint8 codes, per-row zeros,
+float16 / bfloat16 scales), per-tensor int8 scales, float16 activations,
+the router weight applied to the input, and the in-place output."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from moe_helpers import FWD_TOL, forward_error
+from weight_quantized_moe_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+mq = pytest.importorskip("weight_quantized_moe_gb300")
+
+SHAPES = {"tiny": (8, 2, 128, 256), "mid": (16, 4, 512, 384)}   # E, k, H, I
+
+
+def _scales(r, shape, lo=1e-4, hi=3e-4):
+    return r.uniform(lo, hi, shape)
+
+
+def _inputs(E, k, H, T, seed, renorm=True):
+    x = synth.hidden_states(T, H, seed, device="cuda")
+    lg = synth.router_logits(T, E, seed, device="cuda")
+    tw, tid = mq.moe_topk_route(lg, k, renorm)
+    return x, tw, tid
+
+
+def _check(out, x, ex, tw, tid, intermediate="bf16", tol=FWD_TOL, **kw):
+    """Against the oracle with the SiLU-and-mul intermediate rounded to
+    bfloat16, as the GPU holds it.  On these small random layers that one
+    rounding alone moves the output by up to ~1.2e-2 of its RMS (an exact
+    emulation of the arithmetic shows it); with it modelled, the default
+    path matches to within the output's own rounding, and the 1e-2 bound
+    checks everything else."""
+    torch.cuda.synchronize()
+    assert mq.mq_device_status() == 0
+    ref = oracle.moe_forward(x.float().cpu().numpy(), ex, tw.cpu().numpy(), tid.cpu().numpy(),
+                             intermediate=intermediate, **kw)
+    err = forward_error(out.float().cpu().numpy(), ref)
+    assert err <= tol, err
+
+
+# Router weight on the input: bound 2e-2 against the exact oracle.  The
+# weighted input w * x is held in f16 (2^-12 relative) and the intermediate
+# in bf16; the input rounding moves some intermediates across a bf16 rounding
+# boundary (a 2^-8 step), and silu(w g) * (w u) scales each slot's output by
+# about w^2, so the RMS over all tokens is set by the low-weight ones while
+# the largest errors sit in high-weight tokens.  An exact emulation of the
+# arithmetic on these layers gives up to 1.2e-2 against the exact oracle and
+# 0.8e-2 against the bf16-intermediate one; 2e-2 is the 1e-2 budget plus
+# that rounding term.  (The pages' path holds w * x in the activation dtype,
+# bf16, which rounds coarser still.)
+RWOI_TOL = 2e-2
+
+
+@pytest.mark.parametrize("shape", ["tiny", "mid"])
+@pytest.mark.parametrize("zp,sdt", [(False, torch.float32), (True, torch.float16),
+                                    (False, torch.bfloat16), (True, torch.float32)])
+def test_uint8_codes(shape, zp, sdt):
+    E, k, H, I = SHAPES[shape]
+    r = np.random.default_rng(E + H + int(zp))
+    u13 = r.integers(0, 256, (E, 2 * I, H)).astype(np.uint8)
+    u2 = r.integers(0, 256, (E, H, I)).astype(np.uint8)
+    s13 = torch.tensor(_scales(r, (E, 2 * I))).to(sdt)
+    s2 = torch.tensor(_scales(r, (E, H))).to(sdt)
+    z13 = r.integers(96, 160, (E, 2 * I)).astype(np.uint8) if zp else None
+    z2 = r.integers(96, 160, (E, H)).astype(np.uint8) if zp else None
+    ex = oracle.Uint8Experts(u13, s13.double().numpy().copy(), u2, s2.double().numpy().copy(), z13, z2)
+    x, tw, tid = _inputs(E, k, H, 37, seed=3)
+    dev = lambda a: torch.from_numpy(a).cuda()
+    out = mq.moe_quant_forward(x, dev(u13), dev(u2), s13.cuda(), s2.cuda(), tw, tid, bits=8,
+                               has_zp=zp, z13=dev(z13) if zp else None, z2=dev(z2) if zp else None)
+    _check(out, x, ex, tw, tid)
+
+
+@pytest.mark.parametrize("shape", ["tiny", "mid"])
+@pytest.mark.parametrize("sdt", [torch.float32, torch.bfloat16])
+def test_per_tensor_scale(shape, sdt):
+    E, k, H, I = SHAPES[shape]
+    r = np.random.default_rng(7 + E)
+    q13 = r.integers(-127, 128, (E, 2 * I, H)).astype(np.int8)
+    q2 = r.integers(-127, 128, (E, H, I)).astype(np.int8)
+    s13 = torch.tensor(_scales(r, (E,))).to(sdt)
+    s2 = torch.tensor(_scales(r, (E,))).to(sdt)
+    ex = oracle.Int8TensorExperts(q13, s13.double().numpy().copy(), q2, s2.double().numpy().copy())
+    x, tw, tid = _inputs(E, k, H, 29, seed=5)
+    dev = lambda a: torch.from_numpy(a).cuda()
+    out = mq.moe_quant_forward(x, dev(q13), dev(q2), s13.cuda(), s2.cuda(), tw, tid, bits=8)
+    _check(out, x, ex, tw, tid)
+
+
+def _int8_layer(E, H, I, seed):
+    r = np.random.default_rng(seed)
+    q13 = r.integers(-127, 128, (E, 2 * I, H)).astype(np.int8)
+    q2 = r.integers(-127, 128, (E, H, I)).astype(np.int8)
+    s13 = _scales(r, (E, 2 * I)).astype(np.float32)
+    s2 = _scales(r, (E, H)).astype(np.float32)
+    ex = oracle.Int8Experts(q13, s13, q2, s2)
+    dev = [torch.from_numpy(a).cuda() for a in (q13, q2, s13, s2)]
+    return ex, dev
+
+
+@pytest.mark.parametrize("shape", ["tiny", "mid"])
+def test_float16_activations(shape):
+    E, k, H, I = SHAPES[shape]
+    ex, (q13, q2, s13, s2) = _int8_layer(E, H, I, 11)
+    x, tw, tid = _inputs(E, k, H, 33, seed=8)
+    x16 = x.to(torch.float16)
+    out = mq.moe_quant_forward(x16, q13, q2, s13, s2, tw, tid, bits=8)
+    assert out.dtype == torch.float16
+    _check(out, x16, ex, tw, tid)
+
+
+@pytest.mark.parametrize("shape", ["tiny", "mid"])
+@pytest.mark.parametrize("renorm", [True, False])
+def test_router_weight_on_input(shape, renorm):
+    E, k, H, I = SHAPES[shape]
+    ex, (q13, q2, s13, s2) = _int8_layer(E, H, I, 13)
+    x, tw, tid = _inputs(E, k, H, 41, seed=9, renorm=renorm)
+    out = mq.moe_quant_forward(x, q13, q2, s13, s2, tw, tid, bits=8,
+                               apply_router_weight_on_input=True)
+    _check(out, x, ex, tw, tid, intermediate="exact", tol=RWOI_TOL,
+           apply_router_weight_on_input=True)
+
+
+def test_router_weight_on_input_w4a16():
+    wl = synth.Workload("w4s", E=8, k=2, H=256, I=256, Ts=(16,), bits=4, group_size=64,
+                        has_zp=True)
+    from moe_helpers import Layer, inputs
+    layer = Layer(wl, seed=2)
+    x, lg = inputs(wl, 19, seed=2)
+    tw, tid = mq.moe_topk_route(lg, wl.k, True)
+    out = layer.forward(x, tw, tid, apply_router_weight_on_input=True)
+    _check(out, x, layer.oracle_experts(), tw, tid, intermediate="exact", tol=RWOI_TOL,
+           apply_router_weight_on_input=True)
+
+
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float16])
+def test_inplace_equals_out_of_place(dt):
+    E, k, H, I = SHAPES["mid"]
+    ex, (q13, q2, s13, s2) = _int8_layer(E, H, I, 17)
+    x, tw, tid = _inputs(E, k, H, 64, seed=10)
+    x = x.to(dt)
+    ref = mq.moe_quant_forward(x, q13, q2, s13, s2, tw, tid, bits=8)
+    xi = x.clone()
+    got = mq.moe_quant_forward(xi, q13, q2, s13, s2, tw, tid, bits=8, inplace=True)
+    torch.cuda.synchronize()
+    assert got.data_ptr() == xi.data_ptr()
+    assert torch.equal(xi, ref)

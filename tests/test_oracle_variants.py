@@ -117,3 +117,35 @@ def test_router_weight_on_input_brute_force():
     np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
     # and it differs from scaling the output (SiLU is not homogeneous)
     assert not np.allclose(got, oracle.moe_forward(x, ex, w, ids), rtol=1e-6)
+
+
+def test_round_to_bf16_against_torch_and_hand_values():
+    """Ties go to even: 1 + 2^-8 -> 1, 1 + 3 * 2^-8 -> 1 + 2^-6 (even
+    mantissa), -(1 + 2^-9) -> -1; and agreement with torch's conversion on
+    random float32 values (the library routine rounds the same way)."""
+    import torch
+    hand = np.array([1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8, -(1 + 2.0 ** -9), 0.0, 3.0, 2.0 ** -120])
+    want = np.array([1.0, 1 + 2.0 ** -6, -1.0, 0.0, 3.0, 2.0 ** -120])
+    assert np.array_equal(oracle.round_to_bf16(hand), want)
+    v = (np.random.default_rng(0).standard_normal(100000) * 10.0 ** np.random.default_rng(1).uniform(-8, 8, 100000)).astype(np.float32)
+    ref = torch.from_numpy(v).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(oracle.round_to_bf16(v), ref)
+
+
+def test_bf16_intermediate_changes_only_the_intermediate():
+    """With intermediate values that are already bfloat16 numbers the two
+    forms agree exactly; in general they differ by at most the rounding."""
+    ex = _int8_layer(21, E=2, H=8, I=4)
+    x = _rng(22).standard_normal((3, 8))
+    w, ids = _routing(23, 3, 2, 1, renorm=True)
+    a = oracle.moe_forward(x, ex, w, ids)
+    b = oracle.moe_forward(x, ex, w, ids, intermediate="bf16")
+    assert not np.array_equal(a, b)
+    # |delta| <= sum_i |W2| |a_i| 2^-8 per output
+    E, H, I = ex.shape
+    for t in range(3):
+        e = int(ids[t, 0])
+        h = ex.deq13(e) @ x[t]
+        act = oracle.silu(h[:I]) * h[I:]
+        bound = np.abs(ex.deq2(e)) @ np.abs(act) * 2.0 ** -8
+        assert np.all(np.abs(a[t] - b[t]) <= bound * (1 + 1e-9))

@@ -22,4 +22,11 @@ from .binding import (  # noqa: F401
     moe_topk_route,
     MQ_DEV_BAD_EXPERT_ID,
     MQ_DEV_WAIT_TIMEOUT,
+    MQ_FWD_W8_UINT8,
+    MQ_FWD_SCALE_F16,
+    MQ_FWD_SCALE_BF16,
+    MQ_FWD_SCALE_PER_TENSOR,
+    MQ_FWD_ACT_F16,
+    MQ_FWD_ROUTER_WEIGHT_ON_INPUT,
+    forward_flags,
 )

@@ -20,6 +20,13 @@ LIB_PATH = os.path.join(_PKG, "libmoeq.so")
 MQ_OK, MQ_ERR_INVALID_ARG, MQ_ERR_UNSUPPORTED, MQ_ERR_CUDA, MQ_ERR_WORKSPACE = range(5)
 MQ_DEV_BAD_EXPERT_ID = 0x1
 MQ_DEV_WAIT_TIMEOUT = 0x2
+# moe_quant_forward_ex option flags (include/moeq.h)
+MQ_FWD_W8_UINT8 = 0x1
+MQ_FWD_SCALE_F16 = 0x2
+MQ_FWD_SCALE_BF16 = 0x4
+MQ_FWD_SCALE_PER_TENSOR = 0x8
+MQ_FWD_ACT_F16 = 0x10
+MQ_FWD_ROUTER_WEIGHT_ON_INPUT = 0x20
 
 _vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
 _SIGNATURES = {
@@ -34,6 +41,9 @@ _SIGNATURES = {
     "moe_quant_forward_workspace": (_sz, [_i32] * 7),
     "moe_quant_forward": (_i32, [_vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
                                  _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _vp]),
+    "moe_quant_forward_ex": (_i32, [_vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
+                                    _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp,
+                                    ctypes.c_uint, _vp]),
     "moe_quant_forward_noalloc": (_i32, [_vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
                                          _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "mq_kernel_launch_count": (ctypes.c_longlong, []),
@@ -206,19 +216,60 @@ def moe_quant_forward_workspace(T, H, I, E, k, bits=8, group_size=-1) -> int:
     return int(lib().moe_quant_forward_workspace(T, H, I, E, k, bits, group_size))
 
 
+def forward_flags(x, w13, s13, bits, apply_router_weight_on_input=False):
+    """moe_quant_forward_ex flags implied by the tensors' dtypes and shapes:
+    uint8 8-bit codes (moe_wna16), float16 / bfloat16 scales, one scale per
+    expert (fewer scale elements than experts x output rows), float16
+    activations."""
+    f = 0
+    if bits == 8:
+        if w13.dtype == torch.uint8:
+            f |= MQ_FWD_W8_UINT8
+        if s13.dtype == torch.float16:
+            f |= MQ_FWD_SCALE_F16
+        elif s13.dtype == torch.bfloat16:
+            f |= MQ_FWD_SCALE_BF16
+        if s13.numel() < w13.shape[0] * w13.shape[1]:
+            f |= MQ_FWD_SCALE_PER_TENSOR
+    if x.dtype == torch.float16:
+        f |= MQ_FWD_ACT_F16
+    if apply_router_weight_on_input:
+        f |= MQ_FWD_ROUTER_WEIGHT_ON_INPUT
+    return f
+
+
 def moe_quant_forward(x, w13, w2, s13, s2, topk_w, topk_ids, bits=8, group_size=-1,
-                      has_zp=False, z13=None, z2=None, workspace=None, out=None, stream=None):
-    """The fused expert MLP (see moe_quant_forward in include/moeq.h)."""
-    _need(x, torch.bfloat16, "x", 2)
+                      has_zp=False, z13=None, z2=None, workspace=None, out=None, stream=None,
+                      apply_router_weight_on_input=False, inplace=False):
+    """The fused expert MLP (moe_quant_forward / moe_quant_forward_ex in
+    include/moeq.h).  x is bf16 or f16 [T, H]; 8-bit weights are int8 with
+    float32 scales (experts_int8), or uint8 codes with float32 / float16 /
+    bfloat16 scales and optional per-row zeros (moe_wna16 8-bit); a scale of
+    one element per expert is a per-tensor scale.  inplace=True writes the
+    result into x."""
+    if x.dtype not in (torch.bfloat16, torch.float16):
+        raise TypeError(f"x must be bfloat16 or float16, got {x.dtype}")
+    _need(x, x.dtype, "x", 2)
     T, H = x.shape
     E = w13.shape[0]
     I = w13.shape[1] // 2
     k = topk_ids.shape[-1] if topk_ids.dim() == 2 else 1
     if bits == 8:
-        _need(w13, torch.int8, "w13", 3)
-        _need(w2, torch.int8, "w2", 3)
-        _need(s13, torch.float32, "s13")
-        _need(s2, torch.float32, "s2")
+        if w13.dtype not in (torch.int8, torch.uint8) or w2.dtype != w13.dtype:
+            raise TypeError("8-bit weights must be int8 (or uint8 codes), both alike")
+        _need(w13, w13.dtype, "w13", 3)
+        _need(w2, w2.dtype, "w2", 3)
+        if s13.dtype not in (torch.float32, torch.float16, torch.bfloat16) or s2.dtype != s13.dtype:
+            raise TypeError("8-bit scales must be float32, float16 or bfloat16, both alike")
+        _need(s13, s13.dtype, "s13")
+        _need(s2, s2.dtype, "s2")
+        if (s13.numel() < E * w13.shape[1]) != (s2.numel() < E * w2.shape[1]):
+            raise ValueError("per-tensor scales must be given for both w13 and w2")
+        if has_zp:
+            if w13.dtype != torch.uint8:
+                raise ValueError("zero points need uint8 codes")
+            _need(z13, torch.uint8, "z13")
+            _need(z2, torch.uint8, "z2")
     else:
         _need(w13, torch.uint8, "w13", 3)
         _need(w2, torch.uint8, "w2", 3)
@@ -229,18 +280,21 @@ def moe_quant_forward(x, w13, w2, s13, s2, topk_w, topk_ids, bits=8, group_size=
             _need(z2, torch.uint8, "z2")
     _need(topk_w, torch.float32, "topk_w")
     _need(topk_ids, torch.int32, "topk_ids")
+    flags = forward_flags(x, w13, s13, bits, apply_router_weight_on_input)
     ws_need = moe_quant_forward_workspace(T, H, I, E, k, bits, group_size)
     if workspace is None:
         workspace = torch.empty(max(ws_need, 16), dtype=torch.uint8, device=x.device)
     _need(workspace, torch.uint8, "workspace")
+    if inplace:
+        out = x
     if out is None:
-        out = torch.empty(T, H, dtype=torch.bfloat16, device=x.device)
-    _need(out, torch.bfloat16, "out", 2)
-    _check(lib().moe_quant_forward(
+        out = torch.empty(T, H, dtype=x.dtype, device=x.device)
+    _need(out, x.dtype, "out", 2)
+    _check(lib().moe_quant_forward_ex(
         _ptr(x), T, H, I, E, k, bits, group_size, int(bool(has_zp)),
         _ptr(w13), _ptr(w2), _ptr(s13), _ptr(s2), _ptr(z13 if has_zp else None),
         _ptr(z2 if has_zp else None), _ptr(topk_w), _ptr(topk_ids),
-        _ptr(workspace), workspace.numel(), _ptr(out), _stream(stream)))
+        _ptr(workspace), workspace.numel(), _ptr(out), flags, _stream(stream)))
     return out
 
 

@@ -294,16 +294,43 @@ MQ_EXPORT size_t moe_quant_forward_workspace(int T, int H, int I, int E, int k, 
   return ws_layout(T, H, I, E, k, bits).total;
 }
 
+MQ_EXPORT int moe_quant_forward_ex(const void* x, int T, int H, int I, int E, int k, int bits,
+                                   int group_size, int has_zp, const void* w13, const void* w2,
+                                   const void* s13, const void* s2, const uint8_t* z13,
+                                   const uint8_t* z2, const float* topk_w,
+                                   const int32_t* topk_ids, void* workspace, size_t ws_bytes,
+                                   void* out, unsigned flags, void* stream);
+
 MQ_EXPORT int moe_quant_forward(const void* x, int T, int H, int I, int E, int k, int bits,
                                 int group_size, int has_zp, const void* w13, const void* w2,
                                 const void* s13, const void* s2, const uint8_t* z13,
                                 const uint8_t* z2, const float* topk_w, const int32_t* topk_ids,
                                 void* workspace, size_t ws_bytes, void* out, void* stream) {
+  return moe_quant_forward_ex(x, T, H, I, E, k, bits, group_size, has_zp, w13, w2, s13, s2, z13,
+                              z2, topk_w, topk_ids, workspace, ws_bytes, out, 0u, stream);
+}
+
+MQ_EXPORT int moe_quant_forward_ex(const void* x, int T, int H, int I, int E, int k, int bits,
+                                   int group_size, int has_zp, const void* w13, const void* w2,
+                                   const void* s13, const void* s2, const uint8_t* z13,
+                                   const uint8_t* z2, const float* topk_w,
+                                   const int32_t* topk_ids, void* workspace, size_t ws_bytes,
+                                   void* out, unsigned flags, void* stream) {
+  constexpr unsigned kW8Flags = MQ_FWD_W8_UINT8 | MQ_FWD_SCALE_F16 | MQ_FWD_SCALE_BF16 |
+                                MQ_FWD_SCALE_PER_TENSOR;
+  constexpr unsigned kAllFlags = kW8Flags | MQ_FWD_ACT_F16 | MQ_FWD_ROUTER_WEIGHT_ON_INPUT;
   if (T < 0 || H <= 0 || I <= 0 || E < 1) return fail(MQ_ERR_INVALID_ARG, "bad T, H, I or E");
   if (k < 1 || k > E || k > 32) return fail(MQ_ERR_INVALID_ARG, "need 1 <= k <= min(E, 32)");
   if (E > 1024) return fail(MQ_ERR_UNSUPPORTED, "E must be <= 1024");
-  if (!fmt_ok(bits, group_size, has_zp))
-    return fail(MQ_ERR_UNSUPPORTED, "format must be (8, -1, 0) or (4, 32..256, 0|1)");
+  if (flags & ~kAllFlags) return fail(MQ_ERR_UNSUPPORTED, "unknown flags 0x%x", flags & ~kAllFlags);
+  if (bits == 4 && (flags & kW8Flags))
+    return fail(MQ_ERR_UNSUPPORTED, "uint8 codes and scale options apply to bits = 8 only");
+  if ((flags & MQ_FWD_SCALE_F16) && (flags & MQ_FWD_SCALE_BF16))
+    return fail(MQ_ERR_UNSUPPORTED, "scales are float16 or bfloat16, not both");
+  const bool w8zp = bits == 8 && group_size == -1 && has_zp == 1 && (flags & MQ_FWD_W8_UINT8);
+  if (!fmt_ok(bits, group_size, has_zp) && !w8zp)
+    return fail(MQ_ERR_UNSUPPORTED,
+                "format must be (8, -1, 0), (8, -1, 1) with uint8 codes, or (4, 32..256, 0|1)");
   if (H % 128 || I % 128) return fail(MQ_ERR_UNSUPPORTED, "H and I must be multiples of 128");
   if (bits == 4 && (H % group_size || I % group_size))
     return fail(MQ_ERR_UNSUPPORTED, "group_size must divide H and I");
@@ -311,16 +338,18 @@ MQ_EXPORT int moe_quant_forward(const void* x, int T, int H, int I, int E, int k
   if (T == 0) return MQ_OK;
   if (!x || !w13 || !w2 || !s13 || !s2 || !topk_w || !topk_ids || !out || !workspace)
     return fail(MQ_ERR_INVALID_ARG, "null pointer");
-  if (bits == 4 && has_zp && (!z13 || !z2)) return fail(MQ_ERR_INVALID_ARG, "null zero points");
-  if (bits == 4 && !has_zp && (z13 || z2))
-    return fail(MQ_ERR_INVALID_ARG, "zero points given with has_zp = 0");
+  if (has_zp && (!z13 || !z2)) return fail(MQ_ERR_INVALID_ARG, "null zero points");
+  if (!has_zp && (z13 || z2)) return fail(MQ_ERR_INVALID_ARG, "zero points given with has_zp = 0");
   if (!aligned16(x) || !aligned16(w13) || !aligned16(w2) || !aligned16(out) || !aligned16(workspace))
     return fail(MQ_ERR_INVALID_ARG, "x, w13, w2, out and workspace must be 16-byte aligned");
   {
     const char* xb = static_cast<const char*>(x);
     const char* ob = static_cast<const char*>(out);
     const size_t nb = (size_t)T * H * 2;
-    if (ob < xb + nb && xb < ob + nb) return fail(MQ_ERR_INVALID_ARG, "out overlaps x");
+    // out == x is fused_experts' inplace: x is read (gathered) before any
+    // output is written
+    if (ob != xb && ob < xb + nb && xb < ob + nb)
+      return fail(MQ_ERR_INVALID_ARG, "out overlaps x (only out == x is allowed)");
   }
   const WsLayout L = ws_layout(T, H, I, E, k, bits);
   const int bm = kAlignBlock;
@@ -330,12 +359,13 @@ MQ_EXPORT int moe_quant_forward(const void* x, int T, int H, int I, int E, int k
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
   MoeArgs a;
-  a.x = static_cast<const __nv_bfloat16*>(x);
+  a.x = x;
+  a.flags = flags;
   a.T = T; a.H = H; a.I = I; a.E = E; a.k = k;
   a.bits = bits; a.group_size = group_size; a.has_zp = has_zp;
   a.w13 = w13; a.w2 = w2; a.s13 = s13; a.s2 = s2; a.z13 = z13; a.z2 = z2;
   a.topk_w = topk_w; a.topk_ids = topk_ids;
-  a.out = static_cast<__nv_bfloat16*>(out);
+  a.out = out;
   a.status = status_ptr();
   a.sorted = reinterpret_cast<int32_t*>(ws + L.sorted);
   a.block_expert = reinterpret_cast<int32_t*>(ws + L.block_expert);

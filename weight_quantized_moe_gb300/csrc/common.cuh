@@ -87,7 +87,8 @@ MQ_HIDDEN cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int 
                                    int32_t* chunk_start = nullptr);
 
 struct MoeArgs {
-  const __nv_bfloat16* x;
+  const void* x;          // bf16, or f16 with MQ_FWD_ACT_F16
+  unsigned flags;         // MQ_FWD_* options
   int T, H, I, E, k;
   int bits, group_size, has_zp;
   const void* w13;
@@ -98,7 +99,7 @@ struct MoeArgs {
   const uint8_t* z2;
   const float* topk_w;
   const int32_t* topk_ids;
-  __nv_bfloat16* out;
+  void* out;              // bf16, or f16 with MQ_FWD_ACT_F16
   unsigned* status;
   // workspace views
   int32_t* sorted;        // [cap]

@@ -97,7 +97,12 @@ struct TcParams {
   const int32_t* offsets;       // [E + 1] padded expert segments (16-slot blocks)
   const int32_t* chunk_expert;  // expert of each token tile
   const int32_t* chunk_start;   // [E + 1] first token tile of each expert
-  const float* scale;     // int8: fp32 per-output-row scales of this GEMM's weights
+  const void* scale;      // 8-bit: scales of this GEMM's weights (kind below)
+  int scale_kind;         // 8-bit scales: 0 float32, 1 float16, 2 bfloat16
+  int scale_per_tensor;   // 8-bit: one scale per expert instead of one per row
+  uint32_t xmask;         // 8-bit codes: 0x80808080 for int8, 0 for uint8 (moe_wna16)
+  const uint8_t* zrow;    // 8-bit uint8 codes: zero point per row [E * rows], or null (128)
+  int rw_on_input;        // down GEMM: the router weight was applied to the input
   const __half* gscale;   // uint4: f16 group scales [rows, G]
   const uint8_t* gzero;   // uint4: zero points [rows / 2, G], even row in the low nibble
   int G;                  // uint4: groups per row (K / group_size)
@@ -246,23 +251,32 @@ __device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity) {
   }
 }
 
-// int8 x4 -> two f16x2 words, exact.  Flipping the sign bit gives u = x + 128
-// in [0, 255]; the half with bits 0x64uu is 1024 + u; subtracting 1152
-// leaves x.
-__device__ __forceinline__ void int8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  const uint32_t u = w ^ 0x80808080u;
+// 8-bit codes x4 -> two f16x2 words, exact.  xm = 0x80808080 turns an
+// int8 code into u = q + 128 (the sign bit flipped), xm = 0 keeps a uint8
+// code u; the half with bits 0x64uu is 1024 + u, and subtracting
+// zz = 1024 + z (z = 128, or the row's zero point) leaves u - z.
+__device__ __forceinline__ void int8x4_to_f16x4(uint32_t w, uint32_t xm, uint32_t zz,
+                                                uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ xm;
   const uint32_t v0 = __byte_perm(u, 0x64u, 0x4140);  // [u0, 0x64, u1, 0x64]
   const uint32_t v1 = __byte_perm(u, 0x64u, 0x4342);  // [u2, 0x64, u3, 0x64]
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(v0), "r"(0x64806480u));
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(v1), "r"(0x64806480u));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(v0), "r"(zz));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(v1), "r"(zz));
 }
 
-// 16 int8 -> 8 words of f16 pairs.
-__device__ __forceinline__ void convert16(const uint4& v, uint32_t* w) {
-  int8x4_to_f16x4(v.x, w[0], w[1]);
-  int8x4_to_f16x4(v.y, w[2], w[3]);
-  int8x4_to_f16x4(v.z, w[4], w[5]);
-  int8x4_to_f16x4(v.w, w[6], w[7]);
+// 16 codes -> 8 words of f16 pairs.
+__device__ __forceinline__ void convert16(const uint4& v, uint32_t xm, uint32_t zz, uint32_t* w) {
+  int8x4_to_f16x4(v.x, xm, zz, w[0], w[1]);
+  int8x4_to_f16x4(v.y, xm, zz, w[2], w[3]);
+  int8x4_to_f16x4(v.z, xm, zz, w[4], w[5]);
+  int8x4_to_f16x4(v.w, xm, zz, w[6], w[7]);
+}
+
+// 8-bit scale number i of this GEMM's weights, as float.
+__device__ __forceinline__ float load_scale(const TcParams& p, int64_t i) {
+  if (p.scale_kind == 1) return __half2float(static_cast<const __half*>(p.scale)[i]);
+  if (p.scale_kind == 2) return __bfloat162float(static_cast<const __nv_bfloat16*>(p.scale)[i]);
+  return static_cast<const float*>(p.scale)[i];
 }
 
 // Position of K index i inside its octet under the order [0,4,1,5,2,6,3,7]
@@ -568,6 +582,8 @@ __global__ void __launch_bounds__(TileCfg<BN>::kThreads, 1)
       // this thread's weight row (uint4 group scales and zero points)
       const int wrow = MODE == 1 ? w.e * 2 * p.I + ((lane & 1) ? p.I : 0) + w.mt * 64 + q * 16 + (lane >> 1)
                                  : w.e * p.H + w.mt * kTileM + r;
+      // 8-bit: 1024 + zero point of this row (128 unless uint8 codes carry zeros)
+      const uint32_t zz8 = (BITS == 8 && p.zrow) ? (0x6400u | p.zrow[wrow]) * 0x00010001u : 0x64806480u;
       for (int ks = ks0; ks < ks1; ks += kGA, ++st) {
         const int nk = min(kGA, ks1 - ks);
         if (st % kConvGroups != grp) continue;
@@ -599,7 +615,7 @@ __global__ void __launch_bounds__(TileCfg<BN>::kThreads, 1)
 #pragma unroll
               for (int c = 0; c < 4; ++c) {
                 // logical chunk 4h + c sits in x[4h + c] (rot 0) or x[(4h + c + 4) & 7] (rot 4)
-                convert16(sel4(rt, x[(4 * h + c + 4) & 7], x[4 * h + c]), &words[c * 8]);
+                convert16(sel4(rt, x[(4 * h + c + 4) & 7], x[4 * h + c]), p.xmask, zz8, &words[c * 8]);
               }
               tmem_st32(tbase + h * 32, words);
             }
@@ -676,7 +692,7 @@ __global__ void __launch_bounds__(TileCfg<BN>::kThreads, 1)
         const int i = q * 16 + (lane >> 1);
         const int wrow = w.e * 2 * p.I + (odd ? p.I : 0) + w.mt * 64 + i;
         // int8: per-channel scale here; uint4: group scales were applied to A
-        const float sc = BITS == 8 ? p.scale[wrow] : 1.0f;
+        const float sc = BITS == 8 ? load_scale(p, p.scale_per_tensor ? w.e : wrow) : 1.0f;
         // uint4 runs the down GEMM in the K order [0,4,1,5,2,6,3,7] per octet
         const int col = w.mt * 64 + q * 16 + (BITS == 8 ? (lane >> 1) : permute_octet(lane >> 1));
         auto body = [&](auto wtag, int c0) {
@@ -703,7 +719,8 @@ __global__ void __launch_bounds__(TileCfg<BN>::kThreads, 1)
         if (CH > 16 && c0 < w.n) body(IC<16>{}, c0);  // n is a multiple of 16
       } else {
         const int h = w.mt * kTileM + r;
-        const float sc = BITS == 8 ? p.scale[w.e * p.H + h] : 1.0f;
+        const float sc =
+            BITS == 8 ? load_scale(p, p.scale_per_tensor ? w.e : (int64_t)w.e * p.H + h) : 1.0f;
         float* yp = p.ypart + (int64_t)w.split * p.S * p.H;
         auto body = [&](auto wtag, int c0) {
           constexpr int W = decltype(wtag)::value;
@@ -714,7 +731,7 @@ __global__ void __launch_bounds__(TileCfg<BN>::kThreads, 1)
           if (lane < W) {
             const int prow = w.row0 + c0 + lane;
             slot = p.sorted[prow];
-            if (slot < p.S) f = p.xinv[prow] * p.topk_w[slot];
+            if (slot < p.S) f = p.xinv[prow] * (p.rw_on_input ? 1.0f : p.topk_w[slot]);
           }
           load_acc(wtag, c0, v);
 #pragma unroll
@@ -747,11 +764,30 @@ __global__ void __launch_bounds__(TileCfg<BN>::kThreads, 1)
 // [2^14, 2^15): bf16 -> f16 is then exact except for elements below 2^-28
 // of the row maximum (f16 subnormals).  xinv[p] = 2^-e undoes it in the
 // epilogue.  Padding rows are zeros.
+// 8 activations of one uint4 (bf16 or f16), times wmul.
+__device__ __forceinline__ void act8(const uint4& v, bool f16, float wmul, float* f) {
+  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    if (f16) {
+      const float2 t = __half22float2(*reinterpret_cast<const __half2*>(&u[j]));
+      f[2 * j] = t.x * wmul;
+      f[2 * j + 1] = t.y * wmul;
+    } else {
+      f[2 * j] = mq::bf16_lo(u[j]) * wmul;
+      f[2 * j + 1] = mq::bf16_hi(u[j]) * wmul;
+    }
+  }
+}
+
+// x is bf16, or f16 (act_f16); with rw (router weight on the input) each
+// slot's row is first multiplied by its router weight, in float32.
 template <bool PERM>
-__global__ void __launch_bounds__(128) gather_rows_f16(const __nv_bfloat16* __restrict__ x,
+__global__ void __launch_bounds__(128) gather_rows_f16(const void* __restrict__ xv,
                                                        const int32_t* __restrict__ sorted,
                                                        const int32_t* __restrict__ num_padded,
-                                                       int k, int S, int H,
+                                                       int k, int S, int H, int act_f16,
+                                                       const float* __restrict__ rw,
                                                        __half* __restrict__ xs,
                                                        float* __restrict__ xinv) {
   __shared__ float wmax[4];
@@ -767,13 +803,15 @@ __global__ void __launch_bounds__(128) gather_rows_f16(const __nv_bfloat16* __re
     if (threadIdx.x == 0) xinv[p] = 1.0f;
     return;
   }
-  const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)(s / k) * H);
+  const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(xv) + (int64_t)(s / k) * H);
+  const bool f16 = act_f16 != 0;
+  const float wmul = rw ? rw[s] : 1.0f;
   float m = 0.0f;
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    const uint4 v = src[i];
-    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+    float f[8];
+    act8(src[i], f16, wmul, f);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) m = fmaxf(m, fmaxf(fabsf(mq::bf16_lo(u[j])), fabsf(mq::bf16_hi(u[j]))));
+    for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(f[j]));
   }
 #pragma unroll
   for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -786,14 +824,10 @@ __global__ void __launch_bounds__(128) gather_rows_f16(const __nv_bfloat16* __re
   e = max(-120, min(120, e));
   const float scale = ldexpf(1.0f, e);
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    const uint4 v = src[i];
     float f[8];
-    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+    act8(src[i], f16, wmul, f);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      f[2 * j] = mq::bf16_lo(u[j]) * scale;
-      f[2 * j + 1] = mq::bf16_hi(u[j]) * scale;
-    }
+    for (int j = 0; j < 8; ++j) f[j] *= scale;
     uint32_t o[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -856,7 +890,7 @@ __global__ void __launch_bounds__(256) act_rows_to_f16(uint16_t* act, const int3
 __global__ void __launch_bounds__(256) combine_splits(const float* __restrict__ ypart,
                                                       const int32_t* __restrict__ ids, int T,
                                                       int k, int E, int H, int splits,
-                                                      __nv_bfloat16* __restrict__ out) {
+                                                      int out_f16, void* __restrict__ out) {
   const int64_t i4 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int H4 = H / 4;
   mq::pdl_wait();  // ypart comes from the previous kernel
@@ -878,12 +912,19 @@ __global__ void __launch_bounds__(256) combine_splits(const float* __restrict__ 
       acc.w += v.w;
     }
   }
-  __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-  __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
   uint2 o;
-  o.x = *reinterpret_cast<uint32_t*>(&lo);
-  o.y = *reinterpret_cast<uint32_t*>(&hi);
-  *reinterpret_cast<uint2*>(out + (int64_t)t * H + c) = o;
+  if (out_f16) {
+    __half2 lo = __floats2half2_rn(acc.x, acc.y);
+    __half2 hi = __floats2half2_rn(acc.z, acc.w);
+    o.x = *reinterpret_cast<uint32_t*>(&lo);
+    o.y = *reinterpret_cast<uint32_t*>(&hi);
+  } else {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+    o.x = *reinterpret_cast<uint32_t*>(&lo);
+    o.y = *reinterpret_cast<uint32_t*>(&hi);
+  }
+  *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + (int64_t)t * H + c) = o;
 }
 
 // ------------------------------------------------------------ host side --
@@ -998,6 +1039,8 @@ cudaError_t launch_gather_rows(const MoeArgs& a, void* xs, float* xinv, cudaStre
   const cudaError_t err = launch_pdl(
       a.bits == 8 ? gather_rows_f16<false> : gather_rows_f16<true>, dim3((unsigned)a.cap),
       dim3(128), 0, st, a.x, a.sorted, a.num_padded, a.k, a.T * a.k, a.H,
+      (a.flags & MQ_FWD_ACT_F16) ? 1 : 0,
+      (a.flags & MQ_FWD_ROUTER_WEIGHT_ON_INPUT) ? a.topk_w : (const float*)nullptr,
       static_cast<__half*>(xs), xinv);
   return err != cudaSuccess ? err : cudaGetLastError();
 }
@@ -1014,6 +1057,11 @@ void common_params(TcParams& p, const MoeArgs& a) {
   p.has_zp = a.has_zp;
   p.act = nullptr;
   p.ypart = nullptr;
+  p.scale_kind = (a.flags & MQ_FWD_SCALE_F16) ? 1 : (a.flags & MQ_FWD_SCALE_BF16) ? 2 : 0;
+  p.scale_per_tensor = (a.flags & MQ_FWD_SCALE_PER_TENSOR) ? 1 : 0;
+  p.xmask = (a.flags & MQ_FWD_W8_UINT8) ? 0u : 0x80808080u;
+  p.zrow = nullptr;
+  p.rw_on_input = (a.flags & MQ_FWD_ROUTER_WEIGHT_ON_INPUT) ? 1 : 0;
   p.xinv = nullptr;
   p.scale = nullptr;
   p.gscale = nullptr;
@@ -1053,7 +1101,8 @@ cudaError_t launch_gemm1_tc(const MoeArgs& a, const TcPlan& pl, const void* xs,
   p.MT = a.I / 64;
   p.splits = 1;
   if (a.bits == 8) {
-    p.scale = static_cast<const float*>(a.s13);
+    p.scale = a.s13;
+    p.zrow = a.has_zp ? a.z13 : nullptr;
   } else {
     p.gscale = static_cast<const __half*>(a.s13);
     p.gzero = a.z13;
@@ -1103,7 +1152,8 @@ cudaError_t launch_gemm2_tc(const MoeArgs& a, const TcPlan& pl, const float* act
   p.MT = a.H / kTileM;
   p.splits = pl.splits;
   if (a.bits == 8) {
-    p.scale = static_cast<const float*>(a.s2);
+    p.scale = a.s2;
+    p.zrow = a.has_zp ? a.z2 : nullptr;
   } else {
     p.gscale = static_cast<const __half*>(a.s2);
     p.gzero = a.z2;
@@ -1123,6 +1173,6 @@ cudaError_t launch_combine_splits(const MoeArgs& a, const float* ypart, int spli
   if (n == 0) return cudaSuccess;
   const cudaError_t err =
       launch_pdl(combine_splits, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, ypart,
-                 a.topk_ids, a.T, a.k, a.E, a.H, splits, a.out);
+                 a.topk_ids, a.T, a.k, a.E, a.H, splits, (a.flags & MQ_FWD_ACT_F16) ? 1 : 0, a.out);
   return err != cudaSuccess ? err : cudaGetLastError();
 }
