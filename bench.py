@@ -1,9 +1,10 @@
 #!/usr/bin/env python
 """Benchmark of the W8A16 / W4A16 fused-MoE layer forward (tokens/s).
 
-One step = one pass of the hot path over one synthetic batch: router
-(moe_topk_route) + moe_quant_forward (align, gate/up GEMM with fused dequant
-and SiLU-and-mul, down GEMM with fused dequant, weighted combine).  Weights
+One step = one pass of the hot path over one synthetic batch, as one call of
+moe_quant_forward_logits (router logits in: routing -- fused into the align
+kernel for small batches --, align, gate/up GEMM with fused dequant and
+SiLU-and-mul, down GEMM with fused dequant, weighted combine).  Weights
 are quantised once before timing (load time, as on the experts_int8 page).
 
 Default workload: the Mixtral-8x7B-shaped W8A16 layer (E=8, k=2, H=4096,
@@ -193,23 +194,24 @@ class Problem:
                 self.w[which] = (q, s, z)
             del bf
         torch.cuda.synchronize()
-        self.ws = torch.empty(max(mq.moe_quant_forward_workspace(T, H, I, E, wl.k, wl.bits,
-                                                                 wl.group_size), 16),
-                              dtype=torch.uint8, device=device)
+        ws = mq.lib().moe_quant_forward_logits_workspace(T, H, I, E, wl.k, wl.bits, wl.group_size)
+        self.ws = torch.empty(max(int(ws), 16), dtype=torch.uint8, device=device)
         self.out = torch.empty(T, H, dtype=torch.bfloat16, device=device)
-        self.tw = torch.empty(T, wl.k, dtype=torch.float32, device=device)
-        self.tid = torch.empty(T, wl.k, dtype=torch.int32, device=device)
+        # the routing of this batch, for the touched-expert count (the step
+        # routes inside the forward call)
+        self.tw, self.tid = mq.moe_topk_route(self.logits, wl.k, wl.renormalize)
 
     def step(self, x=None, logits=None):
         import weight_quantized_moe_gb300 as mq
         wl = self.wl
         x = self.x if x is None else x
         logits = self.logits if logits is None else logits
-        mq.moe_topk_route(logits, wl.k, wl.renormalize, self.tw, self.tid)
         (q13, s13, z13), (q2, s2, z2) = self.w["w13"], self.w["w2"]
-        mq.moe_quant_forward(x, q13, q2, s13, s2, self.tw, self.tid, bits=wl.bits,
-                             group_size=wl.group_size, has_zp=wl.has_zp, z13=z13, z2=z2,
-                             workspace=self.ws, out=self.out)
+        # ExpertsInt8MoEMethod.apply(x, router_logits, ...) as one call:
+        # routing, align, both expert GEMMs and the combine
+        mq.moe_quant_forward_logits(x, logits, q13, q2, s13, s2, wl.k, wl.renormalize,
+                                    bits=wl.bits, group_size=wl.group_size, has_zp=wl.has_zp,
+                                    z13=z13, z2=z2, workspace=self.ws, out=self.out)
         return self.out
 
     def touched_experts(self):

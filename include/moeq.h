@@ -242,6 +242,29 @@ int moe_quant_forward_ex(const void* x, int T, int H, int I, int E, int k,
                          void* out, unsigned flags, void* stream);
 
 /*
+ * moe_quant_forward_logits -- the whole of ExpertsInt8MoEMethod.apply(layer,
+ * x, router_logits, top_k, renormalize, ...) in one call: select_experts
+ * (softmax, top-k, optional renormalisation; moe_topk_route's arithmetic)
+ * followed by fused_experts (moe_quant_forward_ex).  router_logits float32
+ * [T, E] (device); the chosen weights and ids stay in the workspace.  When
+ * T * k * ceil(E / 32) <= 512 the routing runs inside the align kernel (one
+ * launch fewer); either way the result is bitwise that of moe_topk_route
+ * followed by moe_quant_forward_ex.  Other arguments, limits and errors as
+ * moe_quant_forward_ex; the workspace size comes from
+ * moe_quant_forward_logits_workspace.
+ */
+size_t moe_quant_forward_logits_workspace(int T, int H, int I, int E, int k,
+                                          int bits, int group_size);
+int moe_quant_forward_logits(const void* x, const float* router_logits,
+                             int T, int H, int I, int E, int k, int renormalize,
+                             int bits, int group_size, int has_zp,
+                             const void* w13, const void* w2,
+                             const void* s13, const void* s2,
+                             const uint8_t* z13, const uint8_t* z2,
+                             void* workspace, size_t ws_bytes,
+                             void* out, unsigned flags, void* stream);
+
+/*
  * moe_quant_forward_noalloc -- moe_quant_forward without a workspace
  * argument.  (The pages have no counterpart: their forward allocates its
  * intermediates through torch.)

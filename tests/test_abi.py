@@ -80,6 +80,12 @@ def test_host_side_rejections(lib):
     assert ex(*args(8, -1, 1, None, binding.MQ_FWD_W8_UINT8)) == 1
     assert ex(*args(8, -1, 0, None, 0, out=vp(0x1100))) == 1
     assert ex(*args(8, -1, 0, None, binding.MQ_FWD_ACT_F16, out=fake, ws=16)) == 4
+    # moe_quant_forward_logits: null logits; workspace query includes routing
+    assert lib.moe_quant_forward_logits(fake, None, 4, 128, 128, 8, 2, 1, 8, -1, 0, fake, fake,
+                                        fake, fake, None, None, fake, 1 << 30, vp(0x9000), 0,
+                                        None) == 1
+    assert (lib.moe_quant_forward_logits_workspace(64, 128, 128, 8, 2, 8, -1)
+            > lib.moe_quant_forward_workspace(64, 128, 128, 8, 2, 8, -1))
     # null pointers, odd rows, bad group size, k > 32
     assert lib.moe_quantize_int8_per_channel(None, 4, 8, fake, fake, None) == 1
     assert lib.moe_quantize_int8_per_channel(fake, 4, 12, fake, fake, None) == 1

@@ -151,3 +151,24 @@ def test_inplace_equals_out_of_place(dt):
     torch.cuda.synchronize()
     assert got.data_ptr() == xi.data_ptr()
     assert torch.equal(xi, ref)
+
+
+@pytest.mark.parametrize("name,T", [("tiny", 1), ("tiny", 37), ("fine", 1), ("fine", 64),
+                                    ("tiny", 1100), ("mixtral_decode", 8), ("mixtral_decode", 256)])
+@pytest.mark.parametrize("renorm", [True, False])
+def test_logits_forward_equals_route_then_forward(name, T, renorm):
+    """moe_quant_forward_logits (routing fused into the align kernel for
+    small batches, a separate router kernel otherwise) gives bitwise the
+    result of moe_topk_route followed by moe_quant_forward."""
+    from moe_helpers import Layer, inputs
+    layer = Layer(synth.WORKLOADS[name], seed=1)
+    layer.free_bf16()
+    x, lg = inputs(layer.wl, T, seed=T)
+    tw, tid = mq.moe_topk_route(lg, layer.k, renorm)
+    ref = layer.forward(x, tw, tid)
+    got = mq.moe_quant_forward_logits(x, lg, layer.q13, layer.q2, layer.s13, layer.s2, layer.k,
+                                      renorm, bits=layer.bits, group_size=layer.gs,
+                                      has_zp=layer.has_zp, z13=layer.z13, z2=layer.z2)
+    torch.cuda.synchronize()
+    assert mq.mq_device_status() == 0
+    assert torch.equal(got, ref)

@@ -16,6 +16,7 @@ from .binding import (  # noqa: F401
     moe_align_block,
     moe_align_capacity,
     moe_quant_forward,
+    moe_quant_forward_logits,
     moe_quant_forward_workspace,
     moe_quantize_int8_per_channel,
     moe_quantize_uint4_group,

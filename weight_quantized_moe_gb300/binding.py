@@ -44,6 +44,10 @@ _SIGNATURES = {
     "moe_quant_forward_ex": (_i32, [_vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
                                     _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp,
                                     ctypes.c_uint, _vp]),
+    "moe_quant_forward_logits_workspace": (_sz, [_i32] * 7),
+    "moe_quant_forward_logits": (_i32, [_vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
+                                        _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp,
+                                        ctypes.c_uint, _vp]),
     "moe_quant_forward_noalloc": (_i32, [_vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
                                          _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "mq_kernel_launch_count": (ctypes.c_longlong, []),
@@ -294,6 +298,40 @@ def moe_quant_forward(x, w13, w2, s13, s2, topk_w, topk_ids, bits=8, group_size=
         _ptr(x), T, H, I, E, k, bits, group_size, int(bool(has_zp)),
         _ptr(w13), _ptr(w2), _ptr(s13), _ptr(s2), _ptr(z13 if has_zp else None),
         _ptr(z2 if has_zp else None), _ptr(topk_w), _ptr(topk_ids),
+        _ptr(workspace), workspace.numel(), _ptr(out), flags, _stream(stream)))
+    return out
+
+
+def moe_quant_forward_logits(x, router_logits, w13, w2, s13, s2, top_k, renormalize=True, bits=8,
+                             group_size=-1, has_zp=False, z13=None, z2=None, workspace=None,
+                             out=None, stream=None, apply_router_weight_on_input=False,
+                             inplace=False):
+    """Routing and the expert MLP in one call (moe_quant_forward_logits in
+    include/moeq.h): the same result as moe_topk_route followed by
+    moe_quant_forward, bitwise."""
+    if x.dtype not in (torch.bfloat16, torch.float16):
+        raise TypeError(f"x must be bfloat16 or float16, got {x.dtype}")
+    _need(x, x.dtype, "x", 2)
+    _need(router_logits, torch.float32, "router_logits", 2)
+    T, H = x.shape
+    E = w13.shape[0]
+    I = w13.shape[1] // 2
+    if router_logits.shape != (T, E):
+        raise ValueError(f"router_logits must be [{T}, {E}]")
+    flags = forward_flags(x, w13, s13, bits, apply_router_weight_on_input)
+    ws_need = int(lib().moe_quant_forward_logits_workspace(T, H, I, E, top_k, bits, group_size))
+    if workspace is None:
+        workspace = torch.empty(max(ws_need, 16), dtype=torch.uint8, device=x.device)
+    _need(workspace, torch.uint8, "workspace")
+    if inplace:
+        out = x
+    if out is None:
+        out = torch.empty(T, H, dtype=x.dtype, device=x.device)
+    _need(out, x.dtype, "out", 2)
+    _check(lib().moe_quant_forward_logits(
+        _ptr(x), _ptr(router_logits), T, H, I, E, top_k, int(bool(renormalize)), bits, group_size,
+        int(bool(has_zp)), _ptr(w13), _ptr(w2), _ptr(s13), _ptr(s2),
+        _ptr(z13 if has_zp else None), _ptr(z2 if has_zp else None),
         _ptr(workspace), workspace.numel(), _ptr(out), flags, _stream(stream)))
     return out
 

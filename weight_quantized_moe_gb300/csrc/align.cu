@@ -16,18 +16,25 @@
 // chunks of at most `chunk` slots, the token tiles of the expert GEMMs:
 // chunk_start[e] = index of expert e's first chunk (chunk_start[E] = the
 // number of chunks) and chunk_expert[c] = the expert of chunk c.
+//
+// With PER > 0 it first routes the T tokens itself (router logits in, the
+// router's code, one warp per token), writing topk_w and the ids it then
+// aligns: at small batches one launch instead of two.
 #include "common.cuh"
+#include "route_core.cuh"
 
 namespace {
 
 constexpr int kWarps = 32;
 constexpr int kThreads = kWarps * 32;
 
+template <int PER>
 __global__ void __launch_bounds__(kThreads, 1)
-    align_kernel(const int32_t* __restrict__ ids, int S, int E, int bm, int32_t* __restrict__ sorted,
+    align_kernel(int32_t* __restrict__ ids, int S, int E, int bm, int32_t* __restrict__ sorted,
                  int32_t* __restrict__ block_expert, int32_t* __restrict__ offsets,
                  int32_t* __restrict__ num_padded, int chunk, int32_t* __restrict__ chunk_expert,
-                 int32_t* __restrict__ chunk_start, unsigned* status) {
+                 int32_t* __restrict__ chunk_start, const float* __restrict__ logits, int T,
+                 int k, int renorm, float* __restrict__ topk_w, unsigned* status) {
   extern __shared__ int smem[];
   int* hist = smem;                   // [kWarps][E]
   int* warp_tot = smem + kWarps * E;  // [kWarps] scan scratch
@@ -37,9 +44,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = tid & 31;
 
   for (int i = tid; i < kWarps * E; i += kThreads) hist[i] = 0;
-  mq::pdl_wait();  // the ids come from the previous kernel
+  mq::pdl_wait();  // the ids (or logits) come from the previous kernel
   mq::pdl_trigger();
-  __syncthreads();
+  if constexpr (PER > 0) {
+    float* s_val = reinterpret_cast<float*>(warp_tot2 + kWarps) + warp * 32;
+    int* s_idx = warp_tot2 + kWarps + kWarps * 32 + warp * 32;
+    for (int t = warp; t < T; t += kWarps)
+      mq::route_token<PER>(logits + (int64_t)t * E, E, k, renorm, s_val, s_idx,
+                           topk_w + (int64_t)t * k, ids + (int64_t)t * k);
+  }
+  __syncthreads();  // (ids written by this block are visible to all of it)
 
   const int per_warp = (S + kWarps - 1) / kWarps;
   const int begin = warp * per_warp;
@@ -146,18 +160,64 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
+namespace {
+
+template <int PER>
+cudaError_t launch_align_impl(int32_t* ids, int T, int k, int E, int bm, int32_t* sorted,
+                              int32_t* block_expert, int32_t* offsets, int32_t* num_padded,
+                              unsigned* status, cudaStream_t st, int chunk, int32_t* chunk_expert,
+                              int32_t* chunk_start, const float* logits, int renorm,
+                              float* topk_w) {
+  size_t smem = (size_t)(kWarps * E + 2 * kWarps) * sizeof(int);
+  if (PER > 0) smem += (size_t)kWarps * 32 * (sizeof(float) + sizeof(int));  // routing scratch
+  auto kern = align_kernel<PER>;
+  if (smem > 48 * 1024) {
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)smem);
+    if (err != cudaSuccess) return err;
+  }
+  const cudaError_t err =
+      launch_pdl(kern, dim3(1), dim3(kThreads), smem, st, ids, T * k, E, bm, sorted,
+                 block_expert, offsets, num_padded, chunk, chunk_expert, chunk_start, logits, T, k,
+                 renorm, topk_w, status);
+  return err != cudaSuccess ? err : cudaGetLastError();
+}
+
+}  // namespace
+
 cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int bm, int32_t* sorted,
                          int32_t* block_expert, int32_t* offsets, int32_t* num_padded,
                          unsigned* status, cudaStream_t st, int chunk, int32_t* chunk_expert,
                          int32_t* chunk_start) {
-  const size_t smem = (size_t)(kWarps * E + 2 * kWarps) * sizeof(int);
-  if (smem > 48 * 1024) {
-    cudaError_t err =
-        cudaFuncSetAttribute(align_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  return launch_align_impl<0>(const_cast<int32_t*>(ids), T, k, E, bm, sorted, block_expert,
+                              offsets, num_padded, status, st, chunk, chunk_expert, chunk_start,
+                              nullptr, 0, nullptr);
+}
+
+cudaError_t launch_route_align(const float* logits, int renorm, float* topk_w, int32_t* topk_ids,
+                               int T, int k, int E, int bm, int32_t* sorted,
+                               int32_t* block_expert, int32_t* offsets, int32_t* num_padded,
+                               unsigned* status, cudaStream_t st, int chunk,
+                               int32_t* chunk_expert, int32_t* chunk_start) {
+  if (!route_fused(T, k, E)) {
+    const cudaError_t err = launch_route(logits, T, E, k, renorm, topk_w, topk_ids, st);
     if (err != cudaSuccess) return err;
+    return launch_align(topk_ids, T, k, E, bm, sorted, block_expert, offsets, num_padded, status,
+                        st, chunk, chunk_expert, chunk_start);
   }
-  const cudaError_t err =
-      launch_pdl(align_kernel, dim3(1), dim3(kThreads), smem, st, ids, T * k, E, bm, sorted,
-                 block_expert, offsets, num_padded, chunk, chunk_expert, chunk_start, status);
-  return err != cudaSuccess ? err : cudaGetLastError();
+  const int per = (E + 31) / 32;
+#define MQ_RA(P)                                                                               \
+  return launch_align_impl<P>(topk_ids, T, k, E, bm, sorted, block_expert, offsets, num_padded, \
+                              status, st, chunk, chunk_expert, chunk_start, logits, renorm,      \
+                              topk_w);
+  switch (per) {
+    case 1: MQ_RA(1)
+    case 2: MQ_RA(2)
+    case 3: MQ_RA(3)
+    case 4: MQ_RA(4)
+    case 5: case 6: case 7: case 8: MQ_RA(8)
+    case 9: case 10: case 11: case 12: case 13: case 14: case 15: case 16: MQ_RA(16)
+    default: MQ_RA(32)
+  }
+#undef MQ_RA
 }

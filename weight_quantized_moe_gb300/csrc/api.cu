@@ -107,12 +107,14 @@ constexpr int kAlignBlock = 16;
 
 struct WsLayout {
   size_t sorted, block_expert, offsets, num_padded, chunk_expert, chunk_start, xs, xinv, act,
-      act_inv, y, total;
+      act_inv, y, topk_w, topk_ids, total;
   int64_t cap;
   TcPlan plan;
 };
 
-WsLayout ws_layout(int T, int H, int I, int E, int k, int bits) {
+// with_route: the forward routes itself (router logits in), holding topk_w
+// and topk_ids in the workspace too.
+WsLayout ws_layout(int T, int H, int I, int E, int k, int bits, bool with_route = false) {
   WsLayout L;
   L.plan = tc_plan(T, H, I, E, k, bits);
   const int bm = kAlignBlock;
@@ -131,6 +133,8 @@ WsLayout ws_layout(int T, int H, int I, int E, int k, int bits) {
   L.act = off;          off += align256(sizeof(__nv_bfloat16) * (size_t)cap * (size_t)I);
   L.act_inv = off;      off += align256(sizeof(float) * (size_t)cap);
   L.y = off;            off += align256(sizeof(float) * (size_t)L.plan.splits * (size_t)S * (size_t)H);
+  L.topk_w = off;       if (with_route) off += align256(sizeof(float) * (size_t)S);
+  L.topk_ids = off;     if (with_route) off += align256(sizeof(int32_t) * (size_t)S);
   L.total = off;
   return L;
 }
@@ -310,12 +314,14 @@ MQ_EXPORT int moe_quant_forward(const void* x, int T, int H, int I, int E, int k
                               z2, topk_w, topk_ids, workspace, ws_bytes, out, 0u, stream);
 }
 
-MQ_EXPORT int moe_quant_forward_ex(const void* x, int T, int H, int I, int E, int k, int bits,
-                                   int group_size, int has_zp, const void* w13, const void* w2,
-                                   const void* s13, const void* s2, const uint8_t* z13,
-                                   const uint8_t* z2, const float* topk_w,
-                                   const int32_t* topk_ids, void* workspace, size_t ws_bytes,
-                                   void* out, unsigned flags, void* stream) {
+// The forward.  With logits (router logits [T, E]) it routes itself, into
+// the workspace; otherwise topk_w / topk_ids are the caller's.
+static int forward_impl(const void* x, int T, int H, int I, int E, int k, int bits,
+                        int group_size, int has_zp, const void* w13, const void* w2,
+                        const void* s13, const void* s2, const uint8_t* z13, const uint8_t* z2,
+                        const float* topk_w, const int32_t* topk_ids, const float* logits,
+                        int renorm, void* workspace, size_t ws_bytes, void* out, unsigned flags,
+                        void* stream) {
   constexpr unsigned kW8Flags = MQ_FWD_W8_UINT8 | MQ_FWD_SCALE_F16 | MQ_FWD_SCALE_BF16 |
                                 MQ_FWD_SCALE_PER_TENSOR;
   constexpr unsigned kAllFlags = kW8Flags | MQ_FWD_ACT_F16 | MQ_FWD_ROUTER_WEIGHT_ON_INPUT;
@@ -336,7 +342,8 @@ MQ_EXPORT int moe_quant_forward_ex(const void* x, int T, int H, int I, int E, in
     return fail(MQ_ERR_UNSUPPORTED, "group_size must divide H and I");
   if ((int64_t)T * k > (int64_t(1) << 24)) return fail(MQ_ERR_UNSUPPORTED, "too many token-slots");
   if (T == 0) return MQ_OK;
-  if (!x || !w13 || !w2 || !s13 || !s2 || !topk_w || !topk_ids || !out || !workspace)
+  if (!x || !w13 || !w2 || !s13 || !s2 || !out || !workspace ||
+      (logits ? false : (!topk_w || !topk_ids)))
     return fail(MQ_ERR_INVALID_ARG, "null pointer");
   if (has_zp && (!z13 || !z2)) return fail(MQ_ERR_INVALID_ARG, "null zero points");
   if (!has_zp && (z13 || z2)) return fail(MQ_ERR_INVALID_ARG, "zero points given with has_zp = 0");
@@ -351,13 +358,19 @@ MQ_EXPORT int moe_quant_forward_ex(const void* x, int T, int H, int I, int E, in
     if (ob != xb && ob < xb + nb && xb < ob + nb)
       return fail(MQ_ERR_INVALID_ARG, "out overlaps x (only out == x is allowed)");
   }
-  const WsLayout L = ws_layout(T, H, I, E, k, bits);
+  const WsLayout L = ws_layout(T, H, I, E, k, bits, logits != nullptr);
   const int bm = kAlignBlock;
   if (ws_bytes < L.total)
     return fail(MQ_ERR_WORKSPACE, "workspace %zu bytes, need %zu", ws_bytes, L.total);
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
+  float* rw = logits ? reinterpret_cast<float*>(ws + L.topk_w) : nullptr;
+  int32_t* rid = logits ? reinterpret_cast<int32_t*>(ws + L.topk_ids) : nullptr;
+  if (logits) {
+    topk_w = rw;
+    topk_ids = rid;
+  }
   MoeArgs a;
   a.x = x;
   a.flags = flags;
@@ -379,10 +392,20 @@ MQ_EXPORT int moe_quant_forward_ex(const void* x, int T, int H, int I, int E, in
   a.cap = L.cap;
 
   cudaError_t err;
+  if (logits && !route_fused(T, k, E)) {  // larger batches: the router kernel first
+    LaunchScope ls(MQ_PROF_ROUTE, st);
+    err = launch_route(logits, T, E, k, renorm, rw, rid, st);
+    if (err != cudaSuccess) return cuda_fail(err, "forward: route launch");
+  }
   {
     LaunchScope ls(MQ_PROF_ALIGN, st);
-    err = launch_align(topk_ids, T, k, E, bm, a.sorted, a.block_expert, a.offsets, a.num_padded,
-                       a.status, st, L.plan.bn, a.chunk_expert, a.chunk_start);
+    if (logits && route_fused(T, k, E))  // routing fused into the align kernel
+      err = launch_route_align(logits, renorm, rw, rid, T, k, E, bm, a.sorted, a.block_expert,
+                               a.offsets, a.num_padded, a.status, st, L.plan.bn, a.chunk_expert,
+                               a.chunk_start);
+    else
+      err = launch_align(topk_ids, T, k, E, bm, a.sorted, a.block_expert, a.offsets,
+                         a.num_padded, a.status, st, L.plan.bn, a.chunk_expert, a.chunk_start);
   }
   if (err != cudaSuccess) return cuda_fail(err, "forward: align launch");
   void* xs = ws + L.xs;
@@ -414,4 +437,33 @@ MQ_EXPORT int moe_quant_forward_ex(const void* x, int T, int H, int I, int E, in
   }
   if (err != cudaSuccess) return cuda_fail(err, "forward: combine launch");
   return MQ_OK;
+}
+
+MQ_EXPORT int moe_quant_forward_ex(const void* x, int T, int H, int I, int E, int k, int bits,
+                                   int group_size, int has_zp, const void* w13, const void* w2,
+                                   const void* s13, const void* s2, const uint8_t* z13,
+                                   const uint8_t* z2, const float* topk_w,
+                                   const int32_t* topk_ids, void* workspace, size_t ws_bytes,
+                                   void* out, unsigned flags, void* stream) {
+  return forward_impl(x, T, H, I, E, k, bits, group_size, has_zp, w13, w2, s13, s2, z13, z2,
+                      topk_w, topk_ids, nullptr, 0, workspace, ws_bytes, out, flags, stream);
+}
+
+MQ_EXPORT size_t moe_quant_forward_logits_workspace(int T, int H, int I, int E, int k, int bits,
+                                                    int group_size) {
+  if (T < 0 || H <= 0 || I <= 0 || E < 1 || k < 1 || k > E) return 0;
+  if (!fmt_ok(bits, group_size, 0)) return 0;
+  return ws_layout(T, H, I, E, k, bits, true).total;
+}
+
+MQ_EXPORT int moe_quant_forward_logits(const void* x, const float* router_logits, int T, int H,
+                                       int I, int E, int k, int renormalize, int bits,
+                                       int group_size, int has_zp, const void* w13,
+                                       const void* w2, const void* s13, const void* s2,
+                                       const uint8_t* z13, const uint8_t* z2, void* workspace,
+                                       size_t ws_bytes, void* out, unsigned flags, void* stream) {
+  if (T > 0 && !router_logits) return fail(MQ_ERR_INVALID_ARG, "null router_logits");
+  return forward_impl(x, T, H, I, E, k, bits, group_size, has_zp, w13, w2, s13, s2, z13, z2,
+                      nullptr, nullptr, router_logits, renormalize, workspace, ws_bytes, out,
+                      flags, stream);
 }

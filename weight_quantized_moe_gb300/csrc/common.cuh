@@ -78,6 +78,22 @@ MQ_HIDDEN cudaError_t launch_quant_uint4(const void* w, int64_t rows, int64_t co
                                          uint8_t* qw, uint16_t* sc, uint8_t* qz, cudaStream_t st);
 MQ_HIDDEN cudaError_t launch_route(const float* logits, int T, int E, int k, int renorm,
                                    float* topk_w, int32_t* topk_ids, cudaStream_t st);
+// Router logits -> topk_w / topk_ids -> align as one kernel (the align
+// kernel's 32 warps route first) when the routing work is small enough for
+// one CTA: tokens x k argmax rounds over ceil(E / 32) registers per lane at
+// most kFusedRouteWork (measured: Mixtral-shaped E=8, k=2 gains up to 5 us
+// at T <= 64; E=128, k=8 at T=64 loses 2.4 us).  Otherwise the router kernel
+// runs first.
+constexpr int kFusedRouteWork = 512;
+inline bool route_fused(int T, int k, int E) {
+  return (int64_t)T * k * ((E + 31) / 32) <= kFusedRouteWork;
+}
+MQ_HIDDEN cudaError_t launch_route_align(const float* logits, int renorm, float* topk_w,
+                                         int32_t* topk_ids, int T, int k, int E, int bm,
+                                         int32_t* sorted, int32_t* block_expert,
+                                         int32_t* offsets, int32_t* num_padded, unsigned* status,
+                                         cudaStream_t st, int chunk, int32_t* chunk_expert,
+                                         int32_t* chunk_start);
 // chunk > 0 also writes the chunk table of the expert GEMMs' token tiles
 // (chunk_expert [cap / bm], chunk_start [E + 1]).
 MQ_HIDDEN cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int bm,
