@@ -505,8 +505,14 @@ __global__ void __launch_bounds__(TileCfg<BN>::kThreads, 1)
     // accumulates them into half ip of the unit's accumulator buffer.
     if (lane == 0) {
       constexpr uint32_t kBoxD = (uint32_t)(kBBytesK / 2) >> 4;  // one 64-K activation box
+      constexpr uint32_t kStageD = (uint32_t)kBBytes >> 4;        // one activation stage
+      // descriptor of stage 0's first K slice; stage d's differs only in the
+      // start-address field (address >> 4, no carry below 256 KB)
+      const uint64_t b_desc0 = smem_desc_k_sw128(smem_addr(sB));
       const int ip = warp == 1 ? 0 : 1;
       int st = 0, t = 0;
+      int d = 0;         // stage of step st (st % ND), advanced without a division
+      uint32_t ph = 0;   // its barrier parity ((st / ND) & 1)
       bool ok = true;
       for (int u = blockIdx.x; u < total && ok; u += gridDim.x, ++t) {
         const Unit w = cta_unit<BN>(p, ulist, t, u);
@@ -519,17 +525,20 @@ __global__ void __launch_bounds__(TileCfg<BN>::kThreads, 1)
         const uint32_t d_tmem = tmem + (buf * C::kNI + ip) * BN;
         uint32_t acc = 0;  // the first step of this issuer in the unit overwrites
         for (int ks = ks0; ks < ks1; ks += kGA, ++st) {
+          const int dc = d;
+          const uint32_t phc = ph;
+          if (++d == ND) {
+            d = 0;
+            ph ^= 1u;
+          }
           if (C::kNI == 2 && (st & 1) != ip) continue;
           const int nmma = min(kGA, ks1 - ks) * kEntryK / 16;  // K = 16 per MMA
-          const int d = st % ND;
-          ok = wait_bounded(&ctl->afull[d], (st / ND) & 1, ctl, p.status);
+          ok = wait_bounded(&ctl->afull[dc], phc, ctl, p.status);
           if (!ok) break;
           tc_fence_after();
-          // descriptor of the step's first K slice; the others differ only in
-          // the start-address field (address >> 4, no carry below 256 KB):
           // four K slices of 16 (32 bytes) per 64-K activation box
-          const uint64_t b_desc = smem_desc_k_sw128(smem_addr(sB + d * kBBytes));
-          const uint32_t a_tmem = tmem + kACol0 + d * kAColsPerStep;
+          const uint64_t b_desc = b_desc0 + (uint64_t)(dc * kStageD);
+          const uint32_t a_tmem = tmem + kACol0 + dc * kAColsPerStep;
           if (nmma == 16) {
             mma_ts_x16<2, 4, 6, kBoxD, kBoxD + 2, kBoxD + 4, kBoxD + 6, 2 * kBoxD, 2 * kBoxD + 2,
                        2 * kBoxD + 4, 2 * kBoxD + 6, 3 * kBoxD, 3 * kBoxD + 2, 3 * kBoxD + 4,
@@ -540,7 +549,7 @@ __global__ void __launch_bounds__(TileCfg<BN>::kThreads, 1)
                      kIdesc, kk > 0 ? 1u : acc);
           }
           acc = 1;
-          mma_commit(&ctl->stepfree[d]);
+          mma_commit(&ctl->stepfree[dc]);
         }
         if (!ok) break;
         mma_commit(&ctl->accfull[buf]);
