@@ -166,3 +166,42 @@ def test_forward_mixtral_decode_sampled():
     layer = Layer(W["mixtral_decode"], seed=0)
     cols = np.sort(np.random.default_rng(0).choice(4096, 512, replace=False))
     assert _run(layer, 64, seed=0, tokens=[5, 40], out_cols=cols) <= FWD_TOL
+
+
+def test_forward_captures_into_a_cuda_graph():
+    """The whole forward (routing included) launches only kernels, with no
+    host synchronisation or allocation, so it can be captured into a CUDA
+    graph; replays reproduce the eager result bitwise."""
+    layer = Layer(W["mixtral_decode"], seed=0)
+    layer.free_bf16()
+    x, lg = inputs(layer.wl, 8, seed=12)
+    ws = torch.empty(mq.lib().moe_quant_forward_logits_workspace(8, layer.H, layer.I, layer.E,
+                                                                 layer.k, 8, -1),
+                     dtype=torch.uint8, device="cuda")
+    out = torch.empty(8, layer.H, dtype=torch.bfloat16, device="cuda")
+    fwd = lambda: mq.moe_quant_forward_logits(x, lg, layer.q13, layer.q2, layer.s13, layer.s2,
+                                              layer.k, True, workspace=ws, out=out)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fwd()
+    torch.cuda.current_stream().wait_stream(s)
+    ref = out.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fwd()
+    out.zero_()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert mq.mq_device_status() == 0
+    assert torch.equal(out, ref)
+
+
+@pytest.mark.parametrize("E,k,T", [(1024, 32, 5), (1024, 1, 16), (33, 32, 3)])
+def test_forward_maximum_experts_and_top_k(E, k, T):
+    """The ABI limits: E = 1024 experts, top_k = 32 (and k = E - 1 < 32
+    with an odd expert count)."""
+    wl = synth.Workload("edge", E=E, k=k, H=128, I=128, Ts=(T,))
+    layer = Layer(wl, seed=4)
+    assert _run(layer, T, seed=E + k) <= FWD_TOL
