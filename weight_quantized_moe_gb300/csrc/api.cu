@@ -421,11 +421,11 @@ static int forward_impl(const void* x, int T, int H, int I, int E, int k, int bi
   }
   if (err != cudaSuccess) return cuda_fail(err, "forward: gate/up GEMM launch");
   float* act_inv = reinterpret_cast<float*>(ws + L.act_inv);
-  {
+  if (bits == 4) {  // the uint4 down GEMM runs f16 operands; the 8-bit one reads bf16 act
     LaunchScope ls(MQ_PROF_ACTF16, st);
     err = launch_act_to_f16(a, act_inv, st);
+    if (err != cudaSuccess) return cuda_fail(err, "forward: act conversion launch");
   }
-  if (err != cudaSuccess) return cuda_fail(err, "forward: act conversion launch");
   {
     LaunchScope ls(MQ_PROF_GEMM2, st);
     err = launch_gemm2_tc(a, L.plan, act_inv, a.y, st);

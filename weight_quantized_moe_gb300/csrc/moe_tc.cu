@@ -272,6 +272,42 @@ __device__ __forceinline__ void convert16(const uint4& v, uint32_t xm, uint32_t 
   int8x4_to_f16x4(v.w, xm, zz, w[6], w[7]);
 }
 
+// (a0 - b, a1 - b) as one paired f32 subtraction (sm_100 family).
+__device__ __forceinline__ void f32x2_sub(float a0, float a1, float b, float& r0, float& r1) {
+  asm("{.reg .b64 xa, xb, xd;\n\t"
+      "mov.b64 xa, {%2, %3};\n\t"
+      "mov.b64 xb, {%4, %4};\n\t"
+      "sub.rn.f32x2 xd, xa, xb;\n\t"
+      "mov.b64 {%0, %1}, xd;}"
+      : "=f"(r0), "=f"(r1)
+      : "f"(a0), "f"(a1), "f"(b));
+}
+
+// 8-bit codes x4 -> two bf16x2 words, exact.  u = code ^ xm as above; the
+// float with bits 0x4B0000uu is 2^23 + u, and subtracting zf = 2^23 + z
+// leaves u - z exactly; |u - z| < 256 has at most 8 significant bits, so the
+// top 16 bits of that float are the exact bfloat16.  (Measured faster than
+// building 128 + (u & 127) and 128 or 256 as bfloat16 and subtracting those.)
+__device__ __forceinline__ void int8x4_to_bf16x4(uint32_t w, uint32_t xm, float zf, uint32_t& lo,
+                                                 uint32_t& hi) {
+  const uint32_t u = w ^ xm;
+  float f0, f1, f2, f3;
+  f32x2_sub(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7440)),
+            __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7441)), zf, f0, f1);
+  f32x2_sub(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7442)),
+            __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7443)), zf, f2, f3);
+  lo = __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632);
+  hi = __byte_perm(__float_as_uint(f2), __float_as_uint(f3), 0x7632);
+}
+
+// 16 codes -> 8 words of bf16 pairs.
+__device__ __forceinline__ void convert16_bf16(const uint4& v, uint32_t xm, float zf, uint32_t* w) {
+  int8x4_to_bf16x4(v.x, xm, zf, w[0], w[1]);
+  int8x4_to_bf16x4(v.y, xm, zf, w[2], w[3]);
+  int8x4_to_bf16x4(v.z, xm, zf, w[4], w[5]);
+  int8x4_to_bf16x4(v.w, xm, zf, w[6], w[7]);
+}
+
 // 8-bit scale number i of this GEMM's weights, as float.
 __device__ __forceinline__ float load_scale(const TcParams& p, int64_t i) {
   if (p.scale_kind == 1) return __half2float(static_cast<const __half*>(p.scale)[i]);
@@ -361,7 +397,10 @@ __global__ void __launch_bounds__(TileCfg<BN>::kThreads, 1)
   // MMAs always run N = BN: a token tile's rows past its n belong to other
   // tiles (or are zero fill), and the accumulator columns they produce are
   // never read.  A compile-time descriptor keeps the issue loop short.
-  constexpr uint32_t kIdesc = idesc_f16_f32(kTileM, BN);
+  // The 8-bit down GEMM reads act as written, in bf16 (weights converted to
+  // bf16, exactly); every other GEMM runs f16 operands.
+  constexpr bool kBf16 = MODE == 2 && BITS == 8;
+  constexpr uint32_t kIdesc = kBf16 ? idesc_bf16_f32(kTileM, BN) : idesc_f16_f32(kTileM, BN);
   static_assert(NA <= 16, "ring sizes");
 
   extern __shared__ uint8_t smem_raw[];
@@ -593,6 +632,7 @@ __global__ void __launch_bounds__(TileCfg<BN>::kThreads, 1)
                                  : w.e * p.H + w.mt * kTileM + r;
       // 8-bit: 1024 + zero point of this row (128 unless uint8 codes carry zeros)
       const uint32_t zz8 = (BITS == 8 && p.zrow) ? (0x6400u | p.zrow[wrow]) * 0x00010001u : 0x64806480u;
+      const float zf8 = 8388608.0f + (float)((BITS == 8 && p.zrow) ? p.zrow[wrow] : 128u);
       for (int ks = ks0; ks < ks1; ks += kGA, ++st) {
         const int nk = min(kGA, ks1 - ks);
         if (st % kConvGroups != grp) continue;
@@ -624,7 +664,9 @@ __global__ void __launch_bounds__(TileCfg<BN>::kThreads, 1)
 #pragma unroll
               for (int c = 0; c < 4; ++c) {
                 // logical chunk 4h + c sits in x[4h + c] (rot 0) or x[(4h + c + 4) & 7] (rot 4)
-                convert16(sel4(rt, x[(4 * h + c + 4) & 7], x[4 * h + c]), p.xmask, zz8, &words[c * 8]);
+                const uint4 cv = sel4(rt, x[(4 * h + c + 4) & 7], x[4 * h + c]);
+                if constexpr (kBf16) convert16_bf16(cv, p.xmask, zf8, &words[c * 8]);
+                else convert16(cv, p.xmask, zz8, &words[c * 8]);
               }
               tmem_st32(tbase + h * 32, words);
             }
@@ -740,7 +782,7 @@ __global__ void __launch_bounds__(TileCfg<BN>::kThreads, 1)
           if (lane < W) {
             const int prow = w.row0 + c0 + lane;
             slot = p.sorted[prow];
-            if (slot < p.S) f = p.xinv[prow] * (p.rw_on_input ? 1.0f : p.topk_w[slot]);
+            if (slot < p.S) f = (kBf16 ? 1.0f : p.xinv[prow]) * (p.rw_on_input ? 1.0f : p.topk_w[slot]);
           }
           load_acc(wtag, c0, v);
 #pragma unroll
@@ -849,9 +891,10 @@ __global__ void __launch_bounds__(128) gather_rows_f16(const void* __restrict__ 
   if (threadIdx.x == 0) xinv[p] = ldexpf(1.0f, -e);
 }
 
-// act rows [0, num_padded) converted in place from bf16 to f16, each row
-// scaled by a power of two 2^e so that its largest magnitude lands in
-// [2^14, 2^15) (exact, as in gather_rows_f16); xinv[p] = 2^-e.
+// uint4 weights (f16 down-GEMM operands): act rows [0, num_padded)
+// converted in place from bf16 to f16, each row scaled by a power of two 2^e
+// so that its largest magnitude lands in [2^14, 2^15) (exact, as in
+// gather_rows_f16); xinv[p] = 2^-e.
 __global__ void __launch_bounds__(256) act_rows_to_f16(uint16_t* act, const int32_t* num_padded,
                                                        int I, float* __restrict__ xinv) {
   __shared__ float wmax[8];
@@ -1151,7 +1194,10 @@ cudaError_t launch_gemm2_tc(const MoeArgs& a, const TcPlan& pl, const float* act
     const cuuint64_t dims[2] = {(cuuint64_t)a.I, (cuuint64_t)a.cap};
     const cuuint64_t strides[1] = {(cuuint64_t)a.I * 2};
     const cuuint32_t box[2] = {64, (cuuint32_t)pl.bn};
-    err = make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.act, dims, strides, box,
+    // act: bf16 as written by the gate/up GEMM (8-bit), or f16 after the
+    // in-place conversion (uint4)
+    err = make_map(&tb, a.bits == 8 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                   2, a.act, dims, strides, box,
                    CU_TENSOR_MAP_SWIZZLE_128B);
     if (err != cudaSuccess) return err;
   }
