@@ -39,6 +39,7 @@ from .moe_oracle import (  # noqa: F401
     dequantize_uint4_group,
     dequantize_uint8_per_channel,
     topk_route,
+    topk_route_ex,
     align_capacity,
     align_block,
     silu,

@@ -210,6 +210,96 @@ def topk_route(logits, k, renormalize):
     return w, ids
 
 
+def _scores_f32(logits, scoring_func):
+    """Float32 scores of every expert, in the order the router kernel forms
+    them: softmax as exp(l - max) / sum, sigmoid as 1 / (1 + exp(-l))."""
+    l32 = np.asarray(logits, dtype=_F32)
+    if scoring_func == "softmax":
+        ex = np.exp(l32 - l32.max(axis=1, keepdims=True))
+        return ex / ex.sum(axis=1, keepdims=True, dtype=_F32)
+    return _F32(1) / (_F32(1) + np.exp(-l32))
+
+
+def topk_route_ex(logits, k, renormalize, scoring_func="softmax", num_expert_group=0,
+                  topk_group=0, e_score_correction_bias=None, routed_scaling_factor=1.0):
+    """Router with the extra select_experts arguments: returns (topk_weights
+    float64 [T, k], topk_ids int32 [T, k]).
+
+    ``ExpertsInt8MoEMethod.apply`` and ``MoeWNA16Method.apply_monolithic``
+    hand ``scoring_func``, ``use_grouped_topk`` / ``num_expert_group`` /
+    ``topk_group``, ``e_score_correction_bias`` and
+    ``routed_scaling_factor`` to the router; the pages name them and give no
+    arithmetic.  Reading, step by step:
+
+    1. Score s_e of each expert: softmax over the token's E logits, or
+       sigmoid(logit_e) when ``scoring_func == "sigmoid"``.
+    2. Selection key c_e: the logit itself when there is no correction bias
+       (either score is increasing in the logit, so this is the order of
+       s_e); with a bias b, c_e = s_e + b_e, formed in float32, the
+       precision the router kernel decides in.
+    3. Grouping (``num_expert_group`` G > 1): experts [gE/G, (g+1)E/G) form
+       group g, whose score is the largest key in it.  The ``topk_group``
+       groups with the largest scores (ties: lower group) stay; every expert
+       of the other groups is out.
+    4. Of the experts left, the k with the largest keys (ties: lower index)
+       fill slots j = 0..k-1 from the largest key down.
+    5. Weight j = s_{id_j}: the bias steers the choice only.  With
+       ``renormalize`` it is divided by the sum over the k chosen; then it is
+       multiplied by ``routed_scaling_factor``.
+
+    With the defaults this is ``topk_route``.
+    """
+    logits = np.asarray(logits, dtype=_F32)
+    T, E = logits.shape
+    if scoring_func not in ("softmax", "sigmoid"):
+        raise ValueError("scoring_func must be 'softmax' or 'sigmoid'")
+    if not 1 <= k <= E:
+        raise ValueError("need 1 <= k <= E")
+    G = num_expert_group if num_expert_group and num_expert_group > 1 else 1
+    if G > 1:
+        if E % G:
+            raise ValueError("num_expert_group must divide E")
+        if not 1 <= topk_group <= G:
+            raise ValueError("need 1 <= topk_group <= num_expert_group")
+        if k > topk_group * (E // G):
+            raise ValueError("k exceeds the experts of the kept groups")
+
+    # step 1, float64 (the weights); step 2, the keys
+    l64 = logits.astype(np.float64)
+    if scoring_func == "softmax":
+        ex = np.exp(l64 - l64.max(axis=1, keepdims=True))
+        score = ex / ex.sum(axis=1, keepdims=True)
+    else:
+        score = 1.0 / (1.0 + np.exp(-l64))
+    if e_score_correction_bias is None:
+        key = logits.copy()
+    else:
+        b32 = np.asarray(e_score_correction_bias, dtype=_F32).reshape(E)
+        key = _scores_f32(logits, scoring_func) + b32[None, :]
+    key = np.where(np.isnan(key), -np.inf, key).astype(_F32)
+
+    ids = np.zeros((T, k), np.int32)
+    for t in range(T):
+        allowed = np.ones(E, bool)
+        if G > 1:
+            gsz = E // G
+            gscore = key[t].reshape(G, gsz).max(axis=1)
+            # step 3: groups by score, ties to the lower group
+            gorder = np.lexsort((np.arange(G), -gscore.astype(np.float64)))
+            keep = np.zeros(G, bool)
+            keep[gorder[:topk_group]] = True
+            allowed = np.repeat(keep, gsz)
+        cand = np.nonzero(allowed)[0]
+        # step 4: experts by key, ties to the lower index
+        order = cand[np.lexsort((cand, -key[t, cand].astype(np.float64)))]
+        ids[t] = order[:k]
+
+    w = np.take_along_axis(score, ids, axis=1)   # step 5
+    if renormalize:
+        w = w / w.sum(axis=1, keepdims=True)
+    return w * float(routed_scaling_factor), ids
+
+
 # --------------------------------------------------------------------------
 # Block alignment (implied by fused_experts' grouped GEMM; not on the pages)
 # --------------------------------------------------------------------------
