@@ -115,6 +115,46 @@ int moe_topk_route(const float* logits, int T, int E, int k, int renormalize,
                    float* topk_w, int32_t* topk_ids, void* stream);
 
 /*
+ * Router options: the further select_experts arguments that
+ * ExpertsInt8MoEMethod.apply and MoeWNA16Method.apply_monolithic pass on
+ * (scoring_func, num_expert_group / topk_group of use_grouped_topk,
+ * e_score_correction_bias, routed_scaling_factor).  The pages name them
+ * without their arithmetic; this library reads them as follows.
+ *   1. Score s_e of each expert: softmax over the token's logits
+ *      (MQ_SCORING_SOFTMAX) or sigmoid(logit_e) (MQ_SCORING_SIGMOID).
+ *   2. Selection key: the logit itself when e_score_correction_bias is NULL
+ *      (either score rises with it); else the float32 s_e + bias[e].
+ *   3. num_expert_group G > 1: experts [g*E/G, (g+1)*E/G) form group g,
+ *      scored by its largest key; the topk_group best groups (ties: lower
+ *      group) stay and every expert of the other groups is out.
+ *   4. The k largest keys left (ties: lower index) fill slots 0..k-1.
+ *   5. topk_w[t,j] = s_{id_j} (the bias steers the choice only), divided by
+ *      the sum over the k chosen when renormalize != 0, times
+ *      routed_scaling_factor.
+ * {MQ_SCORING_SOFTMAX, r, 0, 0, NULL, 1.0f} is moe_topk_route's router.
+ */
+#define MQ_SCORING_SOFTMAX 0
+#define MQ_SCORING_SIGMOID 1
+typedef struct mq_route_opts {
+  int scoring_func;                      /* MQ_SCORING_SOFTMAX or MQ_SCORING_SIGMOID */
+  int renormalize;                       /* nonzero: renormalise over the k chosen */
+  int num_expert_group;                  /* 0 or 1: no groups; else 2..32, divides E */
+  int topk_group;                        /* groups kept, 1..num_expert_group (G > 1) */
+  const float* e_score_correction_bias;  /* float32 [E] (device, 16-byte aligned) or NULL */
+  float routed_scaling_factor;           /* finite; 1.0f leaves the weights as they are */
+} mq_route_opts;
+
+/*
+ * moe_topk_route_ex -- moe_topk_route with router options (opts: host
+ * pointer, read during the call).  Limits as moe_topk_route, and with
+ * groups k <= topk_group * E / num_expert_group.  Errors:
+ * MQ_ERR_INVALID_ARG for a NULL opts, an unknown scoring_func, a group
+ * setting outside those limits or a non-finite scaling factor.
+ */
+int moe_topk_route_ex(const float* logits, int T, int E, int k, const mq_route_opts* opts,
+                      float* topk_w, int32_t* topk_ids, void* stream);
+
+/*
  * moe_align_capacity -- number of rows moe_align_block may produce:
  * round_up(T*k + min(E, T*k) * (block_m - 1), block_m).  Returns -1 for bad
  * arguments.
@@ -263,6 +303,24 @@ int moe_quant_forward_logits(const void* x, const float* router_logits,
                              const uint8_t* z13, const uint8_t* z2,
                              void* workspace, size_t ws_bytes,
                              void* out, unsigned flags, void* stream);
+
+/*
+ * moe_quant_forward_logits_ex -- moe_quant_forward_logits with router
+ * options (see mq_route_opts; opts replaces renormalize), as
+ * MoeWNA16Method.apply_monolithic passes them: the result is bitwise that of
+ * moe_topk_route_ex followed by moe_quant_forward_ex.  Workspace from
+ * moe_quant_forward_logits_workspace; other arguments, limits and errors as
+ * moe_quant_forward_logits and moe_topk_route_ex.
+ */
+int moe_quant_forward_logits_ex(const void* x, const float* router_logits,
+                                int T, int H, int I, int E, int k,
+                                const mq_route_opts* opts,
+                                int bits, int group_size, int has_zp,
+                                const void* w13, const void* w2,
+                                const void* s13, const void* s2,
+                                const uint8_t* z13, const uint8_t* z2,
+                                void* workspace, size_t ws_bytes,
+                                void* out, unsigned flags, void* stream);
 
 /*
  * moe_quant_forward_noalloc -- moe_quant_forward without a workspace

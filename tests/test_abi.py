@@ -96,3 +96,42 @@ def test_host_side_rejections(lib):
     assert lib.moe_align_block(fake, 4, 2, 8, 16, fake, fake, fake, fake, 8, None) == 1
     assert lib.moe_quant_forward_workspace(4, 128, 128, 8, 2, 8, -1) > 0
     assert lib.moe_quant_forward_workspace(4, 128, 128, 8, 2, 3, -1) == 0
+
+
+def test_route_options_rejections(lib):
+    """moe_topk_route_ex / moe_quant_forward_logits_ex check the router
+    options on the host before anything is launched."""
+    from weight_quantized_moe_gb300 import binding
+    vp = ctypes.c_void_p
+    fake = vp(0x1000)
+
+    def opts(**kw):
+        base = dict(scoring_func=binding.MQ_SCORING_SIGMOID, renormalize=1, num_expert_group=8,
+                    topk_group=4, e_score_correction_bias=None, routed_scaling_factor=2.5)
+        base.update(kw)
+        return ctypes.byref(binding.MqRouteOpts(**base))
+
+    def route(o, E=256, k=8):
+        return lib.moe_topk_route_ex(fake, 4, E, k, o, fake, fake, None)
+
+    assert lib.moe_topk_route_ex(fake, 4, 256, 8, None, fake, fake, None) == 1  # null opts
+    assert route(opts(scoring_func=2)) == 1
+    assert route(opts(num_expert_group=33, topk_group=1)) == 1
+    assert route(opts(num_expert_group=-1)) == 1
+    assert route(opts(num_expert_group=6)) == 1           # 6 does not divide 256
+    assert route(opts(topk_group=0)) == 1
+    assert route(opts(topk_group=9)) == 1
+    assert route(opts(topk_group=1), k=33) == 1          # k > 32
+    assert route(opts(topk_group=1, num_expert_group=32), k=9) == 1  # 9 > 1 group of 8
+    assert route(opts(routed_scaling_factor=float("inf"))) == 1
+    assert route(opts(routed_scaling_factor=float("nan"))) == 1
+    assert route(opts(e_score_correction_bias=0x1004)) == 1  # misaligned bias
+    assert route(opts(), E=2048) == 2
+    # T = 0 with valid options: nothing to do
+    assert lib.moe_topk_route_ex(fake, 0, 256, 8, opts(), fake, fake, None) == 0
+    assert lib.moe_quant_forward_logits_ex(fake, fake, 4, 128, 128, 256, 8, opts(topk_group=0), 8,
+                                           -1, 0, fake, fake, fake, fake, None, None, fake,
+                                           1 << 30, fake, 0, None) == 1
+    assert lib.moe_quant_forward_logits_ex(fake, fake, 4, 128, 128, 256, 8, None, 8, -1, 0,
+                                           fake, fake, fake, fake, None, None, fake, 1 << 30,
+                                           fake, 0, None) == 1

@@ -29,5 +29,8 @@ from .binding import (  # noqa: F401
     MQ_FWD_SCALE_PER_TENSOR,
     MQ_FWD_ACT_F16,
     MQ_FWD_ROUTER_WEIGHT_ON_INPUT,
+    MQ_SCORING_SOFTMAX,
+    MQ_SCORING_SIGMOID,
+    MqRouteOpts,
     forward_flags,
 )

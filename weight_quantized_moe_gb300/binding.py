@@ -27,6 +27,18 @@ MQ_FWD_SCALE_BF16 = 0x4
 MQ_FWD_SCALE_PER_TENSOR = 0x8
 MQ_FWD_ACT_F16 = 0x10
 MQ_FWD_ROUTER_WEIGHT_ON_INPUT = 0x20
+# mq_route_opts.scoring_func
+MQ_SCORING_SOFTMAX = 0
+MQ_SCORING_SIGMOID = 1
+
+
+class MqRouteOpts(ctypes.Structure):
+    """struct mq_route_opts (include/moeq.h)."""
+    _fields_ = [("scoring_func", ctypes.c_int), ("renormalize", ctypes.c_int),
+                ("num_expert_group", ctypes.c_int), ("topk_group", ctypes.c_int),
+                ("e_score_correction_bias", ctypes.c_void_p),
+                ("routed_scaling_factor", ctypes.c_float)]
+
 
 _vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
 _SIGNATURES = {
@@ -36,6 +48,8 @@ _SIGNATURES = {
     "moe_quantize_int8_per_channel": (_i32, [_vp, _i64, _i64, _vp, _vp, _vp]),
     "moe_quantize_uint4_group": (_i32, [_vp, _i64, _i64, _i32, _vp, _vp, _vp, _vp]),
     "moe_topk_route": (_i32, [_vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp]),
+    "moe_topk_route_ex": (_i32, [_vp, _i32, _i32, _i32, ctypes.POINTER(MqRouteOpts), _vp, _vp,
+                                 _vp]),
     "moe_align_capacity": (_i64, [_i32, _i32, _i32, _i32]),
     "moe_align_block": (_i32, [_vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _i64, _vp]),
     "moe_quant_forward_workspace": (_sz, [_i32] * 7),
@@ -48,6 +62,10 @@ _SIGNATURES = {
     "moe_quant_forward_logits": (_i32, [_vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
                                         _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp,
                                         ctypes.c_uint, _vp]),
+    "moe_quant_forward_logits_ex": (_i32, [_vp, _vp, _i32, _i32, _i32, _i32, _i32,
+                                           ctypes.POINTER(MqRouteOpts), _i32, _i32, _i32, _vp,
+                                           _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp, ctypes.c_uint,
+                                           _vp]),
     "moe_quant_forward_noalloc": (_i32, [_vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
                                          _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "mq_kernel_launch_count": (ctypes.c_longlong, []),
@@ -176,10 +194,34 @@ def moe_quantize_uint4_group(w, group_size, stream=None):
     return qw, sc, qz
 
 
-def moe_topk_route(logits, k, renormalize, topk_w=None, topk_ids=None, stream=None):
-    """fp32 [T, E] -> (topk_w fp32 [T, k], topk_ids int32 [T, k])."""
+def route_opts(E, renormalize, scoring_func="softmax", num_expert_group=0, topk_group=0,
+               e_score_correction_bias=None, routed_scaling_factor=1.0):
+    """The router options as an mq_route_opts, and whether they are the plain
+    softmax router (moe_topk_route's).  e_score_correction_bias: fp32 [E] on
+    the device, or None."""
+    if scoring_func not in ("softmax", "sigmoid"):
+        raise ValueError("scoring_func must be 'softmax' or 'sigmoid'")
+    if e_score_correction_bias is not None:
+        _need(e_score_correction_bias, torch.float32, "e_score_correction_bias", 1)
+        if e_score_correction_bias.numel() != E:
+            raise ValueError(f"e_score_correction_bias must hold E = {E} values")
+    o = MqRouteOpts(MQ_SCORING_SIGMOID if scoring_func == "sigmoid" else MQ_SCORING_SOFTMAX,
+                    int(bool(renormalize)), int(num_expert_group or 0), int(topk_group or 0),
+                    _ptr(e_score_correction_bias), float(routed_scaling_factor))
+    plain = (scoring_func == "softmax" and (num_expert_group or 0) <= 1
+             and e_score_correction_bias is None and float(routed_scaling_factor) == 1.0)
+    return o, plain
+
+
+def moe_topk_route(logits, k, renormalize, topk_w=None, topk_ids=None, stream=None,
+                   scoring_func="softmax", num_expert_group=0, topk_group=0,
+                   e_score_correction_bias=None, routed_scaling_factor=1.0):
+    """fp32 [T, E] -> (topk_w fp32 [T, k], topk_ids int32 [T, k]).  Router
+    options other than the defaults go through moe_topk_route_ex."""
     _need(logits, torch.float32, "logits", 2)
     T, E = logits.shape
+    opts, plain = route_opts(E, renormalize, scoring_func, num_expert_group, topk_group,
+                             e_score_correction_bias, routed_scaling_factor)
     if topk_w is None:
         topk_w = torch.empty(T, k, dtype=torch.float32, device=logits.device)
     if topk_ids is None:
@@ -188,8 +230,12 @@ def moe_topk_route(logits, k, renormalize, topk_w=None, topk_ids=None, stream=No
     _need(topk_ids, torch.int32, "topk_ids")
     if topk_w.numel() != T * k or topk_ids.numel() != T * k:
         raise ValueError("topk_w / topk_ids must hold T * k elements")
-    _check(lib().moe_topk_route(_ptr(logits), T, E, k, int(bool(renormalize)), _ptr(topk_w),
-                                _ptr(topk_ids), _stream(stream)))
+    if plain:
+        _check(lib().moe_topk_route(_ptr(logits), T, E, k, int(bool(renormalize)), _ptr(topk_w),
+                                    _ptr(topk_ids), _stream(stream)))
+    else:
+        _check(lib().moe_topk_route_ex(_ptr(logits), T, E, k, ctypes.byref(opts), _ptr(topk_w),
+                                       _ptr(topk_ids), _stream(stream)))
     return topk_w, topk_ids
 
 
@@ -305,10 +351,12 @@ def moe_quant_forward(x, w13, w2, s13, s2, topk_w, topk_ids, bits=8, group_size=
 def moe_quant_forward_logits(x, router_logits, w13, w2, s13, s2, top_k, renormalize=True, bits=8,
                              group_size=-1, has_zp=False, z13=None, z2=None, workspace=None,
                              out=None, stream=None, apply_router_weight_on_input=False,
-                             inplace=False):
-    """Routing and the expert MLP in one call (moe_quant_forward_logits in
-    include/moeq.h): the same result as moe_topk_route followed by
-    moe_quant_forward, bitwise."""
+                             inplace=False, scoring_func="softmax", num_expert_group=0,
+                             topk_group=0, e_score_correction_bias=None,
+                             routed_scaling_factor=1.0):
+    """Routing and the expert MLP in one call (moe_quant_forward_logits, or
+    moe_quant_forward_logits_ex with router options, in include/moeq.h): the
+    same result as moe_topk_route followed by moe_quant_forward, bitwise."""
     if x.dtype not in (torch.bfloat16, torch.float16):
         raise TypeError(f"x must be bfloat16 or float16, got {x.dtype}")
     _need(x, x.dtype, "x", 2)
@@ -319,6 +367,8 @@ def moe_quant_forward_logits(x, router_logits, w13, w2, s13, s2, top_k, renormal
     if router_logits.shape != (T, E):
         raise ValueError(f"router_logits must be [{T}, {E}]")
     flags = forward_flags(x, w13, s13, bits, apply_router_weight_on_input)
+    opts, plain = route_opts(E, renormalize, scoring_func, num_expert_group, topk_group,
+                             e_score_correction_bias, routed_scaling_factor)
     ws_need = int(lib().moe_quant_forward_logits_workspace(T, H, I, E, top_k, bits, group_size))
     if workspace is None:
         workspace = torch.empty(max(ws_need, 16), dtype=torch.uint8, device=x.device)
@@ -328,11 +378,15 @@ def moe_quant_forward_logits(x, router_logits, w13, w2, s13, s2, top_k, renormal
     if out is None:
         out = torch.empty(T, H, dtype=x.dtype, device=x.device)
     _need(out, x.dtype, "out", 2)
-    _check(lib().moe_quant_forward_logits(
-        _ptr(x), _ptr(router_logits), T, H, I, E, top_k, int(bool(renormalize)), bits, group_size,
-        int(bool(has_zp)), _ptr(w13), _ptr(w2), _ptr(s13), _ptr(s2),
-        _ptr(z13 if has_zp else None), _ptr(z2 if has_zp else None),
-        _ptr(workspace), workspace.numel(), _ptr(out), flags, _stream(stream)))
+    tail = (bits, group_size, int(bool(has_zp)), _ptr(w13), _ptr(w2), _ptr(s13), _ptr(s2),
+            _ptr(z13 if has_zp else None), _ptr(z2 if has_zp else None),
+            _ptr(workspace), workspace.numel(), _ptr(out), flags, _stream(stream))
+    if plain:
+        _check(lib().moe_quant_forward_logits(_ptr(x), _ptr(router_logits), T, H, I, E, top_k,
+                                              int(bool(renormalize)), *tail))
+    else:
+        _check(lib().moe_quant_forward_logits_ex(_ptr(x), _ptr(router_logits), T, H, I, E, top_k,
+                                                 ctypes.byref(opts), *tail))
     return out
 
 

@@ -3,6 +3,7 @@
 #include "common.cuh"
 
 #include <atomic>
+#include <cmath>
 #include <mutex>
 #include <stdarg.h>
 #include <stdio.h>
@@ -264,6 +265,50 @@ MQ_EXPORT int moe_topk_route(const float* logits, int T, int E, int k, int renor
   return err == cudaSuccess ? MQ_OK : cuda_fail(err, "route launch");
 }
 
+// mq_route_opts -> RouteOpts, with the checks moe_topk_route_ex documents.
+static int route_opts_from(const mq_route_opts* opts, int E, int k, RouteOpts* o) {
+  if (!opts) return fail(MQ_ERR_INVALID_ARG, "null route options");
+  if (opts->scoring_func != MQ_SCORING_SOFTMAX && opts->scoring_func != MQ_SCORING_SIGMOID)
+    return fail(MQ_ERR_INVALID_ARG, "unknown scoring_func %d", opts->scoring_func);
+  const int G = opts->num_expert_group;
+  if (G < 0 || G > 32) return fail(MQ_ERR_INVALID_ARG, "num_expert_group must be in [0, 32]");
+  if (G > 1) {
+    if (E % G) return fail(MQ_ERR_INVALID_ARG, "num_expert_group must divide E");
+    if (opts->topk_group < 1 || opts->topk_group > G)
+      return fail(MQ_ERR_INVALID_ARG, "topk_group must be in [1, num_expert_group]");
+    if ((int64_t)k > (int64_t)opts->topk_group * (E / G))
+      return fail(MQ_ERR_INVALID_ARG, "k exceeds the experts of topk_group groups");
+  }
+  if (!std::isfinite(opts->routed_scaling_factor))
+    return fail(MQ_ERR_INVALID_ARG, "routed_scaling_factor must be finite");
+  if (opts->e_score_correction_bias && !aligned16(opts->e_score_correction_bias))
+    return fail(MQ_ERR_INVALID_ARG, "e_score_correction_bias must be 16-byte aligned");
+  o->scoring = opts->scoring_func;
+  o->renorm = opts->renormalize ? 1 : 0;
+  o->groups = G > 1 ? G : 0;
+  o->topk_group = G > 1 ? opts->topk_group : 0;
+  o->bias = opts->e_score_correction_bias;
+  o->scale = opts->routed_scaling_factor;
+  return MQ_OK;
+}
+
+MQ_EXPORT int moe_topk_route_ex(const float* logits, int T, int E, int k,
+                                const mq_route_opts* opts, float* topk_w, int32_t* topk_ids,
+                                void* stream) {
+  if (T < 0) return fail(MQ_ERR_INVALID_ARG, "T must be >= 0");
+  if (E < 1 || E > 1024) return fail(MQ_ERR_UNSUPPORTED, "E must be in [1, 1024]");
+  if (k < 1 || k > E || k > 32) return fail(MQ_ERR_INVALID_ARG, "need 1 <= k <= min(E, 32)");
+  RouteOpts o;
+  const int rc = route_opts_from(opts, E, k, &o);
+  if (rc != MQ_OK) return rc;
+  if (T == 0) return MQ_OK;
+  if (!logits || !topk_w || !topk_ids) return fail(MQ_ERR_INVALID_ARG, "null pointer");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  LaunchScope ls(MQ_PROF_ROUTE, st);
+  cudaError_t err = launch_route_ex(logits, T, E, k, o, topk_w, topk_ids, st);
+  return err == cudaSuccess ? MQ_OK : cuda_fail(err, "route launch");
+}
+
 MQ_EXPORT int64_t moe_align_capacity(int T, int k, int E, int block_m) {
   if (T < 0 || k < 1 || E < 1 || block_m < 1) return -1;
   const int64_t S = (int64_t)T * k;
@@ -320,8 +365,8 @@ static int forward_impl(const void* x, int T, int H, int I, int E, int k, int bi
                         int group_size, int has_zp, const void* w13, const void* w2,
                         const void* s13, const void* s2, const uint8_t* z13, const uint8_t* z2,
                         const float* topk_w, const int32_t* topk_ids, const float* logits,
-                        int renorm, void* workspace, size_t ws_bytes, void* out, unsigned flags,
-                        void* stream) {
+                        const RouteOpts& ro, void* workspace, size_t ws_bytes, void* out,
+                        unsigned flags, void* stream) {
   constexpr unsigned kW8Flags = MQ_FWD_W8_UINT8 | MQ_FWD_SCALE_F16 | MQ_FWD_SCALE_BF16 |
                                 MQ_FWD_SCALE_PER_TENSOR;
   constexpr unsigned kAllFlags = kW8Flags | MQ_FWD_ACT_F16 | MQ_FWD_ROUTER_WEIGHT_ON_INPUT;
@@ -392,15 +437,19 @@ static int forward_impl(const void* x, int T, int H, int I, int E, int k, int bi
   a.cap = L.cap;
 
   cudaError_t err;
-  if (logits && !route_fused(T, k, E)) {  // larger batches: the router kernel first
+  // the plain softmax router of small batches runs inside the align kernel
+  const bool plain = route_opts_plain(ro);
+  const bool fused = logits && plain && route_fused(T, k, E);
+  if (logits && !fused) {  // otherwise the router kernel first
     LaunchScope ls(MQ_PROF_ROUTE, st);
-    err = launch_route(logits, T, E, k, renorm, rw, rid, st);
+    err = plain ? launch_route(logits, T, E, k, ro.renorm, rw, rid, st)
+                : launch_route_ex(logits, T, E, k, ro, rw, rid, st);
     if (err != cudaSuccess) return cuda_fail(err, "forward: route launch");
   }
   {
     LaunchScope ls(MQ_PROF_ALIGN, st);
-    if (logits && route_fused(T, k, E))  // routing fused into the align kernel
-      err = launch_route_align(logits, renorm, rw, rid, T, k, E, bm, a.sorted, a.block_expert,
+    if (fused)
+      err = launch_route_align(logits, ro.renorm, rw, rid, T, k, E, bm, a.sorted, a.block_expert,
                                a.offsets, a.num_padded, a.status, st, L.plan.bn, a.chunk_expert,
                                a.chunk_start);
     else
@@ -445,8 +494,9 @@ MQ_EXPORT int moe_quant_forward_ex(const void* x, int T, int H, int I, int E, in
                                    const uint8_t* z2, const float* topk_w,
                                    const int32_t* topk_ids, void* workspace, size_t ws_bytes,
                                    void* out, unsigned flags, void* stream) {
+  const RouteOpts none = {MQ_SCORING_SOFTMAX, 0, 0, 0, nullptr, 1.0f};
   return forward_impl(x, T, H, I, E, k, bits, group_size, has_zp, w13, w2, s13, s2, z13, z2,
-                      topk_w, topk_ids, nullptr, 0, workspace, ws_bytes, out, flags, stream);
+                      topk_w, topk_ids, nullptr, none, workspace, ws_bytes, out, flags, stream);
 }
 
 MQ_EXPORT size_t moe_quant_forward_logits_workspace(int T, int H, int I, int E, int k, int bits,
@@ -463,7 +513,23 @@ MQ_EXPORT int moe_quant_forward_logits(const void* x, const float* router_logits
                                        const uint8_t* z13, const uint8_t* z2, void* workspace,
                                        size_t ws_bytes, void* out, unsigned flags, void* stream) {
   if (T > 0 && !router_logits) return fail(MQ_ERR_INVALID_ARG, "null router_logits");
+  const RouteOpts ro = {MQ_SCORING_SOFTMAX, renormalize ? 1 : 0, 0, 0, nullptr, 1.0f};
   return forward_impl(x, T, H, I, E, k, bits, group_size, has_zp, w13, w2, s13, s2, z13, z2,
-                      nullptr, nullptr, router_logits, renormalize, workspace, ws_bytes, out,
-                      flags, stream);
+                      nullptr, nullptr, router_logits, ro, workspace, ws_bytes, out, flags, stream);
+}
+
+MQ_EXPORT int moe_quant_forward_logits_ex(const void* x, const float* router_logits, int T,
+                                          int H, int I, int E, int k, const mq_route_opts* opts,
+                                          int bits, int group_size, int has_zp, const void* w13,
+                                          const void* w2, const void* s13, const void* s2,
+                                          const uint8_t* z13, const uint8_t* z2, void* workspace,
+                                          size_t ws_bytes, void* out, unsigned flags,
+                                          void* stream) {
+  if (k < 1 || k > E || k > 32) return fail(MQ_ERR_INVALID_ARG, "need 1 <= k <= min(E, 32)");
+  RouteOpts ro;
+  const int rc = route_opts_from(opts, E, k, &ro);
+  if (rc != MQ_OK) return rc;
+  if (T > 0 && !router_logits) return fail(MQ_ERR_INVALID_ARG, "null router_logits");
+  return forward_impl(x, T, H, I, E, k, bits, group_size, has_zp, w13, w2, s13, s2, z13, z2,
+                      nullptr, nullptr, router_logits, ro, workspace, ws_bytes, out, flags, stream);
 }

@@ -78,6 +78,21 @@ MQ_HIDDEN cudaError_t launch_quant_uint4(const void* w, int64_t rows, int64_t co
                                          uint8_t* qw, uint16_t* sc, uint8_t* qz, cudaStream_t st);
 MQ_HIDDEN cudaError_t launch_route(const float* logits, int T, int E, int k, int renorm,
                                    float* topk_w, int32_t* topk_ids, cudaStream_t st);
+// Router options beyond softmax + renormalisation (moe_topk_route_ex).
+struct RouteOpts {
+  int scoring;        // MQ_SCORING_SOFTMAX / MQ_SCORING_SIGMOID
+  int renorm;
+  int groups;         // expert groups; <= 1: none
+  int topk_group;     // groups kept when groups > 1
+  const float* bias;  // score-correction bias [E] (device) or null
+  float scale;        // routed scaling factor
+};
+inline bool route_opts_plain(const RouteOpts& o) {
+  return o.scoring == MQ_SCORING_SOFTMAX && o.groups <= 1 && !o.bias && o.scale == 1.0f;
+}
+MQ_HIDDEN cudaError_t launch_route_ex(const float* logits, int T, int E, int k,
+                                      const RouteOpts& o, float* topk_w, int32_t* topk_ids,
+                                      cudaStream_t st);
 // Router logits -> topk_w / topk_ids -> align as one kernel (the align
 // kernel's 32 warps route first) when the routing work is small enough for
 // one CTA: tokens x k argmax rounds over ceil(E / 32) registers per lane at
