@@ -57,10 +57,8 @@ constexpr int kUnitList = 512;            // work units per CTA decoded once int
 // * The int8 weight ring (16 KB entries) is as deep as shared memory allows:
 //   HBM needs about 200 KB in flight per SM.
 // * Synchronisation with the MMA issuer happens per MMA step of kG weight
-//   stages (16 MMAs).  A tcgen05.mma with M = 128, K = 16 issues in about 45
-//   cycles for any N <= 64, and each wait or commit costs about as much as
-//   an MMA, so batching keeps the issuing thread below the time HBM needs to
-//   deliver the weights.
+//   stages (16 MMAs): the wait and commit around a step cost several MMAs'
+//   worth of issue time, so a step batches 16 of them.
 // * Tensor memory holds two accumulator buffers and kSteps converted-A
 //   stages of kG * 64 columns; the activation ring has the same depth, and
 //   one MMA commit per step frees both.
@@ -70,10 +68,14 @@ constexpr int kUnitList = 512;            // work units per CTA decoded once int
 //   every other step, so that one thread's wait and commit overlap the
 //   other's MMAs; each issuer accumulates its steps into its own half of the
 //   accumulator (kNI = 2 halves, added in a fixed order by the epilogue),
-//   and step st uses tensor-memory stage st % 2 (kSteps = 2).
-template <int BN>
+//   and step st uses tensor-memory stage st % 2 (kSteps = 2).  Not for the
+//   8-bit down GEMM: its bf16 conversion needs the third stage of overlap
+//   more than the issuers need each other (measured on Mixtral shapes: the
+//   launch takes 104 us with one issuer and three stages, 118 us with two
+//   issuers and two).
+template <int BN, int NI>
 struct TileCfg {
-  static constexpr int kNI = BN == 16 ? 2 : 1;  // MMA issuer threads
+  static constexpr int kNI = NI;                // MMA issuer threads
   static constexpr int kACol0 = 2 * kNI * BN;   // two accumulator buffers of kNI halves
   static constexpr int kStepFit = ((int)kTmemCols - kACol0) / kAColsPerStep;
   static constexpr int kSteps = kNI == 2 ? 2 : (kStepFit > kMaxSteps ? kMaxSteps : kStepFit);
@@ -87,6 +89,9 @@ struct TileCfg {
   static_assert(kNI == 1 || (kSteps == 2 && kStepFit >= 2), "two issuers: one stage each");
   static_assert(kAStagesSmem >= 3, "weight ring depth");
 };
+
+template <int MODE, int BITS, int BN>
+using CfgOf = TileCfg<BN, (BN == 16 && !(MODE == 2 && BITS == 8)) ? 2 : 1>;
 
 struct TcParams {
   int H, I, E, k, S;
@@ -379,10 +384,10 @@ __device__ __forceinline__ void group_words(const TcParams& p, int wrow, int k, 
 // consumer per slot); a converter waits for its step's activations only
 // after it has seen the MMAs of the slot's previous use complete.
 template <int MODE, int BITS, int BN>
-__global__ void __launch_bounds__(TileCfg<BN>::kThreads, 1)
+__global__ void __launch_bounds__(CfgOf<MODE, BITS, BN>::kThreads, 1)
     moe_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const TcParams p) {
-  using C = TileCfg<BN>;
+  using C = CfgOf<MODE, BITS, BN>;
   // one weight stage = 128 rows x 128 bytes: 128 K of int8 or 256 K of uint4
   constexpr int kEntryK = BITS == 8 ? 128 : 256;
   constexpr int kGA = 256 / kEntryK;  // weight stages per MMA step (256 K)
@@ -1010,9 +1015,9 @@ cudaError_t make_map(CUtensorMap* map, CUtensorMapDataType dt, int rank, const v
 
 // At least 120 KB so that only one CTA fits on an SM: each CTA allocates all
 // 512 tensor-memory columns.
-template <int BN>
+template <int MODE, int BITS, int BN>
 constexpr size_t smem_for() {
-  using C = TileCfg<BN>;
+  using C = CfgOf<MODE, BITS, BN>;
   const size_t need = 1024 + (size_t)C::kAStagesSmem * kABytes + (size_t)C::kSteps * C::kBBytes +
                       sizeof(SharedCtl) + kUnitList * sizeof(int4);
   return need < 120 * 1024 ? 120 * 1024 : need;
@@ -1021,14 +1026,14 @@ constexpr size_t smem_for() {
 template <int MODE, int BITS, int BN>
 cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const TcParams& p,
                         int max_units, cudaStream_t st) {
-  constexpr size_t smem = smem_for<BN>();
+  constexpr size_t smem = smem_for<MODE, BITS, BN>();
   auto kern = moe_gemm_tc<MODE, BITS, BN>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   const int sms = tc_num_sms();
   const int grid = max_units < sms ? max_units : sms;
   if (grid <= 0) return cudaSuccess;
-  err = launch_pdl(kern, dim3(grid), dim3(TileCfg<BN>::kThreads), smem, st, ta, tb, p);
+  err = launch_pdl(kern, dim3(grid), dim3(CfgOf<MODE, BITS, BN>::kThreads), smem, st, ta, tb, p);
   return err != cudaSuccess ? err : cudaGetLastError();
 }
 
