@@ -205,3 +205,20 @@ def test_forward_maximum_experts_and_top_k(E, k, T):
     wl = synth.Workload("edge", E=E, k=k, H=128, I=128, Ts=(T,))
     layer = Layer(wl, seed=4)
     assert _run(layer, T, seed=E + k) <= FWD_TOL
+
+
+def test_bench_end_to_end_loop_delivers_each_output():
+    """The benchmark's pipelined serving loop (uploads and downloads on their
+    own streams, two buffers of each) leaves every step's output on the host
+    equal to the forward's result."""
+    import bench
+    prob = bench.Problem(W["tiny"], 16, seed=3)
+    ref = prob.step().clone()
+    run = bench.EndToEnd(prob)
+    for _ in range(5):
+        run.step()
+    run.finish()
+    torch.cuda.synchronize()
+    assert mq.mq_device_status() == 0
+    for h in run.out_h:
+        assert torch.equal(h, ref.cpu())
