@@ -27,6 +27,7 @@ namespace {
 
 constexpr int kWarps = 32;
 constexpr int kThreads = kWarps * 32;
+constexpr int kBatch = 8;  // 32-slot steps whose ids a warp loads before using them
 
 template <int PER>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -59,12 +60,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int begin = warp * per_warp;
   const int end = min(S, begin + per_warp);
   bool bad = false;
-  for (int base = begin; base < end; base += 32) {
-    const int s = base + lane;
-    if (s < end) {
-      const int e = ids[s];
-      if (e >= 0 && e < E) atomicAdd(&hist[warp * E + e], 1);
-      else bad = true;
+  for (int base = begin; base < end; base += 32 * kBatch) {
+    int ev[kBatch];  // all loads of the batch in flight before the first use
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int s = base + b * 32 + lane;
+      ev[b] = s < end ? ids[s] : 0;
+    }
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      if (base + b * 32 >= end) break;  // warp-uniform
+      if (base + b * 32 + lane < end) {
+        if (ev[b] >= 0 && ev[b] < E) atomicAdd(&hist[warp * E + ev[b]], 1);
+        else bad = true;
+      }
     }
   }
   if (__any_sync(0xffffffffu, bad) && lane == 0) mq::flag(status, MQ_DEV_BAD_EXPERT_ID);
@@ -141,20 +150,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
 
-  // ---- stable placement ---------------------------------------------------
-  for (int base = begin; base < end; base += 32) {
-    const int s = base + lane;
-    int ex = -1;
-    if (s < end) {
-      ex = ids[s];
-      if (ex < 0 || ex >= E) ex = -1;
+  // ---- stable placement (32-slot steps in slot order) ----------------------
+  for (int base = begin; base < end; base += 32 * kBatch) {
+    int ev[kBatch];
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int s = base + b * 32 + lane;
+      ev[b] = s < end ? ids[s] : -1;
     }
-    const unsigned peers = __match_any_sync(0xffffffffu, ex);
-    const int rank = __popc(peers & ((1u << lane) - 1u));
-    if (ex >= 0) sorted[hist[warp * E + ex] + rank] = s;
-    __syncwarp();
-    if (ex >= 0 && rank == 0) hist[warp * E + ex] += __popc(peers);
-    __syncwarp();
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      if (base + b * 32 >= end) break;  // warp-uniform
+      const int s = base + b * 32 + lane;
+      const int ex = (s < end && ev[b] >= 0 && ev[b] < E) ? ev[b] : -1;
+      const unsigned peers = __match_any_sync(0xffffffffu, ex);
+      const int rank = __popc(peers & ((1u << lane) - 1u));
+      if (ex >= 0) sorted[hist[warp * E + ex] + rank] = s;
+      __syncwarp();
+      if (ex >= 0 && rank == 0) hist[warp * E + ex] += __popc(peers);
+      __syncwarp();
+    }
   }
 }
 

@@ -943,11 +943,17 @@ __global__ void __launch_bounds__(256) act_rows_to_f16(uint16_t* act, const int3
   if (threadIdx.x == 0) xinv[p] = ldexpf(1.0f, -e);
 }
 
-// out[t, :] = sum over valid slots j and K splits of ypart[split, t*k + j, :].
+// out[t, :] = sum over valid slots j and K splits of ypart[split, t*k + j, :],
+// in the order (j, split).  Without K splits (prefill plans) the partial
+// sums are read once from HBM: eight slots' loads are all issued before
+// their sums, so that enough bytes are in flight, with streaming cache hints.
+// With K splits (decode plans, a few MB that the down GEMM just wrote to L2)
+// a plain loop over the slots is faster.
 __global__ void __launch_bounds__(256) combine_splits(const float* __restrict__ ypart,
                                                       const int32_t* __restrict__ ids, int T,
                                                       int k, int E, int H, int splits,
                                                       int out_f16, void* __restrict__ out) {
+  constexpr int kBatch = 8;
   const int64_t i4 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int H4 = H / 4;
   mq::pdl_wait();  // ypart comes from the previous kernel
@@ -957,16 +963,42 @@ __global__ void __launch_bounds__(256) combine_splits(const float* __restrict__ 
   const int c = (int)(i4 % H4) * 4;
   const int64_t S = (int64_t)T * k;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int j = 0; j < k; ++j) {
-    const int64_t s = (int64_t)t * k + j;
-    const int e = ids[s];
-    if (e < 0 || e >= E) continue;
-    for (int sp = 0; sp < splits; ++sp) {
-      const float4 v = *reinterpret_cast<const float4*>(ypart + (sp * S + s) * H + c);
-      acc.x += v.x;
-      acc.y += v.y;
-      acc.z += v.z;
-      acc.w += v.w;
+  if (splits == 1) {
+    for (int j0 = 0; j0 < k; j0 += kBatch) {
+      float4 v[kBatch];
+      bool ok[kBatch];
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const int64_t s = (int64_t)t * k + j0 + b;
+        ok[b] = false;
+        if (j0 + b < k) {
+          const int e = ids[s];
+          ok[b] = e >= 0 && e < E;
+          if (ok[b]) v[b] = __ldcs(reinterpret_cast<const float4*>(ypart + s * H + c));
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        if (ok[b]) {
+          acc.x += v[b].x;
+          acc.y += v[b].y;
+          acc.z += v[b].z;
+          acc.w += v[b].w;
+        }
+      }
+    }
+  } else {
+    for (int j = 0; j < k; ++j) {
+      const int64_t s = (int64_t)t * k + j;
+      const int e = ids[s];
+      if (e < 0 || e >= E) continue;
+      for (int sp = 0; sp < splits; ++sp) {
+        const float4 v = *reinterpret_cast<const float4*>(ypart + (sp * S + s) * H + c);
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+      }
     }
   }
   uint2 o;
