@@ -727,6 +727,31 @@ __global__ void __launch_bounds__(CfgOf<MODE, BITS, BN>::kThreads, 1)
       const bool both = C::kNI == 2 && nsteps >= 2;
       const int half0 = (C::kNI == 2 && !both) ? (est & 1) : 0;
       est += nsteps;
+      // Per-column values of the tile, loaded while its MMAs still run (a
+      // unit of a few MMA steps would otherwise wait on these dependent
+      // loads): column i * 32 + lane in element i.  MODE 1: the activation
+      // row scale; MODE 2: the token-slot (S for padding) and its factor
+      // (activation row scale x router weight).
+      constexpr int NP = (BN + 31) / 32;
+      float colf[NP];
+      int colslot[NP];
+#pragma unroll
+      for (int i = 0; i < NP; ++i) {
+        const int cc = i * 32 + lane;
+        colf[i] = MODE == 1 ? 1.0f : 0.0f;
+        colslot[i] = p.S;
+        if (cc < w.n) {
+          if (MODE == 1) colf[i] = p.xinv[w.row0 + cc];
+          else colslot[i] = p.sorted[w.row0 + cc];
+        }
+      }
+      if (MODE == 2) {
+#pragma unroll
+        for (int i = 0; i < NP; ++i)
+          if (colslot[i] < p.S)
+            colf[i] = (kBf16 ? 1.0f : p.xinv[w.row0 + i * 32 + lane]) *
+                      (p.rw_on_input ? 1.0f : p.topk_w[colslot[i]]);
+      }
       if (!warp_wait_sleepy(&ctl->accfull[buf], (t >> 1) & 1, ctl, p.status, lane)) break;
       tc_fence_after();
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (buf * C::kNI + half0) * BN;
@@ -751,11 +776,11 @@ __global__ void __launch_bounds__(CfgOf<MODE, BITS, BN>::kThreads, 1)
         const float sc = BITS == 8 ? load_scale(p, p.scale_per_tensor ? w.e : wrow) : 1.0f;
         // uint4 runs the down GEMM in the K order [0,4,1,5,2,6,3,7] per octet
         const int col = w.mt * 64 + q * 16 + (BITS == 8 ? (lane >> 1) : permute_octet(lane >> 1));
-        auto body = [&](auto wtag, int c0) {
+        // xv: element c0 / 32 of colf (column c0 + cj on lane (c0 & 31) + cj)
+        auto body = [&](auto wtag, int c0, float xv) {
           constexpr int W = decltype(wtag)::value;
           constexpr int HW = W / 2;
           uint32_t v[W];
-          const float xv = lane < W ? p.xinv[w.row0 + c0 + lane] : 1.0f;
           load_acc(wtag, c0, v);
 #pragma unroll
           for (int jj = 0; jj < HW; ++jj) {
@@ -763,7 +788,7 @@ __global__ void __launch_bounds__(CfgOf<MODE, BITS, BN>::kThreads, 1)
             const float hi = __uint_as_float(v[jj + HW]) * sc;  // own row, column jj + HW
             const float got = __shfl_xor_sync(0xffffffffu, odd ? lo : hi, 1);
             const int cj = odd ? jj + HW : jj;
-            const float xs = __shfl_sync(0xffffffffu, xv, cj);
+            const float xs = __shfl_sync(0xffffffffu, xv, (c0 & 31) + cj);
             const float g = (odd ? got : lo) * xs;
             const float up = (odd ? hi : got) * xs;
             const float a = __fdividef(g * up, 1.0f + __expf(-g));  // silu(g) * up
@@ -771,35 +796,60 @@ __global__ void __launch_bounds__(CfgOf<MODE, BITS, BN>::kThreads, 1)
           }
         };
         int c0 = 0;
-        for (; c0 + CH <= w.n; c0 += CH) body(IC<CH>{}, c0);
-        if (CH > 16 && c0 < w.n) body(IC<16>{}, c0);  // n is a multiple of 16
+        for (; c0 + CH <= w.n; c0 += CH) {
+          float xv = colf[0];
+#pragma unroll
+          for (int i = 1; i < NP; ++i)
+            if ((c0 >> 5) == i) xv = colf[i];
+          body(IC<CH>{}, c0, xv);
+        }
+        if (CH > 16 && c0 < w.n) {  // n is a multiple of 16
+          float xv = colf[0];
+#pragma unroll
+          for (int i = 1; i < NP; ++i)
+            if ((c0 >> 5) == i) xv = colf[i];
+          body(IC<16>{}, c0, xv);
+        }
       } else {
         const int h = w.mt * kTileM + r;
         const float sc =
             BITS == 8 ? load_scale(p, p.scale_per_tensor ? w.e : (int64_t)w.e * p.H + h) : 1.0f;
         float* yp = p.ypart + (int64_t)w.split * p.S * p.H;
-        auto body = [&](auto wtag, int c0) {
+        // slot, f: element c0 / 32 of colslot, colf (column c0 + jj on lane (c0 & 31) + jj)
+        auto body = [&](auto wtag, int c0, int slot, float f) {
           constexpr int W = decltype(wtag)::value;
           uint32_t v[W];
-          // per column: its slot and the factor (act row scale x router weight)
-          int slot = p.S;
-          float f = 0.0f;
-          if (lane < W) {
-            const int prow = w.row0 + c0 + lane;
-            slot = p.sorted[prow];
-            if (slot < p.S) f = (kBf16 ? 1.0f : p.xinv[prow]) * (p.rw_on_input ? 1.0f : p.topk_w[slot]);
-          }
           load_acc(wtag, c0, v);
 #pragma unroll
           for (int jj = 0; jj < W; ++jj) {
-            const int sj = __shfl_sync(0xffffffffu, slot, jj);
-            const float fj = __shfl_sync(0xffffffffu, f, jj);
+            const int sj = __shfl_sync(0xffffffffu, slot, (c0 & 31) + jj);
+            const float fj = __shfl_sync(0xffffffffu, f, (c0 & 31) + jj);
             if (sj < p.S) yp[(int64_t)sj * p.H + h] = __uint_as_float(v[jj]) * sc * fj;
           }
         };
         int c0 = 0;
-        for (; c0 + CH <= w.n; c0 += CH) body(IC<CH>{}, c0);
-        if (CH > 16 && c0 < w.n) body(IC<16>{}, c0);  // n is a multiple of 16
+        for (; c0 + CH <= w.n; c0 += CH) {
+          int sl = colslot[0];
+          float fc = colf[0];
+#pragma unroll
+          for (int i = 1; i < NP; ++i)
+            if ((c0 >> 5) == i) {
+              sl = colslot[i];
+              fc = colf[i];
+            }
+          body(IC<CH>{}, c0, sl, fc);
+        }
+        if (CH > 16 && c0 < w.n) {  // n is a multiple of 16
+          int sl = colslot[0];
+          float fc = colf[0];
+#pragma unroll
+          for (int i = 1; i < NP; ++i)
+            if ((c0 >> 5) == i) {
+              sl = colslot[i];
+              fc = colf[i];
+            }
+          body(IC<16>{}, c0, sl, fc);
+        }
       }
       tc_fence_before();
       __syncwarp();
