@@ -9,10 +9,10 @@
 //   shared memory, one 16 KB box (128 rows x 128 bytes) per K step; for the
 //   gate/up GEMM a 4-D tensor map fetches the 64 gate rows and the matching
 //   64 up rows in that one box.  Converter warpgroups turn the codes into
-//   f16 (gate/up) or bf16 (down) -- exact, every int8 value is both -- and
+//   f16 (bf16 in the 8-bit down GEMM; exact, every int8 value is both) and
 //   write them straight into tensor memory with tcgen05.st, so shared
-//   memory never holds 16-bit weights.  The per-channel scale is applied once per output in the
-//   epilogue (sum_k x*(q*s) = s * sum_k x*q).
+//   memory never holds 16-bit weights.  The per-channel scale is applied
+//   once per output in the epilogue (sum_k x*(q*s) = s * sum_k x*q).
 // * The activations (token rows gathered per expert block) are the B
 //   operand: TMA tiles with the 128-byte swizzle in a second, short ring,
 //   read by tcgen05.mma from shared memory.
@@ -367,11 +367,12 @@ __device__ __forceinline__ void group_words(const TcParams& p, int wrow, int k, 
   ss = sb * 0x00010001u;
 }
 
-// Both GEMMs run f16 operands; their activation rows carry an exact
-// power-of-two scale (xinv undoes it in the epilogue).
+// f16 operands carry an exact power-of-two scale per activation row (xinv
+// undoes it in the epilogue); the 8-bit down GEMM runs bf16 operands on act
+// as written.
 // MODE 1: gate/up GEMM, SiLU-and-mul epilogue -> act (bf16).
-// MODE 2: down GEMM on act (converted in place to scaled f16 in between),
-//         router-weighted epilogue -> ypart.
+// MODE 2: down GEMM on act (uint4: converted in place to scaled f16 in
+//         between), router-weighted epilogue -> ypart.
 //
 // `st` numbers MMA steps (256 K, i.e. kGA weight stages of 16 KB, of one
 // work unit) in schedule order; step st belongs to converter group
