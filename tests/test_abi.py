@@ -135,3 +135,23 @@ def test_route_options_rejections(lib):
     assert lib.moe_quant_forward_logits_ex(fake, fake, 4, 128, 128, 256, 8, None, 8, -1, 0,
                                            fake, fake, fake, fake, None, None, fake, 1 << 30,
                                            fake, 0, None) == 1
+
+
+def test_route_opts_marshalling():
+    """The binding's mq_route_opts matches the C layout, and only the
+    defaults count as the plain router."""
+    from weight_quantized_moe_gb300 import binding
+    assert ctypes.sizeof(binding.MqRouteOpts) == 32
+    assert binding.MqRouteOpts.e_score_correction_bias.offset == 16
+    assert binding.MqRouteOpts.routed_scaling_factor.offset == 24
+    o, plain = binding.route_opts(64, True)
+    assert plain and o.scoring_func == binding.MQ_SCORING_SOFTMAX and o.renormalize == 1
+    assert o.routed_scaling_factor == 1.0 and not o.e_score_correction_bias
+    for kw in (dict(scoring_func="sigmoid"), dict(num_expert_group=8, topk_group=2),
+               dict(routed_scaling_factor=2.5)):
+        o, plain = binding.route_opts(64, False, **kw)
+        assert not plain
+    o, plain = binding.route_opts(64, False, num_expert_group=1, topk_group=0)
+    assert plain
+    with pytest.raises(ValueError):
+        binding.route_opts(64, True, scoring_func="tanh")
