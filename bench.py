@@ -60,12 +60,16 @@ def dist_setup(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    cuda = torch.cuda.is_available()
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    else:
+        if cuda:
+            torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if cuda else "gloo")
+    elif cuda:
         torch.cuda.set_device(0)
+    elif args.impl != "reference":
+        raise RuntimeError("bench.py needs a CUDA device (only --impl reference runs on the CPU)")
     return world, rank, local
 
 
@@ -328,11 +332,13 @@ def ncu_traffic(kernel, workload_key):
 
 
 # ---------------------------------------------------------------- oracle --
-def oracle_sample(wl, T, seed, n_tokens, device="cuda"):
+def oracle_sample(wl, T, seed, n_tokens, device=None):
     """Inputs for timing the CPU oracle on a bounded token sample of the
     workload: the oracle quantises the touched experts itself (load time,
     untimed); the timed part is route + align + forward on the sample."""
     import oracle
+    if device is None:  # the generators run on the GPU when there is one
+        device = "cuda" if torch.cuda.is_available() else "cpu"
     x = synth.hidden_states(T, wl.H, seed, device=device).float().cpu().numpy()
     lg = synth.router_logits(T, wl.E, seed, bias=wl.bias, device=device).cpu().numpy()
     _, ids = oracle.topk_route(lg, wl.k, wl.renormalize)
