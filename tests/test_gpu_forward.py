@@ -168,6 +168,18 @@ def test_forward_mixtral_decode_sampled():
     assert _run(layer, 64, seed=0, tokens=[5, 40], out_cols=cols) <= FWD_TOL
 
 
+@pytest.mark.parametrize("name,T,tokens", [("mixtral_prefill", 4096, [0, 2047, 4095]),
+                                           ("fine", 4096, [1, 3000]),
+                                           ("w4a16", 2048, [5, 2047])])
+def test_forward_prefill_sizes_sampled(name, T, tokens):
+    """The prefill-sized layers in the benchmark's launch configuration
+    (128-token tiles, no K split, the eight-slot combine): sampled tokens and
+    512 sampled output columns against the oracle."""
+    layer = Layer(W[name], seed=0)
+    cols = np.sort(np.random.default_rng(T).choice(layer.H, 512, replace=False))
+    assert _run(layer, T, seed=5, tokens=tokens, out_cols=cols) <= FWD_TOL
+
+
 def test_forward_captures_into_a_cuda_graph():
     """The whole forward (routing included) launches only kernels, with no
     host synchronisation or allocation, so it can be captured into a CUDA
