@@ -216,8 +216,10 @@ size_t moe_quant_forward_workspace(int T, int H, int I, int E, int k,
  *     y  = dequant(w2[e]) . a                 (H values)
  *     out[t] += topk_w[t,j] * y
  * x bf16 [T, H] (device), topk_w float32 [T, k], topk_ids int32 [T, k]
- * (device, e.g. from moe_topk_route), out bf16 [T, H] (device; must not
- * overlap x).  The block alignment runs inside, in the workspace.
+ * (device, e.g. from moe_topk_route), out bf16 [T, H] (device; either x
+ * itself -- fused_experts' inplace, x is read before any output is written --
+ * or not overlapping x at all).  The block alignment runs inside, in the
+ * workspace.
  * Accumulation is float32; the intermediate a is rounded to bf16.
  * Limits: H % 128 == 0, I % 128 == 0, E <= 1024, 1 <= k <= min(E, 32).
  * Errors: MQ_ERR_INVALID_ARG (null/misaligned pointers, bad shapes),
