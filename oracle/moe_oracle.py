@@ -33,6 +33,11 @@ Sources (vLLM API documentation pages):
 * P-int8 ``ExpertsInt8MoEMethod.apply`` passes ``apply_router_weight_on_input``
   through to ``fused_experts``; the supported activation dtypes are bf16 and
   fp16.
+* P-int8 ``ExpertsInt8MoEMethod.apply`` and P-wna16
+  ``MoeWNA16Method.apply_monolithic`` name the further router arguments
+  (``scoring_func``, ``num_expert_group`` / ``topk_group``,
+  ``e_score_correction_bias``, ``routed_scaling_factor``) without their
+  arithmetic; ``topk_route_ex`` states the reading taken.
 
 Readings taken where the pages are silent are marked "Reading:" in place.
 """
