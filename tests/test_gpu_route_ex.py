@@ -3,6 +3,8 @@ moe_quant_forward_logits_ex): sigmoid scoring, expert groups, the
 score-correction bias and the routed scaling factor, against the oracle's
 ``topk_route_ex``."""
 
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -91,7 +93,7 @@ def test_route_ex_defaults_equal_plain_router():
         w1 = torch.empty_like(w0)
         i1 = torch.empty_like(i0)
         binding._check(binding.lib().moe_topk_route_ex(
-            binding._ptr(lg), 500, 128, 8, __import__("ctypes").byref(opts), binding._ptr(w1),
+            binding._ptr(lg), 500, 128, 8, ctypes.byref(opts), binding._ptr(w1),
             binding._ptr(i1), binding._stream()))
         torch.cuda.synchronize()
         assert torch.equal(i0, i1) and torch.equal(w0, w1)
