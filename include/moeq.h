@@ -346,6 +346,10 @@ int moe_quant_forward_logits_ex(const void* x, const float* router_logits,
  * the previous call's contents (nothing in it needs to start at zero): calls
  * whose GPU work overlaps -- on different streams, or from several host
  * threads -- race on it and must be serialised by the caller.
+ * The array's device address is looked up once per device and cached for the
+ * life of the process (as is the status word's, for every call): do not keep
+ * using the library on a device after cudaDeviceReset() on it, since the
+ * module's arrays may then live at other addresses.
  */
 int moe_quant_forward_noalloc(const void* x, int T, int H, int I, int E, int k,
                               int bits, int group_size, int has_zp,

@@ -30,6 +30,26 @@ def forward_error(got, ref):
     return float(excess.max() / rms)
 
 
+def plain_error(got, ref):
+    """max_i |got_i - ref_i| / rms(ref), without the output-rounding term."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    rms = float(np.sqrt(np.mean(ref ** 2)))
+    if rms == 0.0:
+        return float(np.max(np.abs(got))) if got.size else 0.0
+    return float(np.max(np.abs(got - ref)) / rms) if got.size else 0.0
+
+
+def check_forward(got, ref, tol=FWD_TOL, what=""):
+    """Assert the forward tolerance; the message gives both the bound's
+    figure and the plain max |err| / rms beside it."""
+    err = forward_error(got, ref)
+    plain = plain_error(got, ref)
+    assert err <= tol, (f"{what} forward error {err:.3e} > {tol:.0e} "
+                        f"(plain max|err|/rms {plain:.3e})")
+    return err, plain
+
+
 def route_tolerance(E):
     """Relative bound on |w_gpu - w_ref| / w_ref for float32 softmax weights:
     E-term float32 sum plus exp and the final division, each a few units of

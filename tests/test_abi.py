@@ -155,3 +155,23 @@ def test_route_opts_marshalling():
     assert plain
     with pytest.raises(ValueError):
         binding.route_opts(64, True, scoring_func="tanh")
+
+
+def test_binding_rejects_bad_weight_tensors():
+    """Every forward wrapper checks the weights, scales and zero points
+    before any pointer reaches the library: host tensors and wrong dtypes
+    are refused (the GPU tests cover strided views)."""
+    import torch
+    from weight_quantized_moe_gb300 import binding
+    w13 = torch.zeros(2, 8, 16, dtype=torch.int8)
+    w2 = torch.zeros(2, 16, 4, dtype=torch.int8)
+    s13 = torch.zeros(2, 8)
+    s2 = torch.zeros(2, 16)
+    with pytest.raises(ValueError, match="CUDA"):
+        binding.check_weights(w13, w2, s13, s2, 8, False)
+    with pytest.raises(TypeError):
+        binding.check_weights(w13.float(), w2, s13, s2, 8, False)
+    with pytest.raises(TypeError):  # uint4 storage is uint8
+        binding.check_weights(w13, w2, s13.half(), s2.half(), 4, True)
+    with pytest.raises(ValueError, match="bits"):
+        binding.check_weights(w13, w2, s13, s2, 6, False)

@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import oracle
-from moe_helpers import FWD_TOL, Layer, forward_error, inputs
+from moe_helpers import FWD_TOL, Layer, check_forward, inputs
 from weight_quantized_moe_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -31,7 +31,7 @@ def _run(layer, T, seed=0, tokens=None, out_cols=None, renorm=True):
     got = out.float().cpu().numpy()[sel]
     if out_cols is not None:
         got = got[:, out_cols]
-    return forward_error(got, ref)
+    return check_forward(got, ref, what=f"{layer.wl.name} T={T}")[0]
 
 
 @pytest.fixture(scope="module")
@@ -65,7 +65,7 @@ def test_forward_k_equals_e_identical_experts():
     W13, W2 = ex.deq13(0), ex.deq2(0)
     h = x.float().cpu().numpy().astype(np.float64) @ W13.T
     ref = (oracle.silu(h[:, :128]) * h[:, 128:]) @ W2.T
-    assert forward_error(out, ref) <= FWD_TOL
+    check_forward(out, ref, what="dense identity")
 
 
 def test_forward_zero_input(tiny):
@@ -84,7 +84,7 @@ def test_forward_invalid_ids_flagged(tiny):
     ids = tid.cpu().numpy()
     ex = tiny.oracle_experts()
     ref = oracle.moe_forward(x.float().cpu().numpy(), ex, tw.cpu().numpy(), ids)
-    assert forward_error(out.float().cpu().numpy(), ref) <= FWD_TOL
+    check_forward(out.float().cpu().numpy(), ref, what="invalid ids")
 
 
 def test_forward_empty_batch(tiny):

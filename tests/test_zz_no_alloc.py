@@ -13,7 +13,7 @@ import ctypes
 import pytest
 import torch
 
-from moe_helpers import FWD_TOL, Layer, forward_error, inputs
+from moe_helpers import Layer, inputs
 from weight_quantized_moe_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -35,8 +35,13 @@ def _noalloc_via_cabi(layer, x, tw, tid):
     return status, out
 
 
-@pytest.mark.parametrize("name,Ts", [("mixtral_decode", (64, 8)), ("fine", (64, 37))])
+@pytest.mark.parametrize("name,Ts", [("mixtral_decode", (64, 8)), ("fine", (64, 37)),
+                                     ("w4a16", (32, 7))])
 def test_noalloc_matches_workspace_forward_twice(name, Ts):
+    """Both calls run the same kernels on the same inputs as the workspace
+    forward, so the outputs must be bitwise equal; the second, smaller call
+    finds the first call's data in the shared scratch (the uint4 case also
+    rewrites its act rows in place there)."""
     layer = Layer(synth.WORKLOADS[name], seed=0)
     layer.free_bf16()
     for call, T in enumerate(Ts):
@@ -47,8 +52,23 @@ def test_noalloc_matches_workspace_forward_twice(name, Ts):
         assert status == 0, mq.binding.lib().mq_last_error_message().decode()
         torch.cuda.synchronize()
         assert mq.mq_device_status() == 0
-        err = forward_error(got.float().cpu().numpy(), ref.float().cpu().numpy())
-        assert err <= FWD_TOL, (call, err)
+        assert torch.equal(got, ref), (name, call, T)
+
+
+def test_noalloc_python_wrapper_matches_workspace_forward():
+    """The binding's wrapper of the same entry point (argument checks, then
+    the C call) gives the workspace forward's result."""
+    layer = Layer(synth.WORKLOADS["w4a16"], seed=1)
+    layer.free_bf16()
+    x, lg = inputs(layer.wl, 5, seed=3)
+    tw, tid = mq.moe_topk_route(lg, layer.k, True)
+    ref = layer.forward(x, tw, tid)
+    got = mq.binding.moe_quant_forward_noalloc(x, layer.q13, layer.q2, layer.s13, layer.s2, tw,
+                                               tid, bits=4, group_size=layer.gs, has_zp=True,
+                                               z13=layer.z13, z2=layer.z2)
+    torch.cuda.synchronize()
+    assert mq.mq_device_status() == 0
+    assert torch.equal(got, ref)
 
 
 def test_noalloc_rejects_oversized_batch():
@@ -61,3 +81,14 @@ def test_noalloc_rejects_oversized_batch():
                                          ctypes.c_void_p(0x10000000), None)
     assert status == binding.MQ_ERR_UNSUPPORTED
     assert b"scratch" in L.mq_last_error_message()
+
+
+def test_noalloc_python_wrapper_rejects_strided_weights():
+    """A transposed (non-contiguous) weight view is refused by the wrapper's
+    checks before its pointer reaches the library."""
+    layer = Layer(synth.WORKLOADS["tiny"], seed=0)
+    x, lg = inputs(layer.wl, 4, seed=1)
+    tw, tid = mq.moe_topk_route(lg, layer.k, True)
+    bad = layer.q13.transpose(1, 2)
+    with pytest.raises(ValueError, match="contiguous"):
+        mq.binding.moe_quant_forward_noalloc(x, bad, layer.q2, layer.s13, layer.s2, tw, tid)

@@ -288,6 +288,39 @@ def forward_flags(x, w13, s13, bits, apply_router_weight_on_input=False):
     return f
 
 
+def check_weights(w13, w2, s13, s2, bits, has_zp, z13=None, z2=None):
+    """Dtype, device and contiguity checks of the expert weights, scales and
+    zero points, shared by every forward wrapper (the kernels read them
+    through raw device pointers and tensor maps)."""
+    if bits == 8:
+        if w13.dtype not in (torch.int8, torch.uint8) or w2.dtype != w13.dtype:
+            raise TypeError("8-bit weights must be int8 (or uint8 codes), both alike")
+        _need(w13, w13.dtype, "w13", 3)
+        _need(w2, w2.dtype, "w2", 3)
+        if s13.dtype not in (torch.float32, torch.float16, torch.bfloat16) or s2.dtype != s13.dtype:
+            raise TypeError("8-bit scales must be float32, float16 or bfloat16, both alike")
+        _need(s13, s13.dtype, "s13")
+        _need(s2, s2.dtype, "s2")
+        E = w13.shape[0]
+        if (s13.numel() < E * w13.shape[1]) != (s2.numel() < E * w2.shape[1]):
+            raise ValueError("per-tensor scales must be given for both w13 and w2")
+        if has_zp:
+            if w13.dtype != torch.uint8:
+                raise ValueError("zero points need uint8 codes")
+            _need(z13, torch.uint8, "z13")
+            _need(z2, torch.uint8, "z2")
+    elif bits == 4:
+        _need(w13, torch.uint8, "w13", 3)
+        _need(w2, torch.uint8, "w2", 3)
+        _need(s13, torch.float16, "s13")
+        _need(s2, torch.float16, "s2")
+        if has_zp:
+            _need(z13, torch.uint8, "z13")
+            _need(z2, torch.uint8, "z2")
+    else:
+        raise ValueError(f"bits must be 8 or 4, got {bits}")
+
+
 def moe_quant_forward(x, w13, w2, s13, s2, topk_w, topk_ids, bits=8, group_size=-1,
                       has_zp=False, z13=None, z2=None, workspace=None, out=None, stream=None,
                       apply_router_weight_on_input=False, inplace=False):
@@ -304,30 +337,7 @@ def moe_quant_forward(x, w13, w2, s13, s2, topk_w, topk_ids, bits=8, group_size=
     E = w13.shape[0]
     I = w13.shape[1] // 2
     k = topk_ids.shape[-1] if topk_ids.dim() == 2 else 1
-    if bits == 8:
-        if w13.dtype not in (torch.int8, torch.uint8) or w2.dtype != w13.dtype:
-            raise TypeError("8-bit weights must be int8 (or uint8 codes), both alike")
-        _need(w13, w13.dtype, "w13", 3)
-        _need(w2, w2.dtype, "w2", 3)
-        if s13.dtype not in (torch.float32, torch.float16, torch.bfloat16) or s2.dtype != s13.dtype:
-            raise TypeError("8-bit scales must be float32, float16 or bfloat16, both alike")
-        _need(s13, s13.dtype, "s13")
-        _need(s2, s2.dtype, "s2")
-        if (s13.numel() < E * w13.shape[1]) != (s2.numel() < E * w2.shape[1]):
-            raise ValueError("per-tensor scales must be given for both w13 and w2")
-        if has_zp:
-            if w13.dtype != torch.uint8:
-                raise ValueError("zero points need uint8 codes")
-            _need(z13, torch.uint8, "z13")
-            _need(z2, torch.uint8, "z2")
-    else:
-        _need(w13, torch.uint8, "w13", 3)
-        _need(w2, torch.uint8, "w2", 3)
-        _need(s13, torch.float16, "s13")
-        _need(s2, torch.float16, "s2")
-        if has_zp:
-            _need(z13, torch.uint8, "z13")
-            _need(z2, torch.uint8, "z2")
+    check_weights(w13, w2, s13, s2, bits, has_zp, z13, z2)
     _need(topk_w, torch.float32, "topk_w")
     _need(topk_ids, torch.int32, "topk_ids")
     flags = forward_flags(x, w13, s13, bits, apply_router_weight_on_input)
@@ -366,6 +376,7 @@ def moe_quant_forward_logits(x, router_logits, w13, w2, s13, s2, top_k, renormal
     I = w13.shape[1] // 2
     if router_logits.shape != (T, E):
         raise ValueError(f"router_logits must be [{T}, {E}]")
+    check_weights(w13, w2, s13, s2, bits, has_zp, z13, z2)
     flags = forward_flags(x, w13, s13, bits, apply_router_weight_on_input)
     opts, plain = route_opts(E, renormalize, scoring_func, num_expert_group, topk_group,
                              e_score_correction_bias, routed_scaling_factor)
@@ -399,6 +410,11 @@ def moe_quant_forward_noalloc(x, w13, w2, s13, s2, topk_w, topk_ids, bits=8, gro
     E = w13.shape[0]
     I = w13.shape[1] // 2
     k = topk_ids.shape[-1] if topk_ids.dim() == 2 else 1
+    check_weights(w13, w2, s13, s2, bits, has_zp, z13, z2)
+    if bits == 8 and (w13.dtype != torch.int8 or s13.dtype != torch.float32
+                      or s13.numel() != E * w13.shape[1]):
+        raise TypeError("moe_quant_forward_noalloc takes the experts_int8 format (int8 codes, "
+                        "float32 per-channel scales) or uint4")
     _need(topk_w, torch.float32, "topk_w")
     _need(topk_ids, torch.int32, "topk_ids")
     if out is None:

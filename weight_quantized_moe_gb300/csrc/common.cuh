@@ -36,10 +36,18 @@ __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v 
 // Programmatic dependent launch.  The forward's kernels are launched so that
 // each may start while its predecessor in the stream is still running.
 // pdl_wait() blocks until the predecessor has completed and its writes are
-// visible; pdl_trigger() lets the successor begin launching.  Every kernel
-// triggers only after its own wait, so when a kernel starts, all kernels
-// before its predecessor have completed: only the predecessor's outputs need
-// the wait.  Without the launch attribute both are no-ops.
+// visible; pdl_trigger() lets the successor begin launching.  Without the
+// launch attribute both are no-ops.
+//
+// Ordering the kernels rely on: the align kernel and the small kernels
+// (gather, act conversion, combine) trigger only after their own wait; the
+// expert GEMMs trigger early, before their wait, so that the next GEMM can
+// set up and start its weight stream.  A GEMM therefore may start while the
+// kernel two launches back is still running (e.g. the down GEMM while the
+// gather runs), but never before the align kernel has completed: before its
+// own wait a GEMM may read only the align kernel's outputs (the chunk table,
+// the sorted slots, the expert counts and offsets), the router's outputs
+// written before the align kernel, and the weights.  Everything else waits.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
