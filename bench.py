@@ -53,6 +53,9 @@ def parse_args():
     p.add_argument("--sweep", default="auto",
                    help="comma list of extra T values timed after the main run, 'auto' or 'none'")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--path", default="auto", choices=["auto", "tc", "decode"],
+                   help="consumers of the expert GEMMs: by GEMM and batch size (auto), "
+                        "tcgen05 for both (tc) or warp-level MMAs for both (decode)")
     return p.parse_args()
 
 
@@ -182,9 +185,9 @@ class ClockSampler:
 class Problem:
     """One layer's weights (quantised on the device) and one batch."""
 
-    def __init__(self, wl, T, seed, device="cuda"):
+    def __init__(self, wl, T, seed, device="cuda", path="auto"):
         import weight_quantized_moe_gb300 as mq
-        self.wl, self.T, self.seed = wl, T, seed
+        self.wl, self.T, self.seed, self.path = wl, T, seed, path
         E, H, I = wl.E, wl.H, wl.I
         self.x = synth.hidden_states(T, H, seed, device=device)
         self.logits = synth.router_logits(T, E, seed, bias=wl.bias, device=device)
@@ -216,7 +219,7 @@ class Problem:
         # routing, align, both expert GEMMs and the combine
         mq.moe_quant_forward_logits(x, logits, q13, q2, s13, s2, wl.k, wl.renormalize,
                                     bits=wl.bits, group_size=wl.group_size, has_zp=wl.has_zp,
-                                    z13=z13, z2=z2, workspace=self.ws, out=out)
+                                    z13=z13, z2=z2, workspace=self.ws, out=out, path=self.path)
         return out
 
     def touched_experts(self):
@@ -452,7 +455,7 @@ def main():
     wl = synth.WORKLOADS[args.workload]
     T = args.T
     peaks = measured_peaks()
-    prob = Problem(wl, T, args.seed + rank)
+    prob = Problem(wl, T, args.seed + rank, path=args.path)
 
     clocks = ClockSampler(torch.cuda.current_device()).start()
     time.sleep(0.3)
@@ -513,7 +516,7 @@ def main():
     elif args.sweep not in ("none", ""):
         extra = [int(t) for t in args.sweep.split(",")]
     for t in extra:
-        p2 = Problem(wl, t, args.seed + rank)
+        p2 = Problem(wl, t, args.seed + rank, path=args.path)
         steps = max(20, args.steps // 4)
         m2 = max_over_ranks(time_loop(p2.step, steps, 3, world), world)
         sweep.append({"T": t, "tokens_per_s": sum_over_ranks(t * steps, world) / (m2 / 1e3),

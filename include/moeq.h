@@ -264,6 +264,23 @@ int moe_quant_forward(const void* x, int T, int H, int I, int E, int k,
 #define MQ_FWD_SCALE_PER_TENSOR 0x8u
 #define MQ_FWD_ACT_F16 0x10u
 #define MQ_FWD_ROUTER_WEIGHT_ON_INPUT 0x20u
+/*
+ * Kernel selection (no counterpart on the pages; the result is the same
+ * forward either way, up to float32 summation order).  The expert GEMMs
+ * stream TMA-staged weight tiles through converter warps that dequantise
+ * them exactly; the products run either on tcgen05 (a single issuing thread
+ * per SM, accumulators in tensor memory) or, for experts holding a few
+ * token-slots, on warp-level MMAs issued by the converter warps themselves.
+ * By default the gate/up GEMM of 8-bit batches of up to 32 tokens takes the
+ * warp-level MMAs and everything else tcgen05 (the faster choice measured
+ * on GB300 for each GEMM and batch size).
+ * MQ_FWD_PATH_TENSOR_CORE forces tcgen05 for both GEMMs, MQ_FWD_PATH_DECODE
+ * the warp-level MMAs for both (MQ_ERR_UNSUPPORTED for uint4 with
+ * group_size 32 or 64); at most one of the two.  Either fits the workspace
+ * the query returns.
+ */
+#define MQ_FWD_PATH_TENSOR_CORE 0x40u
+#define MQ_FWD_PATH_DECODE 0x80u
 
 /*
  * moe_quant_forward_ex -- moe_quant_forward with option flags (above).

@@ -10,7 +10,9 @@ of every sampled token is compared.  The sizes span the kernels' plans:
 16-token tiles with two MMA issuers and split-K 4-8 in the down GEMM
 (Mixtral-shaped T = 1, 8, 32), 64-token tiles (T = 64), the fused router in
 the align kernel (small T·k·ceil(E/32)) and the separate router kernel
-(fine-grained T = 512), and the uint4 path at T = 1.
+(fine-grained T = 512), and the uint4 path at T = 1 -- each with the
+default consumers (warp-level MMAs in the 8-bit gate/up GEMM up to 32
+tokens, tcgen05 elsewhere) and with tcgen05 forced for both GEMMs.
 """
 
 import numpy as np
@@ -46,11 +48,11 @@ def sample_tokens(ids, n_min=16, seed=0):
     return np.array(sorted(chosen))
 
 
-def _logits_case(layer, T, seed):
+def _logits_case(layer, T, seed, path="auto"):
     x, lg = inputs(layer.wl, T, seed)
     out = mq.moe_quant_forward_logits(x, lg, layer.q13, layer.q2, layer.s13, layer.s2, layer.k,
                                       layer.wl.renormalize, bits=layer.bits, group_size=layer.gs,
-                                      has_zp=layer.has_zp, z13=layer.z13, z2=layer.z2)
+                                      has_zp=layer.has_zp, z13=layer.z13, z2=layer.z2, path=path)
     torch.cuda.synchronize()
     assert mq.mq_device_status() == 0
     ow, oid = oracle.topk_route(lg.cpu().numpy(), layer.k, layer.wl.renormalize)
@@ -61,7 +63,7 @@ def _logits_case(layer, T, seed):
     ex = layer.oracle_experts(np.unique(oid[sel]))
     ref = oracle.moe_forward(x.float().cpu().numpy(), ex, ow, oid, tokens=sel)
     got = out.float().cpu().numpy()[sel]
-    return check_forward(got, ref, what=f"{layer.wl.name} T={T} ({sel.size} tokens)")
+    return check_forward(got, ref, what=f"{layer.wl.name} T={T} path={path} ({sel.size} tokens)")
 
 
 @pytest.fixture(scope="module")
@@ -72,21 +74,24 @@ def mixtral():
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("path", ["auto", "tc"])
 @pytest.mark.parametrize("T", [1, 8, 32, 64])
-def test_logits_forward_mixtral_decode(mixtral, T):
-    _logits_case(mixtral, T, seed=20 + T)
+def test_logits_forward_mixtral_decode(mixtral, T, path):
+    _logits_case(mixtral, T, seed=20 + T, path=path)
 
 
+@pytest.mark.parametrize("path", ["auto", "tc"])
 @pytest.mark.parametrize("T", [1, 64, 512])
-def test_logits_forward_fine_grained(T):
+def test_logits_forward_fine_grained(T, path):
     layer = Layer(W["fine"], seed=0)
-    _logits_case(layer, T, seed=30 + T)
+    _logits_case(layer, T, seed=30 + T, path=path)
 
 
+@pytest.mark.parametrize("path", ["auto", "tc"])
 @pytest.mark.parametrize("T", [1, 32])
-def test_logits_forward_w4a16(T):
+def test_logits_forward_w4a16(T, path):
     layer = Layer(W["w4a16"], seed=0)
-    _logits_case(layer, T, seed=40 + T)
+    _logits_case(layer, T, seed=40 + T, path=path)
 
 
 def test_sample_tokens_covers_first_and_last_slot():

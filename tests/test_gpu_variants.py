@@ -48,10 +48,11 @@ def _check(out, x, ex, tw, tid, intermediate="bf16", tol=FWD_TOL, **kw):
                   f"(plain max|err|/rms vs the exact oracle {plain_error(got, exact):.3e});")
 
 
+@pytest.mark.parametrize("path", ["decode", "tc"])
 @pytest.mark.parametrize("shape", ["tiny", "mid"])
 @pytest.mark.parametrize("zp,sdt", [(False, torch.float32), (True, torch.float16),
                                     (False, torch.bfloat16), (True, torch.float32)])
-def test_uint8_codes(shape, zp, sdt):
+def test_uint8_codes(shape, zp, sdt, path):
     E, k, H, I = SHAPES[shape]
     r = np.random.default_rng(E + H + int(zp))
     u13 = r.integers(0, 256, (E, 2 * I, H)).astype(np.uint8)
@@ -64,13 +65,15 @@ def test_uint8_codes(shape, zp, sdt):
     x, tw, tid = _inputs(E, k, H, 37, seed=3)
     dev = lambda a: torch.from_numpy(a).cuda()
     out = mq.moe_quant_forward(x, dev(u13), dev(u2), s13.cuda(), s2.cuda(), tw, tid, bits=8,
-                               has_zp=zp, z13=dev(z13) if zp else None, z2=dev(z2) if zp else None)
+                               has_zp=zp, z13=dev(z13) if zp else None, z2=dev(z2) if zp else None,
+                               path=path)
     _check(out, x, ex, tw, tid)
 
 
+@pytest.mark.parametrize("path", ["decode", "tc"])
 @pytest.mark.parametrize("shape", ["tiny", "mid"])
 @pytest.mark.parametrize("sdt", [torch.float32, torch.bfloat16])
-def test_per_tensor_scale(shape, sdt):
+def test_per_tensor_scale(shape, sdt, path):
     E, k, H, I = SHAPES[shape]
     r = np.random.default_rng(7 + E)
     q13 = r.integers(-127, 128, (E, 2 * I, H)).astype(np.int8)
@@ -80,7 +83,8 @@ def test_per_tensor_scale(shape, sdt):
     ex = oracle.Int8TensorExperts(q13, s13.double().numpy().copy(), q2, s2.double().numpy().copy())
     x, tw, tid = _inputs(E, k, H, 29, seed=5)
     dev = lambda a: torch.from_numpy(a).cuda()
-    out = mq.moe_quant_forward(x, dev(q13), dev(q2), s13.cuda(), s2.cuda(), tw, tid, bits=8)
+    out = mq.moe_quant_forward(x, dev(q13), dev(q2), s13.cuda(), s2.cuda(), tw, tid, bits=8,
+                               path=path)
     _check(out, x, ex, tw, tid)
 
 
@@ -95,48 +99,52 @@ def _int8_layer(E, H, I, seed):
     return ex, dev
 
 
+@pytest.mark.parametrize("path", ["decode", "tc"])
 @pytest.mark.parametrize("shape", ["tiny", "mid"])
-def test_float16_activations(shape):
+def test_float16_activations(shape, path):
     E, k, H, I = SHAPES[shape]
     ex, (q13, q2, s13, s2) = _int8_layer(E, H, I, 11)
     x, tw, tid = _inputs(E, k, H, 33, seed=8)
     x16 = x.to(torch.float16)
-    out = mq.moe_quant_forward(x16, q13, q2, s13, s2, tw, tid, bits=8)
+    out = mq.moe_quant_forward(x16, q13, q2, s13, s2, tw, tid, bits=8, path=path)
     assert out.dtype == torch.float16
     _check(out, x16, ex, tw, tid)
 
 
+@pytest.mark.parametrize("path", ["decode", "tc"])
 @pytest.mark.parametrize("shape", ["tiny", "mid"])
 @pytest.mark.parametrize("renorm", [True, False])
-def test_router_weight_on_input(shape, renorm):
+def test_router_weight_on_input(shape, renorm, path):
     E, k, H, I = SHAPES[shape]
     ex, (q13, q2, s13, s2) = _int8_layer(E, H, I, 13)
     x, tw, tid = _inputs(E, k, H, 41, seed=9, renorm=renorm)
     out = mq.moe_quant_forward(x, q13, q2, s13, s2, tw, tid, bits=8,
-                               apply_router_weight_on_input=True)
+                               apply_router_weight_on_input=True, path=path)
     _check(out, x, ex, tw, tid, apply_router_weight_on_input=True)
 
 
-def test_router_weight_on_input_w4a16():
-    wl = synth.Workload("w4s", E=8, k=2, H=256, I=256, Ts=(16,), bits=4, group_size=64,
+@pytest.mark.parametrize("gs,path", [(64, "tc"), (128, "tc"), (128, "decode")])
+def test_router_weight_on_input_w4a16(gs, path):
+    wl = synth.Workload("w4s", E=8, k=2, H=256, I=256, Ts=(16,), bits=4, group_size=gs,
                         has_zp=True)
     from moe_helpers import Layer, inputs
     layer = Layer(wl, seed=2)
     x, lg = inputs(wl, 19, seed=2)
     tw, tid = mq.moe_topk_route(lg, wl.k, True)
-    out = layer.forward(x, tw, tid, apply_router_weight_on_input=True)
+    out = layer.forward(x, tw, tid, apply_router_weight_on_input=True, path=path)
     _check(out, x, layer.oracle_experts(), tw, tid, apply_router_weight_on_input=True)
 
 
+@pytest.mark.parametrize("path", ["decode", "tc"])
 @pytest.mark.parametrize("dt", [torch.bfloat16, torch.float16])
-def test_inplace_equals_out_of_place(dt):
+def test_inplace_equals_out_of_place(dt, path):
     E, k, H, I = SHAPES["mid"]
     ex, (q13, q2, s13, s2) = _int8_layer(E, H, I, 17)
     x, tw, tid = _inputs(E, k, H, 64, seed=10)
     x = x.to(dt)
-    ref = mq.moe_quant_forward(x, q13, q2, s13, s2, tw, tid, bits=8)
+    ref = mq.moe_quant_forward(x, q13, q2, s13, s2, tw, tid, bits=8, path=path)
     xi = x.clone()
-    got = mq.moe_quant_forward(xi, q13, q2, s13, s2, tw, tid, bits=8, inplace=True)
+    got = mq.moe_quant_forward(xi, q13, q2, s13, s2, tw, tid, bits=8, inplace=True, path=path)
     torch.cuda.synchronize()
     assert got.data_ptr() == xi.data_ptr()
     assert torch.equal(xi, ref)

@@ -29,6 +29,8 @@ from .binding import (  # noqa: F401
     MQ_FWD_SCALE_PER_TENSOR,
     MQ_FWD_ACT_F16,
     MQ_FWD_ROUTER_WEIGHT_ON_INPUT,
+    MQ_FWD_PATH_TENSOR_CORE,
+    MQ_FWD_PATH_DECODE,
     MQ_SCORING_SOFTMAX,
     MQ_SCORING_SIGMOID,
     MqRouteOpts,

@@ -27,6 +27,9 @@ MQ_FWD_SCALE_BF16 = 0x4
 MQ_FWD_SCALE_PER_TENSOR = 0x8
 MQ_FWD_ACT_F16 = 0x10
 MQ_FWD_ROUTER_WEIGHT_ON_INPUT = 0x20
+MQ_FWD_PATH_TENSOR_CORE = 0x40
+MQ_FWD_PATH_DECODE = 0x80
+_PATH_FLAGS = {"auto": 0, "tc": MQ_FWD_PATH_TENSOR_CORE, "decode": MQ_FWD_PATH_DECODE}
 # mq_route_opts.scoring_func
 MQ_SCORING_SOFTMAX = 0
 MQ_SCORING_SIGMOID = 1
@@ -266,12 +269,16 @@ def moe_quant_forward_workspace(T, H, I, E, k, bits=8, group_size=-1) -> int:
     return int(lib().moe_quant_forward_workspace(T, H, I, E, k, bits, group_size))
 
 
-def forward_flags(x, w13, s13, bits, apply_router_weight_on_input=False):
+def forward_flags(x, w13, s13, bits, apply_router_weight_on_input=False, path="auto"):
     """moe_quant_forward_ex flags implied by the tensors' dtypes and shapes:
     uint8 8-bit codes (moe_wna16), float16 / bfloat16 scales, one scale per
     expert (fewer scale elements than experts x output rows), float16
-    activations."""
-    f = 0
+    activations; and the consumers of the expert GEMMs: path "auto" (by
+    GEMM and batch size), "tc" (tcgen05 for both) or "decode" (warp-level
+    MMAs for both)."""
+    if path not in _PATH_FLAGS:
+        raise ValueError("path must be 'auto', 'tc' or 'decode'")
+    f = _PATH_FLAGS[path]
     if bits == 8:
         if w13.dtype == torch.uint8:
             f |= MQ_FWD_W8_UINT8
@@ -323,7 +330,7 @@ def check_weights(w13, w2, s13, s2, bits, has_zp, z13=None, z2=None):
 
 def moe_quant_forward(x, w13, w2, s13, s2, topk_w, topk_ids, bits=8, group_size=-1,
                       has_zp=False, z13=None, z2=None, workspace=None, out=None, stream=None,
-                      apply_router_weight_on_input=False, inplace=False):
+                      apply_router_weight_on_input=False, inplace=False, path="auto"):
     """The fused expert MLP (moe_quant_forward / moe_quant_forward_ex in
     include/moeq.h).  x is bf16 or f16 [T, H]; 8-bit weights are int8 with
     float32 scales (experts_int8), or uint8 codes with float32 / float16 /
@@ -340,7 +347,7 @@ def moe_quant_forward(x, w13, w2, s13, s2, topk_w, topk_ids, bits=8, group_size=
     check_weights(w13, w2, s13, s2, bits, has_zp, z13, z2)
     _need(topk_w, torch.float32, "topk_w")
     _need(topk_ids, torch.int32, "topk_ids")
-    flags = forward_flags(x, w13, s13, bits, apply_router_weight_on_input)
+    flags = forward_flags(x, w13, s13, bits, apply_router_weight_on_input, path)
     ws_need = moe_quant_forward_workspace(T, H, I, E, k, bits, group_size)
     if workspace is None:
         workspace = torch.empty(max(ws_need, 16), dtype=torch.uint8, device=x.device)
@@ -363,7 +370,7 @@ def moe_quant_forward_logits(x, router_logits, w13, w2, s13, s2, top_k, renormal
                              out=None, stream=None, apply_router_weight_on_input=False,
                              inplace=False, scoring_func="softmax", num_expert_group=0,
                              topk_group=0, e_score_correction_bias=None,
-                             routed_scaling_factor=1.0):
+                             routed_scaling_factor=1.0, path="auto"):
     """Routing and the expert MLP in one call (moe_quant_forward_logits, or
     moe_quant_forward_logits_ex with router options, in include/moeq.h): the
     same result as moe_topk_route followed by moe_quant_forward, bitwise."""
@@ -377,7 +384,7 @@ def moe_quant_forward_logits(x, router_logits, w13, w2, s13, s2, top_k, renormal
     if router_logits.shape != (T, E):
         raise ValueError(f"router_logits must be [{T}, {E}]")
     check_weights(w13, w2, s13, s2, bits, has_zp, z13, z2)
-    flags = forward_flags(x, w13, s13, bits, apply_router_weight_on_input)
+    flags = forward_flags(x, w13, s13, bits, apply_router_weight_on_input, path)
     opts, plain = route_opts(E, renormalize, scoring_func, num_expert_group, topk_group,
                              e_score_correction_bias, routed_scaling_factor)
     ws_need = int(lib().moe_quant_forward_logits_workspace(T, H, I, E, top_k, bits, group_size))

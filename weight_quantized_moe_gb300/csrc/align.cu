@@ -15,7 +15,8 @@
 // Optionally (chunk > 0) it also cuts each expert's padded segment into
 // chunks of at most `chunk` slots, the token tiles of the expert GEMMs:
 // chunk_start[e] = index of expert e's first chunk (chunk_start[E] = the
-// number of chunks) and chunk_expert[c] = the expert of chunk c.
+// number of chunks) and chunk_expert[c] = the expert of chunk c.  With
+// counts != null it also writes each expert's number of token-slots.
 //
 // With PER > 0 it first routes the T tokens itself (router logits in, the
 // router's code, one warp per token), writing topk_w and the ids it then
@@ -34,8 +35,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     align_kernel(int32_t* __restrict__ ids, int S, int E, int bm, int32_t* __restrict__ sorted,
                  int32_t* __restrict__ block_expert, int32_t* __restrict__ offsets,
                  int32_t* __restrict__ num_padded, int chunk, int32_t* __restrict__ chunk_expert,
-                 int32_t* __restrict__ chunk_start, const float* __restrict__ logits, int T,
-                 int k, int renorm, float* __restrict__ topk_w, unsigned* status) {
+                 int32_t* __restrict__ chunk_start, int32_t* __restrict__ counts,
+                 const float* __restrict__ logits, int T, int k, int renorm,
+                 float* __restrict__ topk_w, unsigned* status) {
   extern __shared__ int smem[];
   int* hist = smem;                   // [kWarps][E]
   int* warp_tot = smem + kWarps * E;  // [kWarps] scan scratch
@@ -106,6 +108,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int start = incl - padded + (warp ? warp_tot[warp - 1] : 0);
   if (e < E) {
     offsets[e] = start;
+    if (counts) counts[e] = count;
     int run = start;
     for (int w = 0; w < kWarps; ++w) {
       const int c = hist[w * E + e];
@@ -181,8 +184,8 @@ template <int PER>
 cudaError_t launch_align_impl(int32_t* ids, int T, int k, int E, int bm, int32_t* sorted,
                               int32_t* block_expert, int32_t* offsets, int32_t* num_padded,
                               unsigned* status, cudaStream_t st, int chunk, int32_t* chunk_expert,
-                              int32_t* chunk_start, const float* logits, int renorm,
-                              float* topk_w) {
+                              int32_t* chunk_start, int32_t* counts, const float* logits,
+                              int renorm, float* topk_w) {
   size_t smem = (size_t)(kWarps * E + 2 * kWarps) * sizeof(int);
   if (PER > 0) smem += (size_t)kWarps * 32 * (sizeof(float) + sizeof(int));  // routing scratch
   auto kern = align_kernel<PER>;
@@ -193,8 +196,8 @@ cudaError_t launch_align_impl(int32_t* ids, int T, int k, int E, int bm, int32_t
   }
   const cudaError_t err =
       launch_pdl(kern, dim3(1), dim3(kThreads), smem, st, ids, T * k, E, bm, sorted,
-                 block_expert, offsets, num_padded, chunk, chunk_expert, chunk_start, logits, T, k,
-                 renorm, topk_w, status);
+                 block_expert, offsets, num_padded, chunk, chunk_expert, chunk_start, counts,
+                 logits, T, k, renorm, topk_w, status);
   return err != cudaSuccess ? err : cudaGetLastError();
 }
 
@@ -203,28 +206,28 @@ cudaError_t launch_align_impl(int32_t* ids, int T, int k, int E, int bm, int32_t
 cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int bm, int32_t* sorted,
                          int32_t* block_expert, int32_t* offsets, int32_t* num_padded,
                          unsigned* status, cudaStream_t st, int chunk, int32_t* chunk_expert,
-                         int32_t* chunk_start) {
+                         int32_t* chunk_start, int32_t* counts) {
   return launch_align_impl<0>(const_cast<int32_t*>(ids), T, k, E, bm, sorted, block_expert,
                               offsets, num_padded, status, st, chunk, chunk_expert, chunk_start,
-                              nullptr, 0, nullptr);
+                              counts, nullptr, 0, nullptr);
 }
 
 cudaError_t launch_route_align(const float* logits, int renorm, float* topk_w, int32_t* topk_ids,
                                int T, int k, int E, int bm, int32_t* sorted,
                                int32_t* block_expert, int32_t* offsets, int32_t* num_padded,
                                unsigned* status, cudaStream_t st, int chunk,
-                               int32_t* chunk_expert, int32_t* chunk_start) {
+                               int32_t* chunk_expert, int32_t* chunk_start, int32_t* counts) {
   if (!route_fused(T, k, E)) {
     const cudaError_t err = launch_route(logits, T, E, k, renorm, topk_w, topk_ids, st);
     if (err != cudaSuccess) return err;
     return launch_align(topk_ids, T, k, E, bm, sorted, block_expert, offsets, num_padded, status,
-                        st, chunk, chunk_expert, chunk_start);
+                        st, chunk, chunk_expert, chunk_start, counts);
   }
   const int per = (E + 31) / 32;
 #define MQ_RA(P)                                                                               \
   return launch_align_impl<P>(topk_ids, T, k, E, bm, sorted, block_expert, offsets, num_padded, \
-                              status, st, chunk, chunk_expert, chunk_start, logits, renorm,      \
-                              topk_w);
+                              status, st, chunk, chunk_expert, chunk_start, counts, logits,      \
+                              renorm, topk_w);
   switch (per) {
     case 1: MQ_RA(1)
     case 2: MQ_RA(2)

@@ -106,18 +106,59 @@ inline size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
 // split-K partial outputs (fp32).
 constexpr int kAlignBlock = 16;
 
+// Which consumers the expert GEMMs run.  With a few token-slots per expert
+// the converter warps can multiply with warp-level MMAs themselves
+// (TcPlan::sync1 / sync2; token tiles of 16 or 32 rows) instead of feeding
+// one tcgen05.mma issuer.  Measured on GB300 (kernel times per
+// launch): the warp-MMA gate/up GEMM is faster for batches of up to
+// kSyncGateUpMaxT tokens of 8-bit codes (Mixtral-shaped T=1: 49 vs 56 us,
+// T=8: 150 vs 163, T=32: 171 vs 179); the down GEMM (bf16 conversion,
+// heavier) and uint4 are faster on the tcgen05 consumers.  On GB300 each
+// mma.sync takes about 8 cycles of its scheduler's issue that dequant
+// instructions cannot overlap, so the warp MMAs pay off only where the
+// conversion is cheap and few 8-token groups run.
+constexpr int kSyncGateUpMaxT = 32;
+
+TcPlan fwd_plan(int T, int H, int I, int E, int k, int bits, int group_size, unsigned flags) {
+  TcPlan pl = tc_plan(T, H, I, E, k, bits);
+  const bool ok = dec_supported(bits, group_size, H, I);
+  if (flags & MQ_FWD_PATH_TENSOR_CORE) return pl;
+  if (flags & MQ_FWD_PATH_DECODE) {
+    if (!ok) return pl;
+    pl.sync1 = pl.sync2 = true;
+    // an expert receives at most one slot per token: up to 16 tokens every
+    // expert fits one 16-row tile (uint4 keeps 16-row tiles: their register
+    // budget holds two 8-token MMA groups)
+    pl.bn = (bits == 8 && T > 16) ? 32 : 16;
+    // the workspace holds the warp-MMA splits for batches where that mode is
+    // the default's size class, else the tcgen05 plan's
+    if (T <= 64) pl.splits = dec_splits(T, H, I, E, k, bits);
+    return pl;
+  }
+  // default: warp-MMA gate/up GEMM for small 8-bit batches (the tcgen05 plan
+  // uses 16-row tiles up to 32 tokens too, so both GEMMs share the chunk
+  // table)
+  if (ok && bits == 8 && T <= kSyncGateUpMaxT) pl.sync1 = true;
+  return pl;
+}
+
 struct WsLayout {
-  size_t sorted, block_expert, offsets, num_padded, chunk_expert, chunk_start, xs, xinv, act,
-      act_inv, y, topk_w, topk_ids, total;
+  size_t sorted, block_expert, offsets, num_padded, chunk_expert, chunk_start, counts, xs, xinv,
+      act, act_inv, y, topk_w, topk_ids, total;
   int64_t cap;
   TcPlan plan;
 };
 
 // with_route: the forward routes itself (router logits in), holding topk_w
 // and topk_ids in the workspace too.
-WsLayout ws_layout(int T, int H, int I, int E, int k, int bits, bool with_route = false) {
+WsLayout ws_layout(int T, int H, int I, int E, int k, int bits, int group_size,
+                   bool with_route = false) {
   WsLayout L;
   L.plan = tc_plan(T, H, I, E, k, bits);
+  // partial outputs for every consumer choice (the warp-MMA plan's splits
+  // and the tcgen05 plan's), so that a forced choice fits the same workspace
+  const TcPlan fp = fwd_plan(T, H, I, E, k, bits, group_size, MQ_FWD_PATH_DECODE);
+  const int ysplits = L.plan.splits > fp.splits ? L.plan.splits : fp.splits;
   const int bm = kAlignBlock;
   const int64_t S = (int64_t)T * k;
   const int64_t cap = moe_align_capacity(T, k, E, bm);
@@ -129,11 +170,12 @@ WsLayout ws_layout(int T, int H, int I, int E, int k, int bits, bool with_route 
   L.num_padded = off;   off += align256(sizeof(int32_t));
   L.chunk_expert = off; off += align256(sizeof(int32_t) * (size_t)(cap / bm));
   L.chunk_start = off;  off += align256(sizeof(int32_t) * (size_t)(E + 1));
+  L.counts = off;       off += align256(sizeof(int32_t) * (size_t)E);
   L.xs = off;           off += align256(sizeof(__half) * (size_t)cap * (size_t)H);
   L.xinv = off;         off += align256(sizeof(float) * (size_t)cap);
   L.act = off;          off += align256(sizeof(__nv_bfloat16) * (size_t)cap * (size_t)I);
   L.act_inv = off;      off += align256(sizeof(float) * (size_t)cap);
-  L.y = off;            off += align256(sizeof(float) * (size_t)L.plan.splits * (size_t)S * (size_t)H);
+  L.y = off;            off += align256(sizeof(float) * (size_t)ysplits * (size_t)S * (size_t)H);
   L.topk_w = off;       if (with_route) off += align256(sizeof(float) * (size_t)S);
   L.topk_ids = off;     if (with_route) off += align256(sizeof(int32_t) * (size_t)S);
   L.total = off;
@@ -340,7 +382,7 @@ MQ_EXPORT size_t moe_quant_forward_workspace(int T, int H, int I, int E, int k, 
                                              int group_size) {
   if (T < 0 || H <= 0 || I <= 0 || E < 1 || k < 1 || k > E) return 0;
   if (!fmt_ok(bits, group_size, 0)) return 0;
-  return ws_layout(T, H, I, E, k, bits).total;
+  return ws_layout(T, H, I, E, k, bits, group_size).total;
 }
 
 MQ_EXPORT int moe_quant_forward_ex(const void* x, int T, int H, int I, int E, int k, int bits,
@@ -369,7 +411,8 @@ static int forward_impl(const void* x, int T, int H, int I, int E, int k, int bi
                         unsigned flags, void* stream) {
   constexpr unsigned kW8Flags = MQ_FWD_W8_UINT8 | MQ_FWD_SCALE_F16 | MQ_FWD_SCALE_BF16 |
                                 MQ_FWD_SCALE_PER_TENSOR;
-  constexpr unsigned kAllFlags = kW8Flags | MQ_FWD_ACT_F16 | MQ_FWD_ROUTER_WEIGHT_ON_INPUT;
+  constexpr unsigned kAllFlags = kW8Flags | MQ_FWD_ACT_F16 | MQ_FWD_ROUTER_WEIGHT_ON_INPUT |
+                                 MQ_FWD_PATH_TENSOR_CORE | MQ_FWD_PATH_DECODE;
   if (T < 0 || H <= 0 || I <= 0 || E < 1) return fail(MQ_ERR_INVALID_ARG, "bad T, H, I or E");
   if (k < 1 || k > E || k > 32) return fail(MQ_ERR_INVALID_ARG, "need 1 <= k <= min(E, 32)");
   if (E > 1024) return fail(MQ_ERR_UNSUPPORTED, "E must be <= 1024");
@@ -378,6 +421,10 @@ static int forward_impl(const void* x, int T, int H, int I, int E, int k, int bi
     return fail(MQ_ERR_UNSUPPORTED, "uint8 codes and scale options apply to bits = 8 only");
   if ((flags & MQ_FWD_SCALE_F16) && (flags & MQ_FWD_SCALE_BF16))
     return fail(MQ_ERR_UNSUPPORTED, "scales are float16 or bfloat16, not both");
+  if ((flags & MQ_FWD_PATH_TENSOR_CORE) && (flags & MQ_FWD_PATH_DECODE))
+    return fail(MQ_ERR_INVALID_ARG, "MQ_FWD_PATH_TENSOR_CORE and MQ_FWD_PATH_DECODE exclude each other");
+  if ((flags & MQ_FWD_PATH_DECODE) && !dec_supported(bits, group_size, H, I))
+    return fail(MQ_ERR_UNSUPPORTED, "the warp-MMA consumers take 8-bit codes or uint4 with group_size 128 or 256");
   const bool w8zp = bits == 8 && group_size == -1 && has_zp == 1 && (flags & MQ_FWD_W8_UINT8);
   if (!fmt_ok(bits, group_size, has_zp) && !w8zp)
     return fail(MQ_ERR_UNSUPPORTED,
@@ -394,6 +441,8 @@ static int forward_impl(const void* x, int T, int H, int I, int E, int k, int bi
   if (!has_zp && (z13 || z2)) return fail(MQ_ERR_INVALID_ARG, "zero points given with has_zp = 0");
   if (!aligned16(x) || !aligned16(w13) || !aligned16(w2) || !aligned16(out) || !aligned16(workspace))
     return fail(MQ_ERR_INVALID_ARG, "x, w13, w2, out and workspace must be 16-byte aligned");
+  if (!aligned16(s13) || !aligned16(s2) || (z13 && !aligned16(z13)) || (z2 && !aligned16(z2)))
+    return fail(MQ_ERR_INVALID_ARG, "scales and zero points must be 16-byte aligned");
   {
     const char* xb = static_cast<const char*>(x);
     const char* ob = static_cast<const char*>(out);
@@ -403,7 +452,8 @@ static int forward_impl(const void* x, int T, int H, int I, int E, int k, int bi
     if (ob != xb && ob < xb + nb && xb < ob + nb)
       return fail(MQ_ERR_INVALID_ARG, "out overlaps x (only out == x is allowed)");
   }
-  const WsLayout L = ws_layout(T, H, I, E, k, bits, logits != nullptr);
+  const WsLayout L = ws_layout(T, H, I, E, k, bits, group_size, logits != nullptr);
+  const TcPlan plan = fwd_plan(T, H, I, E, k, bits, group_size, flags);
   const int bm = kAlignBlock;
   if (ws_bytes < L.total)
     return fail(MQ_ERR_WORKSPACE, "workspace %zu bytes, need %zu", ws_bytes, L.total);
@@ -431,6 +481,7 @@ static int forward_impl(const void* x, int T, int H, int I, int E, int k, int bi
   a.num_padded = reinterpret_cast<int32_t*>(ws + L.num_padded);
   a.chunk_expert = reinterpret_cast<int32_t*>(ws + L.chunk_expert);
   a.chunk_start = reinterpret_cast<int32_t*>(ws + L.chunk_start);
+  a.counts = reinterpret_cast<int32_t*>(ws + L.counts);
   a.act = reinterpret_cast<__nv_bfloat16*>(ws + L.act);
   a.y = reinterpret_cast<float*>(ws + L.y);
   a.bm = bm;
@@ -446,15 +497,17 @@ static int forward_impl(const void* x, int T, int H, int I, int E, int k, int bi
                 : launch_route_ex(logits, T, E, k, ro, rw, rid, st);
     if (err != cudaSuccess) return cuda_fail(err, "forward: route launch");
   }
+  const int chunk = plan.bn;  // token rows per tile of the chunk table
   {
     LaunchScope ls(MQ_PROF_ALIGN, st);
     if (fused)
       err = launch_route_align(logits, ro.renorm, rw, rid, T, k, E, bm, a.sorted, a.block_expert,
-                               a.offsets, a.num_padded, a.status, st, L.plan.bn, a.chunk_expert,
-                               a.chunk_start);
+                               a.offsets, a.num_padded, a.status, st, chunk, a.chunk_expert,
+                               a.chunk_start, a.counts);
     else
       err = launch_align(topk_ids, T, k, E, bm, a.sorted, a.block_expert, a.offsets,
-                         a.num_padded, a.status, st, L.plan.bn, a.chunk_expert, a.chunk_start);
+                         a.num_padded, a.status, st, chunk, a.chunk_expert, a.chunk_start,
+                         a.counts);
   }
   if (err != cudaSuccess) return cuda_fail(err, "forward: align launch");
   void* xs = ws + L.xs;
@@ -466,23 +519,25 @@ static int forward_impl(const void* x, int T, int H, int I, int E, int k, int bi
   if (err != cudaSuccess) return cuda_fail(err, "forward: gather launch");
   {
     LaunchScope ls(MQ_PROF_GEMM1, st);
-    err = launch_gemm1_tc(a, L.plan, xs, xinv, st);
+    err = launch_gemm1_tc(a, plan, xs, xinv, st);
   }
   if (err != cudaSuccess) return cuda_fail(err, "forward: gate/up GEMM launch");
   float* act_inv = reinterpret_cast<float*>(ws + L.act_inv);
-  if (bits == 4) {  // the uint4 down GEMM runs f16 operands; the 8-bit one reads bf16 act
+  if (bits == 4 && !plan.sync2) {
+    // the tcgen05 uint4 down GEMM runs f16 operands; the 8-bit one and the
+    // warp-MMA mode read bf16 act
     LaunchScope ls(MQ_PROF_ACTF16, st);
     err = launch_act_to_f16(a, act_inv, st);
     if (err != cudaSuccess) return cuda_fail(err, "forward: act conversion launch");
   }
   {
     LaunchScope ls(MQ_PROF_GEMM2, st);
-    err = launch_gemm2_tc(a, L.plan, act_inv, a.y, st);
+    err = launch_gemm2_tc(a, plan, act_inv, a.y, st);
   }
   if (err != cudaSuccess) return cuda_fail(err, "forward: down GEMM launch");
   {
     LaunchScope ls(MQ_PROF_COMBINE, st);
-    err = launch_combine_splits(a, a.y, L.plan.splits, st);
+    err = launch_combine_splits(a, a.y, plan.splits, st);
   }
   if (err != cudaSuccess) return cuda_fail(err, "forward: combine launch");
   return MQ_OK;
@@ -503,7 +558,7 @@ MQ_EXPORT size_t moe_quant_forward_logits_workspace(int T, int H, int I, int E, 
                                                     int group_size) {
   if (T < 0 || H <= 0 || I <= 0 || E < 1 || k < 1 || k > E) return 0;
   if (!fmt_ok(bits, group_size, 0)) return 0;
-  return ws_layout(T, H, I, E, k, bits, true).total;
+  return ws_layout(T, H, I, E, k, bits, group_size, true).total;
 }
 
 MQ_EXPORT int moe_quant_forward_logits(const void* x, const float* router_logits, int T, int H,

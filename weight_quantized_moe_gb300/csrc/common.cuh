@@ -116,14 +116,15 @@ MQ_HIDDEN cudaError_t launch_route_align(const float* logits, int renorm, float*
                                          int32_t* sorted, int32_t* block_expert,
                                          int32_t* offsets, int32_t* num_padded, unsigned* status,
                                          cudaStream_t st, int chunk, int32_t* chunk_expert,
-                                         int32_t* chunk_start);
+                                         int32_t* chunk_start, int32_t* counts);
 // chunk > 0 also writes the chunk table of the expert GEMMs' token tiles
-// (chunk_expert [cap / bm], chunk_start [E + 1]).
+// (chunk_expert [cap / bm], chunk_start [E + 1]); counts != null the number
+// of token-slots of each expert [E].
 MQ_HIDDEN cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int bm,
                                    int32_t* sorted, int32_t* block_expert, int32_t* offsets,
                                    int32_t* num_padded, unsigned* status, cudaStream_t st,
                                    int chunk = 0, int32_t* chunk_expert = nullptr,
-                                   int32_t* chunk_start = nullptr);
+                                   int32_t* chunk_start = nullptr, int32_t* counts = nullptr);
 
 struct MoeArgs {
   const void* x;          // bf16, or f16 with MQ_FWD_ACT_F16
@@ -147,6 +148,7 @@ struct MoeArgs {
   int32_t* num_padded;    // [1]
   int32_t* chunk_expert;  // [cap / bm]: expert of each token tile (chunk)
   int32_t* chunk_start;   // [E + 1]: first chunk of each expert; [E] = number of chunks
+  int32_t* counts;        // [E]: token-slots of each expert
   __nv_bfloat16* act;     // [cap, I]
   float* y;               // [S, H]
   int bm;
@@ -157,6 +159,8 @@ struct MoeArgs {
 struct TcPlan {
   int bn;      // token-slots per tile at most (MMA N <= bn); the align block is 16
   int splits;  // K splits of the down GEMM
+  bool sync1;  // gate/up GEMM: warp-MMA consumers (few tokens per expert), not tcgen05
+  bool sync2;  // down GEMM: the same
 };
 MQ_HIDDEN TcPlan tc_plan(int T, int H, int I, int E, int k, int bits);
 MQ_HIDDEN int tc_num_sms();
@@ -168,6 +172,11 @@ MQ_HIDDEN cudaError_t launch_gemm2_tc(const MoeArgs& a, const TcPlan& pl, const 
                                       float* ypart, cudaStream_t st);
 MQ_HIDDEN cudaError_t launch_combine_splits(const MoeArgs& a, const float* ypart, int splits,
                                             cudaStream_t st);
+
+// Warp-MMA ("decode") mode of the expert GEMMs: the formats it takes, and
+// the K splits of its down GEMM.
+MQ_HIDDEN bool dec_supported(int bits, int group_size, int H, int I);
+MQ_HIDDEN int dec_splits(int T, int H, int I, int E, int k, int bits);
 
 // Records `msg` as the calling thread's mq_last_error_message(); returns status.
 MQ_HIDDEN int mq_set_error(int status, const char* msg);

@@ -25,15 +25,18 @@
 //   MQ_DEV_WAIT_TIMEOUT, stops issuing work, drains its own copies and MMAs
 //   (with a bound again), frees its tensor memory and exits.
 #include "common.cuh"
+#include "dequant.cuh"
 #include "sm100_ptx.cuh"
 
 #include <cudaTypedefs.h>
 
+#include <cmath>
 #include <mutex>
 
 namespace {
 
 using namespace mq::ptx;
+using namespace mq::dq;
 
 constexpr int kBK = 128;                  // K elements per weight stage (one 16 KB TMA box)
 constexpr int kG = 2;                     // weight stages per MMA step
@@ -90,8 +93,51 @@ struct TileCfg {
   static_assert(kAStagesSmem >= 3, "weight ring depth");
 };
 
+// Warp-MMA consumer mode (few token-slots per expert): no tensor memory and
+// no MMA issuer; each converter warp multiplies its converted weight rows
+// straight from registers with mma.sync (m16n8k16, f32 accumulate).  The
+// activation ring is kSteps MMA steps deep -- an even number, so that every
+// slot serves one converter group only (step st uses slot st % kSteps and
+// belongs to group st % 2): each converter warp has then itself seen the
+// slot's previous fill land, which makes its parity wait exact.  The two
+// groups' partial sums reach the epilogue through kPBufs shared-memory
+// buffers of [group][column][row] floats (row stride kPStride keeps the
+// converters' scattered stores and the epilogue's row reads free of bank
+// conflicts).
+template <int BN>
+struct SyncCfg {
+  static constexpr int kNI = 1;
+  static constexpr int kThreads = (kEpiWarp0 + 4) * 32;
+  static constexpr int kSteps = 4;
+  static_assert(kSteps % 2 == 0, "one converter group per activation slot");
+  static constexpr int kACol0 = 0;
+  static constexpr int kBBytesK = BN * kBK * 2;
+  static constexpr int kBBytes = kG * kBBytesK;
+  static constexpr int kPStride = kTileM + 4;
+  static constexpr int kPBytes = kConvGroups * BN * kPStride * 4;
+  static constexpr int kPBufs = BN <= 16 ? 2 : 1;
+  static constexpr int kAFit = (kSmemBudget + 4096 - kSteps * kBBytes - kPBufs * kPBytes) / kABytes;
+  static constexpr int kAStagesSmem = (kAFit > 12 ? 12 : kAFit) & ~1;
+  static_assert(kAStagesSmem >= 4, "weight ring depth");
+};
+
+template <int MODE, int BITS, int BN, bool SYNC>
+struct CfgSel {
+  using type = TileCfg<BN, (BN == 16 && !(MODE == 2 && BITS == 8)) ? 2 : 1>;
+};
 template <int MODE, int BITS, int BN>
-using CfgOf = TileCfg<BN, (BN == 16 && !(MODE == 2 && BITS == 8)) ? 2 : 1>;
+struct CfgSel<MODE, BITS, BN, true> {
+  using type = SyncCfg<BN>;
+};
+template <int MODE, int BITS, int BN, bool SYNC = false>
+using CfgOf = typename CfgSel<MODE, BITS, BN, SYNC>::type;
+
+// Shared memory of the warp-MMA mode's partial-sum buffers (0 otherwise).
+template <bool SYNC, int BN>
+constexpr int partial_bytes() {
+  if constexpr (SYNC) return SyncCfg<BN>::kPBufs * SyncCfg<BN>::kPBytes;
+  else return 0;
+}
 
 struct TcParams {
   int H, I, E, k, S;
@@ -102,6 +148,7 @@ struct TcParams {
   const int32_t* offsets;       // [E + 1] padded expert segments (16-slot blocks)
   const int32_t* chunk_expert;  // expert of each token tile
   const int32_t* chunk_start;   // [E + 1] first token tile of each expert
+  const int32_t* counts;        // [E] token-slots of each expert (warp-MMA mode)
   const void* scale;      // 8-bit: scales of this GEMM's weights (kind below)
   int scale_kind;         // 8-bit scales: 0 float32, 1 float16, 2 bfloat16
   int scale_per_tensor;   // 8-bit: one scale per expert instead of one per row
@@ -256,75 +303,11 @@ __device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity) {
   }
 }
 
-// 8-bit codes x4 -> two f16x2 words, exact.  xm = 0x80808080 turns an
-// int8 code into u = q + 128 (the sign bit flipped), xm = 0 keeps a uint8
-// code u; the half with bits 0x64uu is 1024 + u, and subtracting
-// zz = 1024 + z (z = 128, or the row's zero point) leaves u - z.
-__device__ __forceinline__ void int8x4_to_f16x4(uint32_t w, uint32_t xm, uint32_t zz,
-                                                uint32_t& lo, uint32_t& hi) {
-  const uint32_t u = w ^ xm;
-  const uint32_t v0 = __byte_perm(u, 0x64u, 0x4140);  // [u0, 0x64, u1, 0x64]
-  const uint32_t v1 = __byte_perm(u, 0x64u, 0x4342);  // [u2, 0x64, u3, 0x64]
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(v0), "r"(zz));
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(v1), "r"(zz));
-}
-
-// 16 codes -> 8 words of f16 pairs.
-__device__ __forceinline__ void convert16(const uint4& v, uint32_t xm, uint32_t zz, uint32_t* w) {
-  int8x4_to_f16x4(v.x, xm, zz, w[0], w[1]);
-  int8x4_to_f16x4(v.y, xm, zz, w[2], w[3]);
-  int8x4_to_f16x4(v.z, xm, zz, w[4], w[5]);
-  int8x4_to_f16x4(v.w, xm, zz, w[6], w[7]);
-}
-
-// (a0 - b, a1 - b) as one paired f32 subtraction (sm_100 family).
-__device__ __forceinline__ void f32x2_sub(float a0, float a1, float b, float& r0, float& r1) {
-  asm("{.reg .b64 xa, xb, xd;\n\t"
-      "mov.b64 xa, {%2, %3};\n\t"
-      "mov.b64 xb, {%4, %4};\n\t"
-      "sub.rn.f32x2 xd, xa, xb;\n\t"
-      "mov.b64 {%0, %1}, xd;}"
-      : "=f"(r0), "=f"(r1)
-      : "f"(a0), "f"(a1), "f"(b));
-}
-
-// 8-bit codes x4 -> two bf16x2 words, exact.  u = code ^ xm as above; the
-// float with bits 0x4B0000uu is 2^23 + u, and subtracting zf = 2^23 + z
-// leaves u - z exactly; |u - z| < 256 has at most 8 significant bits, so the
-// top 16 bits of that float are the exact bfloat16.  (Measured faster than
-// building 128 + (u & 127) and 128 or 256 as bfloat16 and subtracting those.)
-__device__ __forceinline__ void int8x4_to_bf16x4(uint32_t w, uint32_t xm, float zf, uint32_t& lo,
-                                                 uint32_t& hi) {
-  const uint32_t u = w ^ xm;
-  float f0, f1, f2, f3;
-  f32x2_sub(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7440)),
-            __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7441)), zf, f0, f1);
-  f32x2_sub(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7442)),
-            __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7443)), zf, f2, f3);
-  lo = __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632);
-  hi = __byte_perm(__float_as_uint(f2), __float_as_uint(f3), 0x7632);
-}
-
-// 16 codes -> 8 words of bf16 pairs.
-__device__ __forceinline__ void convert16_bf16(const uint4& v, uint32_t xm, float zf, uint32_t* w) {
-  int8x4_to_bf16x4(v.x, xm, zf, w[0], w[1]);
-  int8x4_to_bf16x4(v.y, xm, zf, w[2], w[3]);
-  int8x4_to_bf16x4(v.z, xm, zf, w[4], w[5]);
-  int8x4_to_bf16x4(v.w, xm, zf, w[6], w[7]);
-}
-
 // 8-bit scale number i of this GEMM's weights, as float.
 __device__ __forceinline__ float load_scale(const TcParams& p, int64_t i) {
   if (p.scale_kind == 1) return __half2float(static_cast<const __half*>(p.scale)[i]);
   if (p.scale_kind == 2) return __bfloat162float(static_cast<const __nv_bfloat16*>(p.scale)[i]);
   return static_cast<const float*>(p.scale)[i];
-}
-
-// Position of K index i inside its octet under the order [0,4,1,5,2,6,3,7]
-// (index c < 4 at 2c, index c + 4 at 2c + 1).
-__host__ __device__ __forceinline__ int permute_octet(int i) {
-  const int o = i & 7;
-  return (i & ~7) | (o < 4 ? 2 * o : 2 * (o - 4) + 1);
 }
 
 // 16-byte chunk c of a 128-byte swizzled shared-memory row.
@@ -334,23 +317,6 @@ __device__ __forceinline__ uint4 ld_chunk(const uint8_t* row, uint32_t c, uint32
 
 __device__ __forceinline__ uint4 sel4(bool p, const uint4& a, const uint4& b) {
   return make_uint4(p ? a.x : b.x, p ? a.y : b.y, p ? a.z : b.z, p ? a.w : b.w);
-}
-
-// uint4 -> f16, one 32-bit word w = 8 codes k0..k7 of one K octet (two per
-// byte, even index in the low nibble).  Word j of the result holds codes
-// (k_j, k_{j+4}): one mask places both under the f16 exponent of 1024, so
-// within every K octet the tensor-memory order is [0,4,1,5,2,6,3,7]; the
-// activations are laid out in the same order, which leaves the dot product
-// unchanged.  Each half becomes 1024 + q (exact); subtracting zz = 1024 + z
-// gives q - z exactly; multiplying by the f16 group scale ss rounds once.
-__device__ __forceinline__ void uint4x8_to_f16(uint32_t w, uint32_t zz, uint32_t ss, uint32_t* o) {
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint32_t v = ((w >> (4 * j)) & 0x000F000Fu) | 0x64006400u;
-    uint32_t d;
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(v), "r"(zz));
-    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[j]) : "r"(d), "r"(ss));
-  }
 }
 
 // Zero point and scale of one weight row at K position k (uint4), each
@@ -365,6 +331,385 @@ __device__ __forceinline__ void group_words(const TcParams& p, int wrow, int k, 
   }
   zz = (0x6400u | z) * 0x00010001u;
   ss = sb * 0x00010001u;
+}
+
+// --------------------------------------------------------------------------
+// Warp-MMA mode (SYNC): the converter warps multiply, the epilogue warps
+// finish.  Used for experts that hold a few token-slots (token tiles of 16
+// or 32 rows), where one tcgen05.mma per 2 KB of weights costs more issue
+// time than the weight stream leaves.
+//
+// Converter warp (group grp, quarter wq) owns 32 rows of the 128-row weight
+// tile: two m16 MMA tiles.  Lane (g, t) holds, for each of its 4 rows, the
+// 16-byte chunks t and t + 4 of each 128-byte weight-stage row (int8: K
+// [16t, 16t + 16) and [64 + 16t, ...); uint4: [32t, 32t + 32) and
+// [128 + 32t, ...)), and from the activation tile the same K range of token
+// row 8 tg + g.  MMA k-slice j takes codes [4j, 4j + 4) of a chunk as the
+// logical columns (2t, 2t+1, 2t+8, 2t+9), so A and B agree on the K behind
+// every column.  Fragment row g reads tile row rg = (g >> 1) | ((g & 1) << 2)
+// of its 8-row group: the two rows a quarter-warp reads differ by 4 in the
+// 128-byte swizzle phase, so the reads are free of bank conflicts.  In the
+// gate/up GEMM fragment rows 0-7 are gate rows i and rows 8-15 the up rows
+// i; the epilogue pairs them.
+// --------------------------------------------------------------------------
+// Not volatile: the MMA is a pure function of its registers, and the
+// compiler may then schedule the surrounding shared-memory loads and
+// conversions across it.
+template <bool BF16>
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  if constexpr (BF16)
+    asm(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  else
+    asm(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int j) {
+  return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
+}
+
+// Waits until the shared-memory loads that produced `v` have returned (an
+// instruction that reads the registers), so that the slot they came from can
+// be handed back to the TMA producer while the values are still being used.
+template <int N>
+__device__ __forceinline__ void consume(const uint4 (&v)[N]) {
+  uint32_t x = 0;
+#pragma unroll
+  for (int i = 0; i < N; ++i) x ^= v[i].x ^ v[i].y ^ v[i].z ^ v[i].w;
+  uint32_t sink;
+  asm volatile("mov.b32 %0, %1;" : "=r"(sink) : "r"(x));
+}
+
+// Row of the 128-row weight tile held by fragment row (tau, h) of lane
+// group g in converter quarter wq.
+template <int MODE>
+__device__ __forceinline__ int sync_tile_row(int wq, int tau, int h, int rg) {
+  return MODE == 1 ? (h ? 64 : 0) + 16 * wq + 8 * tau + rg : 32 * wq + 16 * tau + 8 * h + rg;
+}
+
+// Weight row (within the expert) of tile row br of weight tile mt.
+template <int MODE>
+__device__ __forceinline__ int sync_weight_row(const TcParams& p, int mt, int br) {
+  return MODE == 1 ? (br >= 64 ? p.I : 0) + mt * 64 + (br & 63) : mt * kTileM + br;
+}
+
+template <int MODE, int BITS, int BN, typename C>
+__device__ __forceinline__ void conv_sync(const TcParams& p, const int4* ulist, int total,
+                                          const uint8_t* sA, const uint8_t* sB, float* partials,
+                                          SharedCtl* ctl, int warp, int lane) {
+  constexpr int kEntryK = BITS == 8 ? 128 : 256;
+  constexpr int kGA = 256 / kEntryK;
+  constexpr int NAG = C::kAStagesSmem / kConvGroups;
+  constexpr int ND = C::kSteps;
+  constexpr int TG = BN / 8;                  // 8-token MMA groups
+  constexpr int kBox = BN * 128;              // bytes of one 64-K activation box
+  constexpr bool kBf16 = MODE == 2;           // down GEMM: bf16 act, bf16 weights
+  constexpr int PS = C::kPStride;
+  const int grp = (warp - kConvWarp0) >> 2;
+  const int wq = (warp - kConvWarp0) & 3;
+  const int g = lane >> 2;
+  const int t = lane & 3;
+  const int rg = (g >> 1) | ((g & 1) << 2);
+  int br[2][2];  // tile rows [tau][h]
+#pragma unroll
+  for (int tau = 0; tau < 2; ++tau)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) br[tau][h] = sync_tile_row<MODE>(wq, tau, h, rg);
+  const int rows_e = MODE == 1 ? 2 * p.I : p.H;
+  int lit = 0, st = 0;
+  bool ok = true;
+  for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
+    const Unit w = cta_unit<BN>(p, ulist, ui, u);
+    const int ks0 = w.split * p.ksteps / p.splits;
+    const int ks1 = (w.split + 1) * p.ksteps / p.splits;
+    // real token-slots of this tile (the rest of its rows are padding)
+    const int nreal = p.counts ? max(1, min(w.n, p.counts[w.e] - (w.row0 - p.offsets[w.e]))) : w.n;
+    const int ntg = min(TG, (nreal + 7) >> 3);
+    // 8-bit: 1024 + z (f16) or 2^23 + z (bf16) of this thread's rows
+    uint32_t zz8[2][2];
+    float zf8[2][2];
+    int64_t wrow[2][2];  // global weight rows
+#pragma unroll
+    for (int tau = 0; tau < 2; ++tau)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        wrow[tau][h] = (int64_t)w.e * rows_e + sync_weight_row<MODE>(p, w.mt, br[tau][h]);
+        uint32_t z = 128u;
+        if (BITS == 8 && p.zrow) z = p.zrow[wrow[tau][h]];
+        zz8[tau][h] = (0x6400u | z) * 0x00010001u;
+        zf8[tau][h] = 8388608.0f + (float)z;
+      }
+    // two accumulator sets (even / odd k-slices, 8-bit) so that an MMA rarely
+    // waits for the previous one on its accumulator; added at the unit end
+    constexpr int NS = (BITS == 8 && TG <= 2) ? 2 : 1;
+    float acc[NS][2][TG][4];
+#pragma unroll
+    for (int q = 0; q < NS; ++q)
+#pragma unroll
+      for (int a = 0; a < 2; ++a)
+#pragma unroll
+        for (int b = 0; b < TG; ++b)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) acc[q][a][b][r] = 0.0f;
+    for (int ks = ks0; ks < ks1; ks += kGA, ++st) {
+      const int nk = min(kGA, ks1 - ks);
+      if (st % kConvGroups != grp) continue;
+      const int d = st % ND;
+      // the step's activations (exact parity: slot d serves this group only,
+      // and this warp waited for its previous fill itself)
+      ok = warp_wait(&ctl->fullB[d], (st / ND) & 1, ctl, p.status, lane);
+      if (!ok) break;
+      const uint8_t* bstep = sB + d * C::kBBytes;
+      for (int j = 0; j < nk && ok; ++j, ++lit) {
+        const int sa = grp * NAG + lit % NAG;
+        // uint4: group scales and zero points of this stage's two K halves,
+        // loaded before the tile wait
+        float gsc[2][2][2];
+        uint32_t gzz[2][2][2];
+        if constexpr (BITS == 4) {
+          constexpr uint32_t kMagic = kBf16 ? 0x4300u : 0x6400u;
+#pragma unroll
+          for (int k2 = 0; k2 < 2; ++k2) {
+            // a K half past the row's end (K = 128 mod 256) has no group
+            const int gi = min(((ks + j) * kEntryK + 128 * k2) / p.gs, p.G - 1);
+#pragma unroll
+            for (int tau = 0; tau < 2; ++tau)
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const int64_t row = wrow[tau][h];
+                gsc[tau][h][k2] = __half2float(p.gscale[row * p.G + gi]);
+                uint32_t z = 8u;
+                if (p.has_zp) z = (p.gzero[(row >> 1) * p.G + gi] >> (4 * (int)(row & 1))) & 15u;
+                gzz[tau][h][k2] = (kMagic | z) * 0x00010001u;
+              }
+          }
+        }
+        ok = warp_wait(&ctl->fullA[sa], (lit / NAG) & 1, ctl, p.status, lane);
+        if (!ok) break;
+        const uint8_t* a = sA + sa * kABytes;
+        // this thread's 8 chunks of the stage into registers; the slot goes
+        // back to the producer as soon as every lane's loads have returned,
+        // so that the ring's slots are in flight to HBM rather than held
+        // through the conversion and the MMAs
+        uint4 pcl[8];  // [tau][h][k2] = pcl[4 tau + 2 h + k2]: chunks t and t + 4
+#pragma unroll
+        for (int tau = 0; tau < 2; ++tau)
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int k2 = 0; k2 < 2; ++k2)
+              pcl[4 * tau + 2 * h + k2] =
+                  ld_chunk(a + br[tau][h] * 128, (uint32_t)(t + 4 * k2), (uint32_t)rg);
+        consume(pcl);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->emptyA[sa]);
+        if constexpr (BITS == 8) {
+          uint4 pc[2][2][2];
+#pragma unroll
+          for (int tau = 0; tau < 2; ++tau)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int k2 = 0; k2 < 2; ++k2) pc[tau][h][k2] = pcl[4 * tau + 2 * h + k2];
+#pragma unroll
+          for (int k2 = 0; k2 < 2; ++k2) {
+            uint32_t lo[2][2][4], hi[2][2][4];  // [tau][h][jj]
+#pragma unroll
+            for (int tau = 0; tau < 2; ++tau)
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                  if constexpr (kBf16)
+                    int8x4_to_bf16x4(word_of(pc[tau][h][k2], jj), p.xmask, zf8[tau][h],
+                                     lo[tau][h][jj], hi[tau][h][jj]);
+                  else
+                    int8x4_to_f16x4(word_of(pc[tau][h][k2], jj), p.xmask, zz8[tau][h],
+                                    lo[tau][h][jj], hi[tau][h][jj]);
+                }
+            // activation box 2j + k2 (64 K), row 8 tg + g, chunks 2t and 2t + 1
+            const uint8_t* bb = bstep + (2 * j + k2) * kBox;
+#pragma unroll
+            for (int tg = 0; tg < TG; ++tg) {
+              if (tg >= ntg) break;
+              const int n = 8 * tg + g;
+              const uint4 b0 = ld_chunk(bb + n * 128, (uint32_t)(2 * t), (uint32_t)(n & 7));
+              const uint4 b1 = ld_chunk(bb + n * 128, (uint32_t)(2 * t + 1), (uint32_t)(n & 7));
+              const uint32_t bw[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+              // consecutive MMAs go to different accumulators: an MMA waits
+              // for the previous one on its accumulator
+#pragma unroll
+              for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+                for (int tau = 0; tau < 2; ++tau)
+                  mma16816<kBf16>(acc[(jj & 1) % NS][tau][tg], lo[tau][0][jj], lo[tau][1][jj],
+                                  hi[tau][0][jj], hi[tau][1][jj], bw[2 * jj], bw[2 * jj + 1]);
+            }
+          }
+        } else {
+          const int kdim = MODE == 1 ? p.H : p.I;
+#pragma unroll
+          for (int k2 = 0; k2 < 2; ++k2) {
+            if ((ks + j) * kEntryK + 128 * k2 >= kdim) break;  // half-filled last stage
+            uint4 pc[2][2];  // [tau][h]: chunk t + 4 k2 of the row
+#pragma unroll
+            for (int tau = 0; tau < 2; ++tau)
+#pragma unroll
+              for (int h = 0; h < 2; ++h) pc[tau][h] = pcl[4 * tau + 2 * h + k2];
+            // the group's partial sums, in two sets (one per octet of an
+            // octet pair) so that consecutive MMAs use different accumulators
+            float part[2][2][TG][4];
+#pragma unroll
+            for (int o2 = 0; o2 < 2; ++o2)
+#pragma unroll
+              for (int a2 = 0; a2 < 2; ++a2)
+#pragma unroll
+                for (int b2 = 0; b2 < TG; ++b2)
+#pragma unroll
+                  for (int r = 0; r < 4; ++r) part[o2][a2][b2][r] = 0.0f;
+            // two octet pairs of the 32-code chunk (16 K each)
+#pragma unroll
+            for (int op = 0; op < 2; ++op) {
+              // activations: K [32t + 128 k2, +32) in box 2 k2 + (t >> 1),
+              // chunks 4 (t & 1) + 2 op and + 1
+              const uint8_t* bb = bstep + (2 * k2 + (t >> 1)) * kBox;
+              uint32_t bw[TG][8];
+#pragma unroll
+              for (int tg = 0; tg < TG; ++tg) {
+                if (tg >= ntg) break;
+                const int n = 8 * tg + g;
+                const uint32_t c0 = (uint32_t)(4 * (t & 1) + 2 * op);
+                const uint4 b0 = ld_chunk(bb + n * 128, c0, (uint32_t)(n & 7));
+                const uint4 b1 = ld_chunk(bb + n * 128, c0 + 1, (uint32_t)(n & 7));
+                bw[tg][0] = b0.x; bw[tg][1] = b0.y; bw[tg][2] = b0.z; bw[tg][3] = b0.w;
+                bw[tg][4] = b1.x; bw[tg][5] = b1.y; bw[tg][6] = b1.z; bw[tg][7] = b1.w;
+              }
+#pragma unroll
+              for (int tau = 0; tau < 2; ++tau) {
+                uint32_t wv[2][2][4];  // [h][octet in pair][word]
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                  for (int oo = 0; oo < 2; ++oo)
+                    uint4x8_to_16<kBf16>(word_of(pc[tau][h], 2 * op + oo), gzz[tau][h][k2],
+                                         wv[h][oo]);
+#pragma unroll
+                for (int oo = 0; oo < 2; ++oo)
+#pragma unroll
+                  for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+                    for (int tg = 0; tg < TG; ++tg) {
+                      if (tg >= ntg) break;
+                      mma16816<kBf16>(part[oo][tau][tg], wv[0][oo][2 * jj], wv[1][oo][2 * jj],
+                                      wv[0][oo][2 * jj + 1], wv[1][oo][2 * jj + 1],
+                                      bw[tg][4 * oo + 2 * jj], bw[tg][4 * oo + 2 * jj + 1]);
+                    }
+              }
+            }
+#pragma unroll
+            for (int tau = 0; tau < 2; ++tau)
+#pragma unroll
+              for (int tg = 0; tg < TG; ++tg)
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+                  acc[0][tau][tg][r] = fmaf(gsc[tau][r >> 1][k2],
+                                            part[0][tau][tg][r] + part[1][tau][tg][r],
+                                            acc[0][tau][tg][r]);
+          }
+        }
+      }
+      if (!ok) break;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->stepfree[d]);  // activation slot d is free
+    }
+    if (!ok) break;
+    // hand this unit's partial sums to the epilogue (all 8 converter warps
+    // arrive, a group without steps in the unit with zeros)
+    const int buf = ui % C::kPBufs;
+    const uint32_t par = C::kPBufs == 2 ? (((ui >> 1) & 1) ^ 1) : ((ui & 1) ^ 1);
+    ok = warp_wait(&ctl->accempty[buf], par, ctl, p.status, lane);
+    if (!ok) break;
+    float* P = partials + (buf * kConvGroups + grp) * BN * PS;
+#pragma unroll
+    for (int tau = 0; tau < 2; ++tau)
+#pragma unroll
+      for (int tg = 0; tg < TG; ++tg)
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+          P[(8 * tg + 2 * t + (r & 1)) * PS + br[tau][r >> 1]] =
+              NS == 2 ? acc[0][tau][tg][r] + acc[NS - 1][tau][tg][r] : acc[0][tau][tg][r];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ctl->accfull[buf]);
+  }
+}
+
+template <int MODE, int BITS, int BN, typename C>
+__device__ __forceinline__ void epi_sync(const TcParams& p, const int4* ulist, int total,
+                                         const float* partials, SharedCtl* ctl, int warp,
+                                         int lane) {
+  constexpr int PS = C::kPStride;
+  const int e = (warp - kEpiWarp0) * 32 + lane;  // 0..127
+  mq::pdl_wait();
+  for (int u = blockIdx.x, t = 0; u < total; u += gridDim.x, ++t) {
+    const Unit w = cta_unit<BN>(p, ulist, t, u);
+    // per-column values (column = lane): MODE 1 the activation row scale
+    // (times the router weight when it applies to the input), MODE 2 the
+    // token-slot and its router weight; loaded before the wait
+    float colf = MODE == 1 ? 1.0f : 0.0f;
+    int colslot = p.S;
+    if (lane < w.n) {
+      if (MODE == 1) colf = p.xinv[w.row0 + lane];
+      if (MODE == 2 || p.rw_on_input) colslot = p.sorted[w.row0 + lane];
+    }
+    if (MODE == 1 && p.rw_on_input) colf *= colslot < p.S ? p.topk_w[colslot] : 0.0f;
+    if (MODE == 2 && colslot < p.S) colf = p.rw_on_input ? 1.0f : p.topk_w[colslot];
+    const int buf = t % C::kPBufs;
+    const uint32_t par = C::kPBufs == 2 ? ((t >> 1) & 1) : (t & 1);
+    float sc0 = 1.0f, sc1 = 1.0f;
+    int col_out = 0;
+    if (MODE == 1) {
+      const int i = e & 63;
+      const int64_t wr = (int64_t)w.e * 2 * p.I + w.mt * 64 + i;
+      if (BITS == 8) {
+        sc0 = load_scale(p, p.scale_per_tensor ? w.e : wr);
+        sc1 = load_scale(p, p.scale_per_tensor ? w.e : wr + p.I);
+      }
+      col_out = w.mt * 64 + (BITS == 8 ? i : permute_octet(i));
+    } else if (BITS == 8) {
+      sc0 = load_scale(p, p.scale_per_tensor ? w.e : (int64_t)w.e * p.H + w.mt * kTileM + e);
+    }
+    if (!warp_wait_sleepy(&ctl->accfull[buf], par, ctl, p.status, lane)) break;
+    const float* P0 = partials + (buf * kConvGroups) * BN * PS;
+    const float* P1 = P0 + BN * PS;
+    if (MODE == 1) {
+      // threads 0-63: even columns, 64-127: odd columns; pair i = e & 63
+      const int i = e & 63;
+      for (int c = e >> 6; c < w.n; c += 2) {
+        const float xs = __shfl_sync(0xffffffffu, colf, c);
+        const float gt = (P0[c * PS + i] + P1[c * PS + i]) * sc0 * xs;
+        const float up = (P0[c * PS + 64 + i] + P1[c * PS + 64 + i]) * sc1 * xs;
+        const float a = __fdividef(gt * up, 1.0f + __expf(-gt));  // silu(g) * up
+        p.act[(int64_t)(w.row0 + c) * p.I + col_out] = __float2bfloat16_rn(a);
+      }
+    } else {
+      float* yp = p.ypart + (int64_t)w.split * p.S * p.H + w.mt * kTileM + e;
+      for (int c = 0; c < w.n; ++c) {
+        const int sl = __shfl_sync(0xffffffffu, colslot, c);
+        const float f = __shfl_sync(0xffffffffu, colf, c);
+        if (sl < p.S) yp[(int64_t)sl * p.H] = (P0[c * PS + e] + P1[c * PS + e]) * sc0 * f;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ctl->accempty[buf]);
+  }
 }
 
 // f16 operands carry an exact power-of-two scale per activation row (xinv
@@ -384,11 +729,11 @@ __device__ __forceinline__ void group_words(const TcParams& p, int wrow, int k, 
 // converter group, each with its own count of weight stages (one sequential
 // consumer per slot); a converter waits for its step's activations only
 // after it has seen the MMAs of the slot's previous use complete.
-template <int MODE, int BITS, int BN>
-__global__ void __launch_bounds__(CfgOf<MODE, BITS, BN>::kThreads, 1)
+template <int MODE, int BITS, int BN, bool SYNC>
+__global__ void __launch_bounds__(CfgOf<MODE, BITS, BN, SYNC>::kThreads, 1)
     moe_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const TcParams p) {
-  using C = CfgOf<MODE, BITS, BN>;
+  using C = CfgOf<MODE, BITS, BN, SYNC>;
   // one weight stage = 128 rows x 128 bytes: 128 K of int8 or 256 K of uint4
   constexpr int kEntryK = BITS == 8 ? 128 : 256;
   constexpr int kGA = 256 / kEntryK;  // weight stages per MMA step (256 K)
@@ -405,7 +750,10 @@ __global__ void __launch_bounds__(CfgOf<MODE, BITS, BN>::kThreads, 1)
   // never read.  A compile-time descriptor keeps the issue loop short.
   // The 8-bit down GEMM reads act as written, in bf16 (weights converted to
   // bf16, exactly); every other GEMM runs f16 operands.
-  constexpr bool kBf16 = MODE == 2 && BITS == 8;
+  // In warp-MMA mode both down GEMMs read act as written (bf16); uint4
+  // weights enter as the exact q - z and their group scale multiplies each
+  // group's float32 partial sum.
+  constexpr bool kBf16 = MODE == 2 && (BITS == 8 || SYNC);
   constexpr uint32_t kIdesc = kBf16 ? idesc_bf16_f32(kTileM, BN) : idesc_f16_f32(kTileM, BN);
   static_assert(NA <= 16, "ring sizes");
 
@@ -414,7 +762,9 @@ __global__ void __launch_bounds__(CfgOf<MODE, BITS, BN>::kThreads, 1)
                                              ~uintptr_t(1023));
   uint8_t* sA = smem;                 // NA x 16 KB (int8 codes, 128-byte swizzle)
   uint8_t* sB = smem + NA * kABytes;  // ND x kG x 2 x BN x 128 B (16-bit, 128-byte swizzle)
-  SharedCtl* ctl = reinterpret_cast<SharedCtl*>(sB + ND * kBBytes);
+  float* partials = reinterpret_cast<float*>(sB + ND * kBBytes);  // warp-MMA mode only
+  constexpr int kPartBytes = partial_bytes<SYNC, BN>();
+  SharedCtl* ctl = reinterpret_cast<SharedCtl*>(sB + ND * kBBytes + kPartBytes);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -427,17 +777,19 @@ __global__ void __launch_bounds__(CfgOf<MODE, BITS, BN>::kThreads, 1)
     for (int s = 0; s < ND; ++s) {
       mbar_init(&ctl->fullB[s], 1);
       mbar_init(&ctl->afull[s], 4);
-      mbar_init(&ctl->stepfree[s], 1);  // MMA commit
+      // MMA commit; warp-MMA mode: the 4 warps of the step's converter group
+      mbar_init(&ctl->stepfree[s], SYNC ? 4 : 1);
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&ctl->accfull[s], C::kNI);  // one commit per issuer
+      // one commit per issuer; warp-MMA mode: all 8 converter warps
+      mbar_init(&ctl->accfull[s], SYNC ? 4 * kConvGroups : C::kNI);
       mbar_init(&ctl->accempty[s], 4);
     }
     mbar_init(&ctl->drain, C::kNI);
     ctl->abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 0) {
+  if (!SYNC && warp == 0) {
     tmem_alloc(&ctl->tmem_base, kTmemCols);
     tmem_relinquish();
   }
@@ -453,7 +805,7 @@ __global__ void __launch_bounds__(CfgOf<MODE, BITS, BN>::kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = ctl->tmem_base;
+  const uint32_t tmem = SYNC ? 0u : ctl->tmem_base;
   // The unit list (from the align kernel, two or more launches back) and the
   // weights do not depend on the previous kernel: the weight stream starts
   // at once.  The activations (and, in the epilogue, their row scales) come
@@ -540,6 +892,8 @@ __global__ void __launch_bounds__(CfgOf<MODE, BITS, BN>::kThreads, 1)
       }
     }
     __syncwarp();
+  } else if (SYNC && warp == 1) {
+    // warp-MMA mode: no MMA issuer
   } else if (warp == 1 || (C::kNI == 2 && warp == kIssuer2Warp)) {
     // ------------------------------------------------- MMA issuer ----
     // One thread runs this loop: it alone waits, issues and commits, so the
@@ -604,6 +958,10 @@ __global__ void __launch_bounds__(CfgOf<MODE, BITS, BN>::kThreads, 1)
       wait_drain(&ctl->drain, 0);
     }
     __syncwarp();
+  } else if (SYNC && warp < kEpiWarp0) {
+    if constexpr (SYNC) conv_sync<MODE, BITS, BN, C>(p, ulist, total, sA, sB, partials, ctl, warp, lane);
+  } else if (SYNC) {
+    if constexpr (SYNC) epi_sync<MODE, BITS, BN, C>(p, ulist, total, partials, ctl, warp, lane);
   } else if (warp < kEpiWarp0) {
     // -------------------------------------------------- converters ----
     // Per MMA step of this group: for each weight stage, wait for the tile
@@ -743,8 +1101,14 @@ __global__ void __launch_bounds__(CfgOf<MODE, BITS, BN>::kThreads, 1)
         colslot[i] = p.S;
         if (cc < w.n) {
           if (MODE == 1) colf[i] = p.xinv[w.row0 + cc];
-          else colslot[i] = p.sorted[w.row0 + cc];
+          if (MODE == 2 || p.rw_on_input) colslot[i] = p.sorted[w.row0 + cc];
         }
+      }
+      if (MODE == 1 && p.rw_on_input) {
+        // router weight on the input: W13 . (w x) = w (W13 . x), applied to
+        // the float32 accumulators with the row scale
+#pragma unroll
+        for (int i = 0; i < NP; ++i) colf[i] *= colslot[i] < p.S ? p.topk_w[colslot[i]] : 0.0f;
       }
       if (MODE == 2) {
 #pragma unroll
@@ -860,7 +1224,7 @@ __global__ void __launch_bounds__(CfgOf<MODE, BITS, BN>::kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (!SYNC && warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -887,14 +1251,12 @@ __device__ __forceinline__ void act8(const uint4& v, bool f16, float wmul, float
   }
 }
 
-// x is bf16, or f16 (act_f16); with rw (router weight on the input) each
-// slot's row is first multiplied by its router weight, in float32.
+// x is bf16, or f16 (act_f16).
 template <bool PERM>
 __global__ void __launch_bounds__(128) gather_rows_f16(const void* __restrict__ xv,
                                                        const int32_t* __restrict__ sorted,
                                                        const int32_t* __restrict__ num_padded,
                                                        int k, int S, int H, int act_f16,
-                                                       const float* __restrict__ rw,
                                                        __half* __restrict__ xs,
                                                        float* __restrict__ xinv) {
   __shared__ float wmax[4];
@@ -912,7 +1274,7 @@ __global__ void __launch_bounds__(128) gather_rows_f16(const void* __restrict__ 
   }
   const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(xv) + (int64_t)(s / k) * H);
   const bool f16 = act_f16 != 0;
-  const float wmul = rw ? rw[s] : 1.0f;
+  const float wmul = 1.0f;
   float m = 0.0f;
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
     float f[8];
@@ -1098,36 +1460,45 @@ cudaError_t make_map(CUtensorMap* map, CUtensorMapDataType dt, int rank, const v
 
 // At least 120 KB so that only one CTA fits on an SM: each CTA allocates all
 // 512 tensor-memory columns.
-template <int MODE, int BITS, int BN>
+template <int MODE, int BITS, int BN, bool SYNC>
 constexpr size_t smem_for() {
-  using C = CfgOf<MODE, BITS, BN>;
+  using C = CfgOf<MODE, BITS, BN, SYNC>;
+  const size_t part = (size_t)partial_bytes<SYNC, BN>();
   const size_t need = 1024 + (size_t)C::kAStagesSmem * kABytes + (size_t)C::kSteps * C::kBBytes +
-                      sizeof(SharedCtl) + kUnitList * sizeof(int4);
+                      part + sizeof(SharedCtl) + kUnitList * sizeof(int4);
   return need < 120 * 1024 ? 120 * 1024 : need;
 }
 
-template <int MODE, int BITS, int BN>
+template <int MODE, int BITS, int BN, bool SYNC>
 cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const TcParams& p,
                         int max_units, cudaStream_t st) {
-  constexpr size_t smem = smem_for<MODE, BITS, BN>();
-  auto kern = moe_gemm_tc<MODE, BITS, BN>;
+  constexpr size_t smem = smem_for<MODE, BITS, BN, SYNC>();
+  static_assert(smem <= 227 * 1024, "shared memory");
+  auto kern = moe_gemm_tc<MODE, BITS, BN, SYNC>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   const int sms = tc_num_sms();
   const int grid = max_units < sms ? max_units : sms;
   if (grid <= 0) return cudaSuccess;
-  err = launch_pdl(kern, dim3(grid), dim3(CfgOf<MODE, BITS, BN>::kThreads), smem, st, ta, tb, p);
+  err = launch_pdl(kern, dim3(grid), dim3(CfgOf<MODE, BITS, BN, SYNC>::kThreads), smem, st, ta,
+                   tb, p);
   return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 template <int MODE, int BITS>
-cudaError_t launch_gemm_bn(int bn, const CUtensorMap& ta, const CUtensorMap& tb,
+cudaError_t launch_gemm_bn(int bn, bool sync, const CUtensorMap& ta, const CUtensorMap& tb,
                            const TcParams& p, int max_units, cudaStream_t st) {
+  if (sync) {  // warp-MMA mode: 16-row tiles, and 32-row tiles for 8-bit codes
+    if (bn == 16) return launch_gemm<MODE, BITS, 16, true>(ta, tb, p, max_units, st);
+    if constexpr (BITS == 8)
+      if (bn == 32) return launch_gemm<MODE, BITS, 32, true>(ta, tb, p, max_units, st);
+    return cudaErrorInvalidValue;
+  }
   switch (bn) {
-    case 16: return launch_gemm<MODE, BITS, 16>(ta, tb, p, max_units, st);
-    case 32: return launch_gemm<MODE, BITS, 32>(ta, tb, p, max_units, st);
-    case 64: return launch_gemm<MODE, BITS, 64>(ta, tb, p, max_units, st);
-    case 128: return launch_gemm<MODE, BITS, 128>(ta, tb, p, max_units, st);
+    case 16: return launch_gemm<MODE, BITS, 16, false>(ta, tb, p, max_units, st);
+    case 32: return launch_gemm<MODE, BITS, 32, false>(ta, tb, p, max_units, st);
+    case 64: return launch_gemm<MODE, BITS, 64, false>(ta, tb, p, max_units, st);
+    case 128: return launch_gemm<MODE, BITS, 128, false>(ta, tb, p, max_units, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -1140,6 +1511,7 @@ inline int entries(int K, int bits) { return (K + entry_k(bits) - 1) / entry_k(b
 
 TcPlan tc_plan(int T, int H, int I, int E, int k, int bits) {
   TcPlan pl;
+  pl.sync1 = pl.sync2 = false;
   const int64_t S = (int64_t)T * k;
   // Token-slots per tile at most (the MMA's N).  A tile is cut from one
   // expert's segment with the rows it has, so a larger bound only costs
@@ -1179,9 +1551,7 @@ cudaError_t launch_gather_rows(const MoeArgs& a, void* xs, float* xinv, cudaStre
   const cudaError_t err = launch_pdl(
       a.bits == 8 ? gather_rows_f16<false> : gather_rows_f16<true>, dim3((unsigned)a.cap),
       dim3(128), 0, st, a.x, a.sorted, a.num_padded, a.k, a.T * a.k, a.H,
-      (a.flags & MQ_FWD_ACT_F16) ? 1 : 0,
-      (a.flags & MQ_FWD_ROUTER_WEIGHT_ON_INPUT) ? a.topk_w : (const float*)nullptr,
-      static_cast<__half*>(xs), xinv);
+      (a.flags & MQ_FWD_ACT_F16) ? 1 : 0, static_cast<__half*>(xs), xinv);
   return err != cudaSuccess ? err : cudaGetLastError();
 }
 
@@ -1191,6 +1561,7 @@ void common_params(TcParams& p, const MoeArgs& a) {
   p.H = a.H; p.I = a.I; p.E = a.E; p.k = a.k; p.S = a.T * a.k;
   p.sorted = a.sorted; p.offsets = a.offsets;
   p.chunk_expert = a.chunk_expert; p.chunk_start = a.chunk_start;
+  p.counts = a.counts;
   p.topk_w = a.topk_w;
   p.status = a.status;
   p.gs = a.bits == 8 ? 0 : a.group_size;
@@ -1252,8 +1623,8 @@ cudaError_t launch_gemm1_tc(const MoeArgs& a, const TcPlan& pl, const void* xs,
   p.xinv = xinv;
   const int64_t units = (a.cap / a.bm) * (int64_t)p.MT;  // token tiles <= 16-slot blocks
   const int mu = (int)(units < (1 << 30) ? units : (1 << 30));
-  return a.bits == 8 ? launch_gemm_bn<1, 8>(pl.bn, ta, tb, p, mu, st)
-                     : launch_gemm_bn<1, 4>(pl.bn, ta, tb, p, mu, st);
+  return a.bits == 8 ? launch_gemm_bn<1, 8>(pl.bn, pl.sync1, ta, tb, p, mu, st)
+                     : launch_gemm_bn<1, 4>(pl.bn, pl.sync1, ta, tb, p, mu, st);
 }
 
 cudaError_t launch_act_to_f16(const MoeArgs& a, float* act_inv, cudaStream_t st) {
@@ -1282,9 +1653,10 @@ cudaError_t launch_gemm2_tc(const MoeArgs& a, const TcPlan& pl, const float* act
     const cuuint64_t dims[2] = {(cuuint64_t)a.I, (cuuint64_t)a.cap};
     const cuuint64_t strides[1] = {(cuuint64_t)a.I * 2};
     const cuuint32_t box[2] = {64, (cuuint32_t)pl.bn};
-    // act: bf16 as written by the gate/up GEMM (8-bit), or f16 after the
-    // in-place conversion (uint4)
-    err = make_map(&tb, a.bits == 8 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+    // act: bf16 as written by the gate/up GEMM (8-bit, and uint4 in warp-MMA
+    // mode), or f16 after the in-place conversion (uint4, tensor cores)
+    err = make_map(&tb, (a.bits == 8 || pl.sync2) ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                    2, a.act, dims, strides, box,
                    CU_TENSOR_MAP_SWIZZLE_128B);
     if (err != cudaSuccess) return err;
@@ -1306,8 +1678,8 @@ cudaError_t launch_gemm2_tc(const MoeArgs& a, const TcPlan& pl, const float* act
   p.xinv = act_inv;
   const int64_t units = (a.cap / a.bm) * (int64_t)p.MT * p.splits;
   const int mu = (int)(units < (1 << 30) ? units : (1 << 30));
-  return a.bits == 8 ? launch_gemm_bn<2, 8>(pl.bn, ta, tb, p, mu, st)
-                     : launch_gemm_bn<2, 4>(pl.bn, ta, tb, p, mu, st);
+  return a.bits == 8 ? launch_gemm_bn<2, 8>(pl.bn, pl.sync2, ta, tb, p, mu, st)
+                     : launch_gemm_bn<2, 4>(pl.bn, pl.sync2, ta, tb, p, mu, st);
 }
 
 cudaError_t launch_combine_splits(const MoeArgs& a, const float* ypart, int splits,
@@ -1318,4 +1690,33 @@ cudaError_t launch_combine_splits(const MoeArgs& a, const float* ypart, int spli
       launch_pdl(combine_splits, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, ypart,
                  a.topk_ids, a.T, a.k, a.E, a.H, splits, (a.flags & MQ_FWD_ACT_F16) ? 1 : 0, a.out);
   return err != cudaSuccess ? err : cudaGetLastError();
+}
+
+bool dec_supported(int bits, int group_size, int H, int I) {
+  if (bits == 8) return true;
+  return bits == 4 && (group_size == 128 || group_size == 256) && H % 128 == 0 && I % 128 == 0;
+}
+
+int dec_splits(int T, int H, int I, int E, int k, int bits) {
+  // K splits of the warp-MMA down GEMM: the units (live experts x H / 128 x
+  // splits, one CTA per SM) should fill the SMs evenly, the last wave nearly
+  // full, with at least two MMA steps per split; fewer splits win near-ties
+  // (each adds partial sums to write and combine).
+  const int64_t S = (int64_t)T * k;
+  const int64_t live = S < E ? S : E;
+  const int steps = (I + 255) / 256;
+  const int sms = tc_num_sms();
+  int best = 1;
+  double best_eff = -1.0;
+  for (int sp = 1; sp <= 8; ++sp) {
+    if (sp > 1 && steps / sp < 2) break;
+    const int64_t units = live * (H / kTileM) * sp;
+    const double waves = (double)units / (double)sms;
+    const double eff = waves / std::ceil(waves) - (sp - 1) * 0.01;
+    if (eff > best_eff + 1e-9) {
+      best_eff = eff;
+      best = sp;
+    }
+  }
+  return best;
 }
