@@ -185,14 +185,16 @@ class ClockSampler:
 class Problem:
     """One layer's weights (quantised on the device) and one batch."""
 
-    def __init__(self, wl, T, seed, device="cuda", path="auto"):
+    def __init__(self, wl, T, seed, device="cuda", path="auto", weights=None):
         import weight_quantized_moe_gb300 as mq
         self.wl, self.T, self.seed, self.path = wl, T, seed, path
         E, H, I = wl.E, wl.H, wl.I
         self.x = synth.hidden_states(T, H, seed, device=device)
         self.logits = synth.router_logits(T, E, seed, bias=wl.bias, device=device)
-        self.w = {}
+        self.w = {} if weights is None else weights  # the same layer's weights, shared
         for which, (N, K) in (("w13", (2 * I, H)), ("w2", (H, I))):
+            if which in self.w:
+                continue
             bf = synth.expert_weights(E, N, K, seed, which, device=device)
             if wl.bits == 8:
                 self.w[which] = mq.moe_quantize_int8_per_channel(bf) + (None,)
@@ -309,6 +311,99 @@ def time_loop(fn, steps, warmup, world, finish=None):
     torch.cuda.synchronize()
     barrier(world)
     return a.elapsed_time(b)
+
+
+def time_steps_flushed(fn, steps, warmup, flush):
+    """Device time of `steps` calls of fn (ms), each preceded by a write of a
+    buffer larger than L2 outside the timed part (for layers whose touched
+    weights would otherwise stay resident in the 129 MB L2)."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    evs = []
+    for _ in range(steps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        fn()
+        b.record(st)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in evs)
+
+
+L2_BYTES = 129 * 2 ** 20
+
+
+def profile_kernels(fn, steps, world):
+    """{kernel slot: (total ms, launches)} of a separate pass of `steps`
+    calls, each kernel bracketed by events on its stream."""
+    import weight_quantized_moe_gb300 as mq
+    mq.mq_profile_enable(True)
+    time_loop(fn, steps, 2, world)
+    mq.mq_profile_enable(False)
+    return mq.mq_profile_read()
+
+
+def roofline_of(wl, T, prof, touched, peaks, long_run, traffic_key=None):
+    """Roofline of the dominant expert GEMM: algorithmic bytes (decode) or
+    flops (prefill) per launch over its mean launch time."""
+    work = algorithmic_work(wl, T, touched)
+    kern = max(("gemm1", "gemm2"), key=lambda k: prof.get(k, (0, 1))[0])
+    k_ms, k_n = prof[kern]
+    k_ms_launch = k_ms / max(k_n, 1)
+    wk = work[kern]
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if wk["flops"] / wk["bytes"] > ridge:
+        achieved = wk["flops"] / (k_ms_launch / 1e3) / 1e12
+        peak = peaks["bf16_tflops_sustained"] if long_run else peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak,
+                "peak_kind": "sustained" if long_run else "burst"}
+    else:
+        achieved = wk["bytes"] / (k_ms_launch / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"]}
+    roof.update({"kernel": kern,
+                 "traffic": ncu_traffic(kern, traffic_key) if traffic_key else None,
+                 "algorithmic_bytes_per_launch": wk["bytes"],
+                 "algorithmic_flops_per_launch": wk["flops"],
+                 "ms_per_launch": k_ms_launch,
+                 "peak_source": peaks["source"] + " (MEASURED_PEAKS.json)"
+                 if peaks["source"] == "measured" else "fallback",
+                 "kernel_ms_per_step": {k: v[0] / v[1] for k, v in prof.items()}})
+    return roof
+
+
+def measure_entry(wl, T, seed, steps, world, peaks, path, weights=None, flush=None):
+    """One extra workload of the line: whole-step tokens/s, the dominant
+    kernel's roofline, the step's HBM fraction and the routing's load."""
+    prob = Problem(wl, T, seed, path=path, weights=weights)
+    touched = prob.touched_experts()
+    bytes_touched = len(touched) * wl.bytes_per_expert()
+    use_flush = flush is not None and bytes_touched < 2 * L2_BYTES
+    if use_flush:
+        ms = time_steps_flushed(prob.step, steps, 3, flush)
+    else:
+        ms = time_loop(prob.step, steps, 3, world)
+    ms = max_over_ranks(ms, world)
+    prof = profile_kernels(prob.step, steps, world)
+    work = algorithmic_work(wl, T, touched)
+    step_bytes = work["gemm1"]["bytes"] + work["gemm2"]["bytes"]
+    ms_step = ms / steps
+    ent = {"workload": f"{wl.name} T={T}", "T": T,
+           "tokens_per_s": sum_over_ranks(T * steps, world) / (ms / 1e3),
+           "ms_per_step": ms_step,
+           "touched_experts": int(len(touched)),
+           "zero_token_experts": int(wl.E - len(touched)),
+           "hbm_frac_step": step_bytes / (ms_step / 1e3) / 1e9 / peaks["hbm_gbs"],
+           "tflops_step": wl.flops(T) / (ms_step / 1e3) / 1e12,
+           "roofline": roofline_of(wl, T, prof, touched, peaks, long_run=False),
+           "l2": "flushed between steps (touched weights < 2x L2)" if use_flush
+           else "touched weights larger than L2 stream from HBM every step"}
+    return ent, prob.w
 
 
 def kernel_source_sha():
@@ -472,35 +567,11 @@ def main():
 
     # per-kernel device times (separate pass of the same steps, events on the
     # launching stream)
-    mq.mq_profile_enable(True)
-    time_loop(prob.step, args.steps, 2, world)
-    mq.mq_profile_enable(False)
-    prof = mq.mq_profile_read()
+    prof = profile_kernels(prob.step, args.steps, world)
     touched = prob.touched_experts()
-    work = algorithmic_work(wl, T, touched)
-    kern = max(("gemm1", "gemm2"), key=lambda k: prof.get(k, (0, 1))[0])
-    k_ms, k_n = prof[kern]
-    k_ms_launch = k_ms / max(k_n, 1)
-    step_total = sum(v[0] for v in prof.values()) / max(args.steps + 2, 1)
-    wk = work[kern]
-    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    if wk["flops"] / wk["bytes"] > ridge:
-        achieved = wk["flops"] / (k_ms_launch / 1e3) / 1e12
-        long_run = ms_max > 1000.0
-        peak = peaks["bf16_tflops_sustained"] if long_run else peaks["bf16_tflops"]
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak}
-    else:
-        achieved = wk["bytes"] / (k_ms_launch / 1e3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"]}
-    roof.update({"kernel": kern, "traffic": ncu_traffic(kern, f"{wl.name}_T{T}"),
-                 "algorithmic_bytes_per_launch": wk["bytes"],
-                 "algorithmic_flops_per_launch": wk["flops"],
-                 "ms_per_launch": k_ms_launch, "peak_source": peaks["source"] + " (MEASURED_PEAKS.json)"
-                 if peaks["source"] == "measured" else "fallback",
-                 "touched_experts": int(len(touched)),
-                 "kernel_ms_per_step": {k: v[0] / v[1] for k, v in prof.items()}})
+    roof = roofline_of(wl, T, prof, touched, peaks, long_run=ms_max > 1000.0,
+                       traffic_key=f"{wl.name}_T{T}")
+    roof["touched_experts"] = int(len(touched))
 
     # end to end through the public API with host buffers
     e2e_run = EndToEnd(prob)
@@ -509,28 +580,50 @@ def main():
     e2e = {"value": tokens_all / (e2e_ms / 1e3), "unit": "tokens/s",
            "h2d_bytes_per_step": T * wl.H * 2 + T * wl.E * 4, "d2h_bytes_per_step": T * wl.H * 2}
 
+    # the rest of the metric: the decode sweep of the same layer, the
+    # prefill half (the same weights, routed with the prefill bias), and the
+    # fine-grained and W4A16 layers
+    steps_x = max(20, args.steps // 4)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
+    clocks_x = ClockSampler(torch.cuda.current_device()).start()
     sweep = []
     extra = []
     if args.sweep == "auto":
-        extra = [t for t in wl.Ts if t != T]
+        extra = [(wl, t) for t in wl.Ts if t != T]
+        if wl.name == "mixtral_decode":
+            extra += [(synth.WORKLOADS["fine"], 64), (synth.WORKLOADS["fine"], 512),
+                      (synth.WORKLOADS["w4a16"], 32)]
     elif args.sweep not in ("none", ""):
-        extra = [int(t) for t in args.sweep.split(",")]
-    for t in extra:
-        p2 = Problem(wl, t, args.seed + rank, path=args.path)
-        steps = max(20, args.steps // 4)
-        m2 = max_over_ranks(time_loop(p2.step, steps, 3, world), world)
-        sweep.append({"T": t, "tokens_per_s": sum_over_ranks(t * steps, world) / (m2 / 1e3),
-                      "ms_per_step": m2 / steps})
-        del p2
+        extra = [(wl, int(t)) for t in args.sweep.split(",")]
+    shared = {wl.name: prob.w}
+    for wl2, t in extra:
+        ent, w = measure_entry(wl2, t, args.seed + rank, steps_x, world, peaks, args.path,
+                               weights=shared.get(wl2.name), flush=flush)
+        shared[wl2.name] = w
+        sweep.append(ent)
+    prefill = None
+    if args.sweep == "auto" and wl.name == "mixtral_decode":
+        pwl = synth.WORKLOADS["mixtral_prefill"]
+        prefill, _ = measure_entry(pwl, 4096, args.seed + rank, steps_x, world, peaks, args.path,
+                                   weights=prob.w)
+    shared.clear()
+    del flush
+    clk_x = clocks_x.stop()
 
     line = {
         "metric": "W8A16 fused-MoE layer tokens/s" if wl.bits == 8 else "W4A16 fused-MoE layer tokens/s",
         "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": ("bf16 activations in/out; int8 weight codes dequantised exactly to f16 "
+                  "(gate/up, activations scaled exactly by a power of two per row) or bf16 "
+                  "(down); float32 accumulation") if wl.bits == 8 else
+                 ("bf16 activations in/out; uint4 codes with f16 group scales as f16 operands; "
+                  "float32 accumulation"),
         "data": "synthetic (seeded N(0,1) activations/logits, N(0,0.02) weights quantised on device)",
         "config": workload_config(wl, T), "roofline": roof, "e2e": e2e,
-        "gpu_launches": int(launches), "clocks": clk, "sweep": sweep,
+        "gpu_launches": int(launches), "clocks": clk, "sweep": sweep, "prefill": prefill,
+        "clocks_sweep": clk_x,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, T, args.seed)
