@@ -47,7 +47,7 @@ constexpr int kABytes = kTileM * kBK;     // int8 A tile per weight stage (16 KB
 constexpr int kConvGroups = 2;            // converter warpgroups (alternate MMA steps)
 constexpr int kConvWarp0 = 3;             // warps 0: A producer, 1: MMA, 2: B producer
 constexpr int kEpiWarp0 = kConvWarp0 + 4 * kConvGroups;  // first epilogue warp
-constexpr int kIssuer2Warp = kEpiWarp0 + 4;  // second MMA issuer (16-token tiles)
+constexpr int kIssuer2Warp = kEpiWarp0 + 4;  // second MMA issuer (16- and 32-token tiles)
 constexpr unsigned long long kWaitNs = 1000000000ull;
 constexpr int kRasterGroup = 8;           // weight tiles per raster group
 constexpr uint32_t kTmemCols = 512;
@@ -67,7 +67,7 @@ constexpr int kUnitList = 512;            // work units per CTA decoded once int
 //   one MMA commit per step frees both.
 // * One tcgen05.mma takes about 80 cycles to issue whatever N is, and the
 //   issuing thread's wait and commit around each 16-MMA step add about a
-//   third to that.  For 16-token tiles a second issuer thread takes
+//   third to that.  For 16- and 32-token tiles a second issuer thread takes
 //   every other step, so that one thread's wait and commit overlap the
 //   other's MMAs; each issuer accumulates its steps into its own half of the
 //   accumulator (kNI = 2 halves, added in a fixed order by the epilogue),
@@ -123,7 +123,7 @@ struct SyncCfg {
 
 template <int MODE, int BITS, int BN, bool SYNC>
 struct CfgSel {
-  using type = TileCfg<BN, (BN == 16 && !(MODE == 2 && BITS == 8)) ? 2 : 1>;
+  using type = TileCfg<BN, (BN <= 32 && !(MODE == 2 && BITS == 8)) ? 2 : 1>;
 };
 template <int MODE, int BITS, int BN>
 struct CfgSel<MODE, BITS, BN, true> {
@@ -1514,13 +1514,18 @@ TcPlan tc_plan(int T, int H, int I, int E, int k, int bits) {
   pl.sync1 = pl.sync2 = false;
   const int64_t S = (int64_t)T * k;
   // Token-slots per tile at most (the MMA's N).  A tile is cut from one
-  // expert's segment with the rows it has, so a larger bound only costs
-  // shared memory for the activation ring, while a smaller one streams an
-  // expert's weights once per tile.  Up to 32 tokens: 16 (with two MMA
-  // issuers, the fastest tile for small loads); up to 64 tokens: 64, which
-  // covers any expert even if it receives the whole batch (an expert gets at
-  // most one slot per token); beyond that, 128.
-  const int bn = T > 64 ? 128 : (T > 32 ? 64 : 16);
+  // expert's segment with the rows it has, so a larger bound costs shared
+  // memory for the activation ring (a shallower weight ring) and activation
+  // traffic, while a smaller one streams an expert's weights once per tile
+  // (the tiles of one expert run side by side, so the second pass mostly
+  // hits L2).  Up to 32 tokens: 16.  Up to 64 tokens: 32 for layers of a
+  // few large experts, whose loads are near-uniform (measured on the
+  // Mixtral-shaped layer, E=8, at T=64: gate/up 186.3 us with 64-row tiles,
+  // 178.3 us with 32-row tiles and two MMA issuers), 64 for layers of many
+  // small experts, where a few experts take most tokens (fine-grained E=128
+  // with Zipf routing at T=64: step 66.9 us with 64-row tiles, 69.2 us with
+  // 32-row ones).  Beyond 64 tokens, 128.
+  const int bn = T > 64 ? 128 : (T > 32 ? (E <= 16 ? 32 : 64) : 16);
   pl.bn = bn;
   // K splits of the down GEMM: enough work units (about 600, four per SM)
   // to keep every SM streaming weights; a fixed target keeps the workspace
