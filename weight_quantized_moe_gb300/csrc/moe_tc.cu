@@ -54,6 +54,11 @@ constexpr uint32_t kTmemCols = 512;
 constexpr int kSmemBudget = 212 * 1024;   // A ring + B ring
 constexpr int kMaxSteps = 4;              // MMA-step ring depth (max)
 constexpr int kUnitList = 512;            // work units per CTA decoded once into shared memory
+// uint4: a work unit's group scales ([128 tile rows][G] f16) and zero points
+// ([64 row pairs][G] bytes) are staged in shared memory, double-buffered
+// across units, when they fit a buffer of kStageBytes (G <= 25)
+constexpr int kStageBytes = 8192;
+inline bool stage_fits(int G) { return 128 * G * 2 + 64 * G <= kStageBytes; }
 
 // Pipeline shape per token-tile width BN.
 //
@@ -76,7 +81,7 @@ constexpr int kUnitList = 512;            // work units per CTA decoded once int
 //   more than the issuers need each other (measured on Mixtral shapes: the
 //   launch takes 104 us with one issuer and three stages, 118 us with two
 //   issuers and two).
-template <int BN, int NI>
+template <int BN, int NI, int SB = 0>
 struct TileCfg {
   static constexpr int kNI = NI;                // MMA issuer threads
   static constexpr int kACol0 = 2 * kNI * BN;   // two accumulator buffers of kNI halves
@@ -85,7 +90,7 @@ struct TileCfg {
   static constexpr int kThreads = (kEpiWarp0 + 4 + (kNI - 1)) * 32;
   static constexpr int kBBytesK = BN * kBK * 2;     // activations per weight stage
   static constexpr int kBBytes = kG * kBBytesK;     // activations per MMA step
-  static constexpr int kAFit = (kSmemBudget - kSteps * kBBytes) / kABytes;
+  static constexpr int kAFit = (kSmemBudget - SB - kSteps * kBBytes) / kABytes;
   static constexpr int kAStagesSmem = kAFit > 12 ? 12 : kAFit;
   static_assert(kACol0 + kSteps * kAColsPerStep <= (int)kTmemCols, "tensor memory budget");
   static_assert(kSteps >= 2, "MMA-step depth");
@@ -104,7 +109,7 @@ struct TileCfg {
 // buffers of [group][column][row] floats (row stride kPStride keeps the
 // converters' scattered stores and the epilogue's row reads free of bank
 // conflicts).
-template <int BN>
+template <int BN, int SB = 0>
 struct SyncCfg {
   static constexpr int kNI = 1;
   static constexpr int kThreads = (kEpiWarp0 + 4) * 32;
@@ -116,18 +121,20 @@ struct SyncCfg {
   static constexpr int kPStride = kTileM + 4;
   static constexpr int kPBytes = kConvGroups * BN * kPStride * 4;
   static constexpr int kPBufs = BN <= 16 ? 2 : 1;
-  static constexpr int kAFit = (kSmemBudget + 4096 - kSteps * kBBytes - kPBufs * kPBytes) / kABytes;
+  static constexpr int kAFit =
+      (kSmemBudget + 4096 - SB - kSteps * kBBytes - kPBufs * kPBytes) / kABytes;
   static constexpr int kAStagesSmem = (kAFit > 12 ? 12 : kAFit) & ~1;
   static_assert(kAStagesSmem >= 4, "weight ring depth");
 };
 
 template <int MODE, int BITS, int BN, bool SYNC>
 struct CfgSel {
-  using type = TileCfg<BN, (BN <= 32 && !(MODE == 2 && BITS == 8)) ? 2 : 1>;
+  using type = TileCfg<BN, (BN <= 32 && !(MODE == 2 && BITS == 8)) ? 2 : 1,
+                       BITS == 4 ? 2 * kStageBytes : 0>;
 };
 template <int MODE, int BITS, int BN>
 struct CfgSel<MODE, BITS, BN, true> {
-  using type = SyncCfg<BN>;
+  using type = SyncCfg<BN, BITS == 4 ? 2 * kStageBytes : 0>;
 };
 template <int MODE, int BITS, int BN, bool SYNC = false>
 using CfgOf = typename CfgSel<MODE, BITS, BN, SYNC>::type;
@@ -137,6 +144,12 @@ template <bool SYNC, int BN>
 constexpr int partial_bytes() {
   if constexpr (SYNC) return SyncCfg<BN>::kPBufs * SyncCfg<BN>::kPBytes;
   else return 0;
+}
+
+// Shared memory of the uint4 scale staging buffers.
+template <int BITS>
+constexpr int stage_bytes() {
+  return BITS == 4 ? 2 * kStageBytes : 0;
 }
 
 struct TcParams {
@@ -160,6 +173,8 @@ struct TcParams {
   int G;                  // uint4: groups per row (K / group_size)
   int gs;                 // uint4: group size
   int has_zp;             // uint4: 0 -> implicit zero 8
+  int stage;              // uint4: group scales / zeros staged in shared memory per unit
+  int gs_log2;            // uint4: log2(group size)
   const float* topk_w;
   __nv_bfloat16* act;     // gate/up output [cap, I]
   float* ypart;           // down output [splits, S, H]
@@ -235,6 +250,8 @@ struct alignas(16) SharedCtl {
   uint64_t stepfree[kMaxSteps];  // MMAs of the step done: TMEM A stage and B stage free
   uint64_t accfull[2];
   uint64_t accempty[2];
+  uint64_t fullS[2];    // uint4 staging: a unit's scales and zeros landed
+  uint64_t emptyS[2];   // uint4 staging: the 8 converter warps are done with them
   uint64_t drain;
   uint32_t tmem_base;
   volatile int abort_flag;
@@ -404,7 +421,7 @@ __device__ __forceinline__ int sync_weight_row(const TcParams& p, int mt, int br
 template <int MODE, int BITS, int BN, typename C>
 __device__ __forceinline__ void conv_sync(const TcParams& p, const int4* ulist, int total,
                                           const uint8_t* sA, const uint8_t* sB, float* partials,
-                                          SharedCtl* ctl, int warp, int lane) {
+                                          const uint8_t* sS, SharedCtl* ctl, int warp, int lane) {
   constexpr int kEntryK = BITS == 8 ? 128 : 256;
   constexpr int kGA = 256 / kEntryK;
   constexpr int NAG = C::kAStagesSmem / kConvGroups;
@@ -450,6 +467,13 @@ __device__ __forceinline__ void conv_sync(const TcParams& p, const int4* ulist, 
     // two accumulator sets (even / odd k-slices, 8-bit) so that an MMA rarely
     // waits for the previous one on its accumulator; added at the unit end
     constexpr int NS = (BITS == 8 && TG <= 2) ? 2 : 1;
+    // uint4: the unit's staged group scales (waited for by every converter
+    // warp on every unit, so that its parity waits stay exact)
+    const uint8_t* stg = sS + (ui & 1) * kStageBytes;
+    if (BITS == 4 && p.stage) {
+      ok = warp_wait(&ctl->fullS[ui & 1], (ui >> 1) & 1, ctl, p.status, lane);
+      if (!ok) break;
+    }
     float acc[NS][2][TG][4];
 #pragma unroll
     for (int q = 0; q < NS; ++q)
@@ -479,15 +503,22 @@ __device__ __forceinline__ void conv_sync(const TcParams& p, const int4* ulist, 
 #pragma unroll
           for (int k2 = 0; k2 < 2; ++k2) {
             // a K half past the row's end (K = 128 mod 256) has no group
-            const int gi = min(((ks + j) * kEntryK + 128 * k2) / p.gs, p.G - 1);
+            const int gi = min(((ks + j) * kEntryK + 128 * k2) >> p.gs_log2, p.G - 1);
 #pragma unroll
             for (int tau = 0; tau < 2; ++tau)
 #pragma unroll
               for (int h = 0; h < 2; ++h) {
                 const int64_t row = wrow[tau][h];
-                gsc[tau][h][k2] = __half2float(p.gscale[row * p.G + gi]);
                 uint32_t z = 8u;
-                if (p.has_zp) z = (p.gzero[(row >> 1) * p.G + gi] >> (4 * (int)(row & 1))) & 15u;
+                if (p.stage) {
+                  const int tr = br[tau][h];
+                  gsc[tau][h][k2] = __half2float(__ushort_as_half(
+                      reinterpret_cast<const uint16_t*>(stg)[tr * p.G + gi]));
+                  if (p.has_zp) z = (stg[256 * p.G + (tr >> 1) * p.G + gi] >> (4 * (tr & 1))) & 15u;
+                } else {
+                  gsc[tau][h][k2] = __half2float(p.gscale[row * p.G + gi]);
+                  if (p.has_zp) z = (p.gzero[(row >> 1) * p.G + gi] >> (4 * (int)(row & 1))) & 15u;
+                }
                 gzz[tau][h][k2] = (kMagic | z) * 0x00010001u;
               }
           }
@@ -631,6 +662,10 @@ __device__ __forceinline__ void conv_sync(const TcParams& p, const int4* ulist, 
       if (lane == 0) mbar_arrive(&ctl->stepfree[d]);  // activation slot d is free
     }
     if (!ok) break;
+    if (BITS == 4 && p.stage) {  // done with the unit's staged scales
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->emptyS[ui & 1]);
+    }
     // hand this unit's partial sums to the epilogue (all 8 converter warps
     // arrive, a group without steps in the unit with zeros)
     const int buf = ui % C::kPBufs;
@@ -784,6 +819,8 @@ __global__ void __launch_bounds__(CfgOf<MODE, BITS, BN, SYNC>::kThreads, 1)
       // one commit per issuer; warp-MMA mode: all 8 converter warps
       mbar_init(&ctl->accfull[s], SYNC ? 4 * kConvGroups : C::kNI);
       mbar_init(&ctl->accempty[s], 4);
+      mbar_init(&ctl->fullS[s], 1);
+      mbar_init(&ctl->emptyS[s], 4 * kConvGroups);
     }
     mbar_init(&ctl->drain, C::kNI);
     ctl->abort_flag = 0;
@@ -797,6 +834,7 @@ __global__ void __launch_bounds__(CfgOf<MODE, BITS, BN, SYNC>::kThreads, 1)
   // role waits on the schedule's global loads at a unit boundary.
   const int total = p.chunk_start[p.E] * p.MT * p.splits;
   int4* ulist = reinterpret_cast<int4*>(ctl + 1);
+  uint8_t* sS = reinterpret_cast<uint8_t*>(ulist + kUnitList);  // uint4 staging, 2 buffers
   for (int i = threadIdx.x; i < kUnitList; i += C::kThreads) {
     const int u = blockIdx.x + i * gridDim.x;
     if (u >= total) break;
@@ -820,10 +858,41 @@ __global__ void __launch_bounds__(CfgOf<MODE, BITS, BN, SYNC>::kThreads, 1)
     int st = 0;
     int lit0 = 0, lit1 = 0;  // weight stages issued into each group's half of the ring
     bool ok = true;
+    int nstaged = 0;  // units whose scales were staged
     for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
       const Unit w = cta_unit<BN>(p, ulist, ui, u);
       const int ks0 = w.split * p.ksteps / p.splits;
       const int ks1 = (w.split + 1) * p.ksteps / p.splits;
+      if (BITS == 4 && p.stage) {
+        // the unit's group scales (and zero points): one contiguous block per
+        // 64 (gate/up) or 128 (down) weight rows, 16-byte aligned because
+        // tiles start at multiples of 64 rows
+        const int b = ui & 1;
+        ok = warp_wait(&ctl->emptyS[b], ((ui >> 1) & 1) ^ 1, ctl, p.status, lane);
+        if (!ok) break;
+        if (lane == 0) {
+          uint8_t* dst = sS + b * kStageBytes;
+          const uint32_t sbytes = 128u * p.G * 2u;
+          const uint32_t zbytes = p.has_zp ? 64u * p.G : 0u;
+          mbar_arrive_expect_tx(&ctl->fullS[b], sbytes + zbytes);
+          if (MODE == 1) {
+            const int64_t r0 = (int64_t)w.e * 2 * p.I + w.mt * 64;  // gate rows; up rows + I
+            bulk_load(dst, p.gscale + r0 * p.G, sbytes / 2, &ctl->fullS[b]);
+            bulk_load(dst + sbytes / 2, p.gscale + (r0 + p.I) * p.G, sbytes / 2, &ctl->fullS[b]);
+            if (p.has_zp) {
+              bulk_load(dst + sbytes, p.gzero + (r0 >> 1) * p.G, zbytes / 2, &ctl->fullS[b]);
+              bulk_load(dst + sbytes + zbytes / 2, p.gzero + ((r0 + p.I) >> 1) * p.G, zbytes / 2,
+                        &ctl->fullS[b]);
+            }
+          } else {
+            const int64_t r0 = (int64_t)w.e * p.H + w.mt * kTileM;
+            bulk_load(dst, p.gscale + r0 * p.G, sbytes, &ctl->fullS[b]);
+            if (p.has_zp) bulk_load(dst + sbytes, p.gzero + (r0 >> 1) * p.G, zbytes, &ctl->fullS[b]);
+          }
+        }
+        __syncwarp();
+        ++nstaged;
+      }
       for (int ks = ks0; ks < ks1 && ok; ks += kGA, ++st) {
         const int g = st % kConvGroups;
         const int nk = min(kGA, ks1 - ks);
@@ -848,7 +917,7 @@ __global__ void __launch_bounds__(CfgOf<MODE, BITS, BN, SYNC>::kThreads, 1)
       }
     }
     // Never leave with copies in flight: wait for the last load issued into
-    // each slot of both halves.
+    // each slot of both halves, and for the last staged scales.
     if (lane == 0) {
       for (int g = 0; g < kConvGroups; ++g) {
         const int n = g ? lit1 : lit0;
@@ -856,6 +925,10 @@ __global__ void __launch_bounds__(CfgOf<MODE, BITS, BN, SYNC>::kThreads, 1)
           const int j = n - d;
           wait_drain(&ctl->fullA[g * NAG + j % NAG], (j / NAG) & 1);
         }
+      }
+      for (int d = 1; d <= (nstaged < 2 ? nstaged : 2); ++d) {
+        const int j = nstaged - d;
+        wait_drain(&ctl->fullS[j & 1], (j >> 1) & 1);
       }
     }
     __syncwarp();
@@ -959,7 +1032,8 @@ __global__ void __launch_bounds__(CfgOf<MODE, BITS, BN, SYNC>::kThreads, 1)
     }
     __syncwarp();
   } else if (SYNC && warp < kEpiWarp0) {
-    if constexpr (SYNC) conv_sync<MODE, BITS, BN, C>(p, ulist, total, sA, sB, partials, ctl, warp, lane);
+    if constexpr (SYNC)
+      conv_sync<MODE, BITS, BN, C>(p, ulist, total, sA, sB, partials, sS, ctl, warp, lane);
   } else if (SYNC) {
     if constexpr (SYNC) epi_sync<MODE, BITS, BN, C>(p, ulist, total, partials, ctl, warp, lane);
   } else if (warp < kEpiWarp0) {
@@ -997,6 +1071,17 @@ __global__ void __launch_bounds__(CfgOf<MODE, BITS, BN, SYNC>::kThreads, 1)
       // 8-bit: 1024 + zero point of this row (128 unless uint8 codes carry zeros)
       const uint32_t zz8 = (BITS == 8 && p.zrow) ? (0x6400u | p.zrow[wrow]) * 0x00010001u : 0x64806480u;
       const float zf8 = 8388608.0f + (float)((BITS == 8 && p.zrow) ? p.zrow[wrow] : 128u);
+      // uint4: the unit's staged group scales (every converter warp waits for
+      // every unit's buffer, so that its parity waits stay exact)
+      const uint8_t* stg = sS + (ui & 1) * kStageBytes;
+      // this row's staged scales and zero points (row srow of the tile)
+      const uint16_t* srow16 = reinterpret_cast<const uint16_t*>(stg) + srow * p.G;
+      const uint8_t* zrow8 = stg + 256 * p.G + (srow >> 1) * p.G;
+      const int zsh = 4 * (srow & 1);
+      if (BITS == 4 && p.stage) {
+        ok = warp_wait(&ctl->fullS[ui & 1], (ui >> 1) & 1, ctl, p.status, lane);
+        if (!ok) break;
+      }
       for (int ks = ks0; ks < ks1; ks += kGA, ++st) {
         const int nk = min(kGA, ks1 - ks);
         if (st % kConvGroups != grp) continue;
@@ -1005,8 +1090,32 @@ __global__ void __launch_bounds__(CfgOf<MODE, BITS, BN, SYNC>::kThreads, 1)
           const int sa = grp * NAG + lit % NAG;
           uint32_t zz[8], ss[8];  // uint4: per 32-K chunk, issued before the tile wait
           if constexpr (BITS == 4) {
+            if (p.stage) {
+              // chunk c of this 256-K stage lies in group g0 + (32 c >> log2 gs):
+              // one staged lookup per distinct group (gs is a power of two)
+              const int g0 = ((ks + j) * kEntryK) >> p.gs_log2;
+              const int csh = p.gs_log2 - 5;  // chunks per group = 2^csh
 #pragma unroll
-            for (int c = 0; c < 8; ++c) group_words(p, wrow, (ks + j) * kEntryK + 32 * c, zz[c], ss[c]);
+              for (int c = 0; c < 8; ++c) {
+                if ((c & ((1 << csh) - 1)) == 0) {
+                  const int g = g0 + (c >> csh);
+                  uint32_t z = 8, sb = 0;  // past the row's end: scale 0
+                  if (g < p.G) {
+                    sb = srow16[g];
+                    if (p.has_zp) z = (zrow8[g] >> zsh) & 15u;
+                  }
+                  zz[c] = (0x6400u | z) * 0x00010001u;
+                  ss[c] = sb * 0x00010001u;
+                } else {
+                  zz[c] = zz[c - 1];
+                  ss[c] = ss[c - 1];
+                }
+              }
+            } else {
+#pragma unroll
+              for (int c = 0; c < 8; ++c)
+                group_words(p, wrow, (ks + j) * kEntryK + 32 * c, zz[c], ss[c]);
+            }
           }
           ok = warp_wait(&ctl->fullA[sa], (lit / NAG) & 1, ctl, p.status, lane);
           if (!ok) break;
@@ -1065,6 +1174,11 @@ __global__ void __launch_bounds__(CfgOf<MODE, BITS, BN, SYNC>::kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctl->afull[d]);
+      }
+      if (!ok) break;
+      if (BITS == 4 && p.stage) {  // done with the unit's staged scales
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->emptyS[ui & 1]);
       }
     }
   } else {
@@ -1465,7 +1579,8 @@ constexpr size_t smem_for() {
   using C = CfgOf<MODE, BITS, BN, SYNC>;
   const size_t part = (size_t)partial_bytes<SYNC, BN>();
   const size_t need = 1024 + (size_t)C::kAStagesSmem * kABytes + (size_t)C::kSteps * C::kBBytes +
-                      part + sizeof(SharedCtl) + kUnitList * sizeof(int4);
+                      part + sizeof(SharedCtl) + kUnitList * sizeof(int4) +
+                      (size_t)stage_bytes<BITS>();
   return need < 120 * 1024 ? 120 * 1024 : need;
 }
 
@@ -1571,6 +1686,9 @@ void common_params(TcParams& p, const MoeArgs& a) {
   p.status = a.status;
   p.gs = a.bits == 8 ? 0 : a.group_size;
   p.has_zp = a.has_zp;
+  p.stage = 0;
+  p.gs_log2 = 0;
+  for (int g = p.gs; g > 1; g >>= 1) ++p.gs_log2;
   p.act = nullptr;
   p.ypart = nullptr;
   p.scale_kind = (a.flags & MQ_FWD_SCALE_F16) ? 1 : (a.flags & MQ_FWD_SCALE_BF16) ? 2 : 0;
@@ -1623,6 +1741,7 @@ cudaError_t launch_gemm1_tc(const MoeArgs& a, const TcPlan& pl, const void* xs,
     p.gscale = static_cast<const __half*>(a.s13);
     p.gzero = a.z13;
     p.G = a.H / a.group_size;
+    p.stage = stage_fits(p.G) ? 1 : 0;
   }
   p.act = a.act;
   p.xinv = xinv;
@@ -1678,6 +1797,7 @@ cudaError_t launch_gemm2_tc(const MoeArgs& a, const TcPlan& pl, const float* act
     p.gscale = static_cast<const __half*>(a.s2);
     p.gzero = a.z2;
     p.G = a.I / a.group_size;
+    p.stage = stage_fits(p.G) ? 1 : 0;
   }
   p.ypart = ypart;
   p.xinv = act_inv;
