@@ -1642,17 +1642,22 @@ TcPlan tc_plan(int T, int H, int I, int E, int k, int bits) {
   // 32-row ones).  Beyond 64 tokens, 128.
   const int bn = T > 64 ? 128 : (T > 32 ? (E <= 16 ? 32 : 64) : 16);
   pl.bn = bn;
-  // K splits of the down GEMM: enough work units (about 600, four per SM)
-  // to keep every SM streaming weights; a fixed target keeps the workspace
-  // size independent of the device.  A split keeps at least two MMA steps.
+  // K splits of the down GEMM.  Decode batches: the split count whose units
+  // (live experts x H / 128 x splits) fill the SMs most evenly (dec_splits;
+  // Mixtral-shaped T=1: 7 splits, 448 units, 2.95 waves, against 8 splits'
+  // 3.37 waves).  Larger batches: enough units (about 600, four per SM) to
+  // keep every SM streaming, each split keeping at least two MMA steps.
   const int64_t live = S < E ? S : E;
   const int64_t blocks = live > S / bn ? live : S / bn;
   const int mt2 = H / kTileM;
   const int steps2 = (I + 255) / 256;
   int splits = 1;
-  while (splits < 8 && blocks * mt2 * splits < 600 && steps2 / (splits * 2) >= 2) splits *= 2;
+  if (T <= 64) {
+    splits = dec_splits(T, H, I, E, k, bits);
+  } else {
+    while (splits < 8 && blocks * mt2 * splits < 600 && steps2 / (splits * 2) >= 2) splits *= 2;
+  }
   pl.splits = splits;
-  (void)bits;
   return pl;
 }
 
@@ -1823,10 +1828,15 @@ bool dec_supported(int bits, int group_size, int H, int I) {
 }
 
 int dec_splits(int T, int H, int I, int E, int k, int bits) {
-  // K splits of the warp-MMA down GEMM: the units (live experts x H / 128 x
-  // splits, one CTA per SM) should fill the SMs evenly, the last wave nearly
-  // full, with at least two MMA steps per split; fewer splits win near-ties
-  // (each adds partial sums to write and combine).
+  // K splits of the down GEMM at decode sizes: the split count whose units
+  // (live experts x H / 128 x splits) fill the SMs most evenly, the last
+  // wave nearly full; fewer splits win near-ties (each adds partial sums to
+  // write and combine), and a unit keeps at least 4 MMA steps (256 K each:
+  // shorter units spend more on hand-off and pipeline turn-around than the
+  // even waves save -- W4A16 E=64 at T=8, 6 steps: down 39 us unsplit, 53 us
+  // in two).  Mixtral-shaped T=1: 7 splits, 2.95 waves (down 38.9 -> 35.3 us
+  // against 8 splits' 3.37 waves).
+  (void)bits;
   const int64_t S = (int64_t)T * k;
   const int64_t live = S < E ? S : E;
   const int steps = (I + 255) / 256;
@@ -1834,7 +1844,7 @@ int dec_splits(int T, int H, int I, int E, int k, int bits) {
   int best = 1;
   double best_eff = -1.0;
   for (int sp = 1; sp <= 8; ++sp) {
-    if (sp > 1 && steps / sp < 2) break;
+    if (sp > 1 && steps / sp < 4) break;
     const int64_t units = live * (H / kTileM) * sp;
     const double waves = (double)units / (double)sms;
     const double eff = waves / std::ceil(waves) - (sp - 1) * 0.01;
