@@ -400,7 +400,8 @@ def measure_entry(wl, T, seed, steps, world, peaks, path, weights=None, flush=No
            "zero_token_experts": int(wl.E - len(touched)),
            "hbm_frac_step": step_bytes / (ms_step / 1e3) / 1e9 / peaks["hbm_gbs"],
            "tflops_step": wl.flops(T) / (ms_step / 1e3) / 1e12,
-           "roofline": roofline_of(wl, T, prof, touched, peaks, long_run=False),
+           "roofline": roofline_of(wl, T, prof, touched, peaks, long_run=False,
+                                   traffic_key=f"{wl.name}_T{T}"),
            "l2": "flushed between steps (touched weights < 2x L2)" if use_flush
            else "touched weights larger than L2 stream from HBM every step"}
     return ent, prob.w
