@@ -274,7 +274,8 @@ class EndToEnd:
 
 
 def algorithmic_work(wl, T, touched):
-    """Per-launch algorithmic bytes and flops of the two expert GEMMs."""
+    """Per-launch algorithmic bytes and flops of the two expert GEMMs (and
+    of the one-launch layer that runs both)."""
     S = T * wl.k
     n_touched = len(touched)
     H, I = wl.H, wl.I
@@ -285,10 +286,11 @@ def algorithmic_work(wl, T, touched):
         gs = wl.group_size
         w13 = I * H + 2 * 2 * I * (H // gs) + (I * (H // gs) if wl.has_zp else 0)
         w2 = H * I // 2 + 2 * H * (I // gs) + ((H // 2) * (I // gs) if wl.has_zp else 0)
-    return {
-        "gemm1": {"bytes": n_touched * w13 + T * H * 2 + S * I * 2, "flops": 4.0 * S * I * H},
-        "gemm2": {"bytes": n_touched * w2 + S * I * 2 + S * H * 4, "flops": 2.0 * S * I * H},
-    }
+    g1 = {"bytes": n_touched * w13 + T * H * 2 + S * I * 2, "flops": 4.0 * S * I * H}
+    g2 = {"bytes": n_touched * w2 + S * I * 2 + S * H * 4, "flops": 2.0 * S * I * H}
+    # the one-launch layer (8-bit, many experts) runs both GEMMs in one kernel
+    layer = {"bytes": g1["bytes"] + g2["bytes"], "flops": g1["flops"] + g2["flops"]}
+    return {"gemm1": g1, "gemm2": g2, "layer": layer}
 
 
 def time_loop(fn, steps, warmup, world, finish=None):
@@ -351,7 +353,7 @@ def roofline_of(wl, T, prof, touched, peaks, long_run, traffic_key=None):
     """Roofline of the dominant expert GEMM: algorithmic bytes (decode) or
     flops (prefill) per launch over its mean launch time."""
     work = algorithmic_work(wl, T, touched)
-    kern = max(("gemm1", "gemm2"), key=lambda k: prof.get(k, (0, 1))[0])
+    kern = max(("gemm1", "gemm2", "layer"), key=lambda k: prof.get(k, (0, 1))[0])
     k_ms, k_n = prof[kern]
     k_ms_launch = k_ms / max(k_n, 1)
     wk = work[kern]

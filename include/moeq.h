@@ -274,13 +274,24 @@ int moe_quant_forward(const void* x, int T, int H, int I, int E, int k,
  * By default the gate/up GEMM of 8-bit batches of up to 32 tokens takes the
  * warp-level MMAs and everything else tcgen05 (the faster choice measured
  * on GB300 for each GEMM and batch size).
- * MQ_FWD_PATH_TENSOR_CORE forces tcgen05 for both GEMMs, MQ_FWD_PATH_DECODE
- * the warp-level MMAs for both (MQ_ERR_UNSUPPORTED for uint4 with
- * group_size 32 or 64); at most one of the two.  Either fits the workspace
- * the query returns.
+ * For 8-bit layers of many small experts both GEMMs can run in one
+ * persistent launch on tcgen05 (token tiles of 64 or 128 rows): each SM
+ * streams its gate/up weight tiles and then its down weight tiles without a
+ * kernel boundary, and the down GEMM of a token tile starts as soon as all
+ * gate/up tiles of that token tile are done.  By default that launch serves
+ * 8-bit batches of 65 to 2048 tokens in layers of more than 16 experts.  It relies on all of its CTAs (one per SM, at most the
+ * SM count) becoming resident together, as they do unless kernels of other
+ * streams hold SMs for longer than a second; its waits on other CTAs give
+ * up after a second with MQ_DEV_WAIT_TIMEOUT.
+ * MQ_FWD_PATH_TENSOR_CORE forces tcgen05 for both GEMMs in two launches,
+ * MQ_FWD_PATH_DECODE the warp-level MMAs for both (MQ_ERR_UNSUPPORTED for
+ * uint4 with group_size 32 or 64), MQ_FWD_PATH_LAYER the one-launch layer
+ * (MQ_ERR_UNSUPPORTED for uint4); at most one of the three.  Each fits the
+ * workspace the query returns.
  */
 #define MQ_FWD_PATH_TENSOR_CORE 0x40u
 #define MQ_FWD_PATH_DECODE 0x80u
+#define MQ_FWD_PATH_LAYER 0x100u
 
 /*
  * moe_quant_forward_ex -- moe_quant_forward with option flags (above).
@@ -396,7 +407,8 @@ int moe_quant_forward_noalloc(const void* x, int T, int H, int I, int E, int k,
 #define MQ_PROF_COMBINE 5
 #define MQ_PROF_GATHER  6
 #define MQ_PROF_ACTF16  7
-#define MQ_PROF_SLOTS   8
+#define MQ_PROF_LAYER   8  /* both expert GEMMs in one launch (MQ_FWD_PATH_LAYER) */
+#define MQ_PROF_SLOTS   9
 
 long long mq_kernel_launch_count(void);
 int mq_profile_enable(int on);

@@ -80,6 +80,11 @@ def test_host_side_rejections(lib):
     assert ex(*args(8, -1, 1, None, binding.MQ_FWD_W8_UINT8)) == 1
     assert ex(*args(8, -1, 0, None, 0, out=vp(0x1100))) == 1
     assert ex(*args(8, -1, 0, None, binding.MQ_FWD_ACT_F16, out=fake, ws=16)) == 4
+    # kernel selection: at most one path flag; the one-launch layer takes 8-bit codes
+    assert ex(*args(8, -1, 0, None, binding.MQ_FWD_PATH_LAYER | binding.MQ_FWD_PATH_TENSOR_CORE)) == 1
+    assert ex(*args(8, -1, 0, None, binding.MQ_FWD_PATH_LAYER | binding.MQ_FWD_PATH_DECODE)) == 1
+    assert ex(*args(4, 128, 0, None, binding.MQ_FWD_PATH_LAYER)) == 2
+    assert ex(*args(8, -1, 0, None, binding.MQ_FWD_PATH_LAYER, ws=16)) == 4
     # moe_quant_forward_logits: null logits; workspace query includes routing
     assert lib.moe_quant_forward_logits(fake, None, 4, 128, 128, 8, 2, 1, 8, -1, 0, fake, fake,
                                         fake, fake, None, None, fake, 1 << 30, vp(0x9000), 0,

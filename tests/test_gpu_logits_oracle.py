@@ -12,7 +12,8 @@ of every sampled token is compared.  The sizes span the kernels' plans:
 the align kernel (small T·k·ceil(E/32)) and the separate router kernel
 (fine-grained T = 512), and the uint4 path at T = 1 -- each with the
 default consumers (warp-level MMAs in the 8-bit gate/up GEMM up to 32
-tokens, tcgen05 elsewhere) and with tcgen05 forced for both GEMMs.
+tokens, tcgen05 elsewhere), with tcgen05 forced for both GEMMs in two
+launches, and (8-bit) with both GEMMs forced into one launch.
 """
 
 import numpy as np
@@ -74,13 +75,13 @@ def mixtral():
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("path", ["auto", "tc"])
+@pytest.mark.parametrize("path", ["auto", "tc", "layer"])
 @pytest.mark.parametrize("T", [1, 8, 32, 64])
 def test_logits_forward_mixtral_decode(mixtral, T, path):
     _logits_case(mixtral, T, seed=20 + T, path=path)
 
 
-@pytest.mark.parametrize("path", ["auto", "tc"])
+@pytest.mark.parametrize("path", ["auto", "tc", "layer"])
 @pytest.mark.parametrize("T", [1, 64, 512])
 def test_logits_forward_fine_grained(T, path):
     layer = Layer(W["fine"], seed=0)

@@ -48,7 +48,7 @@ def _check(out, x, ex, tw, tid, intermediate="bf16", tol=FWD_TOL, **kw):
                   f"(plain max|err|/rms vs the exact oracle {plain_error(got, exact):.3e});")
 
 
-@pytest.mark.parametrize("path", ["decode", "tc"])
+@pytest.mark.parametrize("path", ["decode", "tc", "layer"])
 @pytest.mark.parametrize("shape", ["tiny", "mid"])
 @pytest.mark.parametrize("zp,sdt", [(False, torch.float32), (True, torch.float16),
                                     (False, torch.bfloat16), (True, torch.float32)])
@@ -70,7 +70,7 @@ def test_uint8_codes(shape, zp, sdt, path):
     _check(out, x, ex, tw, tid)
 
 
-@pytest.mark.parametrize("path", ["decode", "tc"])
+@pytest.mark.parametrize("path", ["decode", "tc", "layer"])
 @pytest.mark.parametrize("shape", ["tiny", "mid"])
 @pytest.mark.parametrize("sdt", [torch.float32, torch.bfloat16])
 def test_per_tensor_scale(shape, sdt, path):
@@ -99,7 +99,7 @@ def _int8_layer(E, H, I, seed):
     return ex, dev
 
 
-@pytest.mark.parametrize("path", ["decode", "tc"])
+@pytest.mark.parametrize("path", ["decode", "tc", "layer"])
 @pytest.mark.parametrize("shape", ["tiny", "mid"])
 def test_float16_activations(shape, path):
     E, k, H, I = SHAPES[shape]
@@ -111,7 +111,7 @@ def test_float16_activations(shape, path):
     _check(out, x16, ex, tw, tid)
 
 
-@pytest.mark.parametrize("path", ["decode", "tc"])
+@pytest.mark.parametrize("path", ["decode", "tc", "layer"])
 @pytest.mark.parametrize("shape", ["tiny", "mid"])
 @pytest.mark.parametrize("renorm", [True, False])
 def test_router_weight_on_input(shape, renorm, path):
@@ -135,7 +135,7 @@ def test_router_weight_on_input_w4a16(gs, path):
     _check(out, x, layer.oracle_experts(), tw, tid, apply_router_weight_on_input=True)
 
 
-@pytest.mark.parametrize("path", ["decode", "tc"])
+@pytest.mark.parametrize("path", ["decode", "tc", "layer"])
 @pytest.mark.parametrize("dt", [torch.bfloat16, torch.float16])
 def test_inplace_equals_out_of_place(dt, path):
     E, k, H, I = SHAPES["mid"]

@@ -31,6 +31,7 @@ from .binding import (  # noqa: F401
     MQ_FWD_ROUTER_WEIGHT_ON_INPUT,
     MQ_FWD_PATH_TENSOR_CORE,
     MQ_FWD_PATH_DECODE,
+    MQ_FWD_PATH_LAYER,
     MQ_SCORING_SOFTMAX,
     MQ_SCORING_SIGMOID,
     MqRouteOpts,

@@ -29,7 +29,9 @@ MQ_FWD_ACT_F16 = 0x10
 MQ_FWD_ROUTER_WEIGHT_ON_INPUT = 0x20
 MQ_FWD_PATH_TENSOR_CORE = 0x40
 MQ_FWD_PATH_DECODE = 0x80
-_PATH_FLAGS = {"auto": 0, "tc": MQ_FWD_PATH_TENSOR_CORE, "decode": MQ_FWD_PATH_DECODE}
+MQ_FWD_PATH_LAYER = 0x100
+_PATH_FLAGS = {"auto": 0, "tc": MQ_FWD_PATH_TENSOR_CORE, "decode": MQ_FWD_PATH_DECODE,
+               "layer": MQ_FWD_PATH_LAYER}
 # mq_route_opts.scoring_func
 MQ_SCORING_SOFTMAX = 0
 MQ_SCORING_SIGMOID = 1
@@ -76,7 +78,8 @@ _SIGNATURES = {
     "mq_profile_read": (_i32, [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_longlong), _i32]),
 }
 
-PROF_SLOTS = ("quant", "route", "align", "gemm1", "gemm2", "combine", "gather", "act_f16")
+PROF_SLOTS = ("quant", "route", "align", "gemm1", "gemm2", "combine", "gather", "act_f16",
+              "layer")
 
 _lib = None
 
@@ -274,10 +277,11 @@ def forward_flags(x, w13, s13, bits, apply_router_weight_on_input=False, path="a
     uint8 8-bit codes (moe_wna16), float16 / bfloat16 scales, one scale per
     expert (fewer scale elements than experts x output rows), float16
     activations; and the consumers of the expert GEMMs: path "auto" (by
-    GEMM and batch size), "tc" (tcgen05 for both) or "decode" (warp-level
-    MMAs for both)."""
+    GEMM and batch size), "tc" (tcgen05 for both, two launches), "decode"
+    (warp-level MMAs for both) or "layer" (both GEMMs in one tcgen05
+    launch, 8-bit codes)."""
     if path not in _PATH_FLAGS:
-        raise ValueError("path must be 'auto', 'tc' or 'decode'")
+        raise ValueError("path must be 'auto', 'tc', 'decode' or 'layer'")
     f = _PATH_FLAGS[path]
     if bits == 8:
         if w13.dtype == torch.uint8:

@@ -36,7 +36,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                  int32_t* __restrict__ block_expert, int32_t* __restrict__ offsets,
                  int32_t* __restrict__ num_padded, int chunk, int32_t* __restrict__ chunk_expert,
                  int32_t* __restrict__ chunk_start, int32_t* __restrict__ counts,
-                 const float* __restrict__ logits, int T, int k, int renorm,
+                 int32_t* __restrict__ dep, const float* __restrict__ logits, int T, int k, int renorm,
                  float* __restrict__ topk_w, unsigned* status) {
   extern __shared__ int smem[];
   int* hist = smem;                   // [kWarps][E]
@@ -148,6 +148,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (e < E) {
       chunk_start[e] = cstart;
       for (int c = 0; c < nch; ++c) chunk_expert[cstart + c] = e;
+      if (dep)
+        for (int c = 0; c < nch; ++c) dep[cstart + c] = 0;
     }
     if (tid == 0) chunk_start[E] = warp_tot2[kWarps - 1];
   }
@@ -184,8 +186,8 @@ template <int PER>
 cudaError_t launch_align_impl(int32_t* ids, int T, int k, int E, int bm, int32_t* sorted,
                               int32_t* block_expert, int32_t* offsets, int32_t* num_padded,
                               unsigned* status, cudaStream_t st, int chunk, int32_t* chunk_expert,
-                              int32_t* chunk_start, int32_t* counts, const float* logits,
-                              int renorm, float* topk_w) {
+                              int32_t* chunk_start, int32_t* counts, int32_t* dep,
+                              const float* logits, int renorm, float* topk_w) {
   size_t smem = (size_t)(kWarps * E + 2 * kWarps) * sizeof(int);
   if (PER > 0) smem += (size_t)kWarps * 32 * (sizeof(float) + sizeof(int));  // routing scratch
   auto kern = align_kernel<PER>;
@@ -197,7 +199,7 @@ cudaError_t launch_align_impl(int32_t* ids, int T, int k, int E, int bm, int32_t
   const cudaError_t err =
       launch_pdl(kern, dim3(1), dim3(kThreads), smem, st, ids, T * k, E, bm, sorted,
                  block_expert, offsets, num_padded, chunk, chunk_expert, chunk_start, counts,
-                 logits, T, k, renorm, topk_w, status);
+                 dep, logits, T, k, renorm, topk_w, status);
   return err != cudaSuccess ? err : cudaGetLastError();
 }
 
@@ -206,27 +208,28 @@ cudaError_t launch_align_impl(int32_t* ids, int T, int k, int E, int bm, int32_t
 cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int bm, int32_t* sorted,
                          int32_t* block_expert, int32_t* offsets, int32_t* num_padded,
                          unsigned* status, cudaStream_t st, int chunk, int32_t* chunk_expert,
-                         int32_t* chunk_start, int32_t* counts) {
+                         int32_t* chunk_start, int32_t* counts, int32_t* dep) {
   return launch_align_impl<0>(const_cast<int32_t*>(ids), T, k, E, bm, sorted, block_expert,
                               offsets, num_padded, status, st, chunk, chunk_expert, chunk_start,
-                              counts, nullptr, 0, nullptr);
+                              counts, dep, nullptr, 0, nullptr);
 }
 
 cudaError_t launch_route_align(const float* logits, int renorm, float* topk_w, int32_t* topk_ids,
                                int T, int k, int E, int bm, int32_t* sorted,
                                int32_t* block_expert, int32_t* offsets, int32_t* num_padded,
                                unsigned* status, cudaStream_t st, int chunk,
-                               int32_t* chunk_expert, int32_t* chunk_start, int32_t* counts) {
+                               int32_t* chunk_expert, int32_t* chunk_start, int32_t* counts,
+                               int32_t* dep) {
   if (!route_fused(T, k, E)) {
     const cudaError_t err = launch_route(logits, T, E, k, renorm, topk_w, topk_ids, st);
     if (err != cudaSuccess) return err;
     return launch_align(topk_ids, T, k, E, bm, sorted, block_expert, offsets, num_padded, status,
-                        st, chunk, chunk_expert, chunk_start, counts);
+                        st, chunk, chunk_expert, chunk_start, counts, dep);
   }
   const int per = (E + 31) / 32;
 #define MQ_RA(P)                                                                               \
   return launch_align_impl<P>(topk_ids, T, k, E, bm, sorted, block_expert, offsets, num_padded, \
-                              status, st, chunk, chunk_expert, chunk_start, counts, logits,      \
+                              status, st, chunk, chunk_expert, chunk_start, counts, dep, logits, \
                               renorm, topk_w);
   switch (per) {
     case 1: MQ_RA(1)

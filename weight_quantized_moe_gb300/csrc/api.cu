@@ -119,10 +119,24 @@ constexpr int kAlignBlock = 16;
 // conversion is cheap and few 8-token groups run.
 constexpr int kSyncGateUpMaxT = 32;
 
+// The one-launch layer by default where it measured faster than two
+// launches (fine-grained E=128, k=8, H=2048, I=768 with Zipf routing, step
+// with the L2 flushed: T=128 83.0 -> 77.2 us, T=512 132.4 -> 124.1 us): layers
+// of many small experts with 128-row token tiles, where each GEMM alone runs
+// few MMA steps per SM.  At T=64 (64-row tiles) both take 59-60 us, at
+// T=4096 both 574 us; Mixtral-shaped layers (E=8) lose with it (T=64: 291 ->
+// 305 us, as 64-row tiles replace the 32-row ones).
+bool layer_default(int T, int E) { return E > 16 && T > 64 && T <= 2048; }
+
 TcPlan fwd_plan(int T, int H, int I, int E, int k, int bits, int group_size, unsigned flags) {
   TcPlan pl = tc_plan(T, H, I, E, k, bits);
   const bool ok = dec_supported(bits, group_size, H, I);
   if (flags & MQ_FWD_PATH_TENSOR_CORE) return pl;
+  if (flags & MQ_FWD_PATH_LAYER) {  // 8-bit only (checked by the caller)
+    pl.layer = true;
+    if (pl.bn < 64) pl.bn = 64;
+    return pl;
+  }
   if (flags & MQ_FWD_PATH_DECODE) {
     if (!ok) return pl;
     pl.sync1 = pl.sync2 = true;
@@ -139,12 +153,14 @@ TcPlan fwd_plan(int T, int H, int I, int E, int k, int bits, int group_size, uns
   // uses 16-row tiles up to 32 tokens too, so both GEMMs share the chunk
   // table)
   if (ok && bits == 8 && T <= kSyncGateUpMaxT) pl.sync1 = true;
+  // one launch for both GEMMs of 8-bit layers of many experts (measured rule above)
+  if (bits == 8 && !pl.sync1 && pl.bn >= 64 && layer_default(T, E)) pl.layer = true;
   return pl;
 }
 
 struct WsLayout {
-  size_t sorted, block_expert, offsets, num_padded, chunk_expert, chunk_start, counts, xs, xinv,
-      act, act_inv, y, topk_w, topk_ids, total;
+  size_t sorted, block_expert, offsets, num_padded, chunk_expert, chunk_start, counts, dep, xs,
+      xinv, act, act_inv, y, topk_w, topk_ids, total;
   int64_t cap;
   TcPlan plan;
 };
@@ -171,6 +187,7 @@ WsLayout ws_layout(int T, int H, int I, int E, int k, int bits, int group_size,
   L.chunk_expert = off; off += align256(sizeof(int32_t) * (size_t)(cap / bm));
   L.chunk_start = off;  off += align256(sizeof(int32_t) * (size_t)(E + 1));
   L.counts = off;       off += align256(sizeof(int32_t) * (size_t)E);
+  L.dep = off;          off += align256(sizeof(int32_t) * (size_t)(cap / bm));
   L.xs = off;           off += align256(sizeof(__half) * (size_t)cap * (size_t)H);
   L.xinv = off;         off += align256(sizeof(float) * (size_t)cap);
   L.act = off;          off += align256(sizeof(__nv_bfloat16) * (size_t)cap * (size_t)I);
@@ -412,7 +429,8 @@ static int forward_impl(const void* x, int T, int H, int I, int E, int k, int bi
   constexpr unsigned kW8Flags = MQ_FWD_W8_UINT8 | MQ_FWD_SCALE_F16 | MQ_FWD_SCALE_BF16 |
                                 MQ_FWD_SCALE_PER_TENSOR;
   constexpr unsigned kAllFlags = kW8Flags | MQ_FWD_ACT_F16 | MQ_FWD_ROUTER_WEIGHT_ON_INPUT |
-                                 MQ_FWD_PATH_TENSOR_CORE | MQ_FWD_PATH_DECODE;
+                                 MQ_FWD_PATH_TENSOR_CORE | MQ_FWD_PATH_DECODE |
+                                 MQ_FWD_PATH_LAYER;
   if (T < 0 || H <= 0 || I <= 0 || E < 1) return fail(MQ_ERR_INVALID_ARG, "bad T, H, I or E");
   if (k < 1 || k > E || k > 32) return fail(MQ_ERR_INVALID_ARG, "need 1 <= k <= min(E, 32)");
   if (E > 1024) return fail(MQ_ERR_UNSUPPORTED, "E must be <= 1024");
@@ -421,8 +439,13 @@ static int forward_impl(const void* x, int T, int H, int I, int E, int k, int bi
     return fail(MQ_ERR_UNSUPPORTED, "uint8 codes and scale options apply to bits = 8 only");
   if ((flags & MQ_FWD_SCALE_F16) && (flags & MQ_FWD_SCALE_BF16))
     return fail(MQ_ERR_UNSUPPORTED, "scales are float16 or bfloat16, not both");
-  if ((flags & MQ_FWD_PATH_TENSOR_CORE) && (flags & MQ_FWD_PATH_DECODE))
-    return fail(MQ_ERR_INVALID_ARG, "MQ_FWD_PATH_TENSOR_CORE and MQ_FWD_PATH_DECODE exclude each other");
+  {
+    const unsigned paths = flags & (MQ_FWD_PATH_TENSOR_CORE | MQ_FWD_PATH_DECODE | MQ_FWD_PATH_LAYER);
+    if (paths & (paths - 1))
+      return fail(MQ_ERR_INVALID_ARG, "at most one of the MQ_FWD_PATH_* flags");
+  }
+  if ((flags & MQ_FWD_PATH_LAYER) && bits != 8)
+    return fail(MQ_ERR_UNSUPPORTED, "the one-launch layer takes 8-bit codes");
   if ((flags & MQ_FWD_PATH_DECODE) && !dec_supported(bits, group_size, H, I))
     return fail(MQ_ERR_UNSUPPORTED, "the warp-MMA consumers take 8-bit codes or uint4 with group_size 128 or 256");
   const bool w8zp = bits == 8 && group_size == -1 && has_zp == 1 && (flags & MQ_FWD_W8_UINT8);
@@ -482,6 +505,7 @@ static int forward_impl(const void* x, int T, int H, int I, int E, int k, int bi
   a.chunk_expert = reinterpret_cast<int32_t*>(ws + L.chunk_expert);
   a.chunk_start = reinterpret_cast<int32_t*>(ws + L.chunk_start);
   a.counts = reinterpret_cast<int32_t*>(ws + L.counts);
+  a.dep = reinterpret_cast<int32_t*>(ws + L.dep);
   a.act = reinterpret_cast<__nv_bfloat16*>(ws + L.act);
   a.y = reinterpret_cast<float*>(ws + L.y);
   a.bm = bm;
@@ -503,11 +527,11 @@ static int forward_impl(const void* x, int T, int H, int I, int E, int k, int bi
     if (fused)
       err = launch_route_align(logits, ro.renorm, rw, rid, T, k, E, bm, a.sorted, a.block_expert,
                                a.offsets, a.num_padded, a.status, st, chunk, a.chunk_expert,
-                               a.chunk_start, a.counts);
+                               a.chunk_start, a.counts, plan.layer ? a.dep : nullptr);
     else
       err = launch_align(topk_ids, T, k, E, bm, a.sorted, a.block_expert, a.offsets,
                          a.num_padded, a.status, st, chunk, a.chunk_expert, a.chunk_start,
-                         a.counts);
+                         a.counts, plan.layer ? a.dep : nullptr);
   }
   if (err != cudaSuccess) return cuda_fail(err, "forward: align launch");
   void* xs = ws + L.xs;
@@ -517,6 +541,17 @@ static int forward_impl(const void* x, int T, int H, int I, int E, int k, int bi
     err = launch_gather_rows(a, xs, xinv, st);
   }
   if (err != cudaSuccess) return cuda_fail(err, "forward: gather launch");
+  if (plan.layer) {
+    {
+      LaunchScope ls(MQ_PROF_LAYER, st);
+      err = launch_layer_tc(a, plan, xs, xinv, a.y, st);
+    }
+    if (err != cudaSuccess) return cuda_fail(err, "forward: expert layer launch");
+    LaunchScope ls(MQ_PROF_COMBINE, st);
+    err = launch_combine_splits(a, a.y, plan.splits, st);
+    if (err != cudaSuccess) return cuda_fail(err, "forward: combine launch");
+    return MQ_OK;
+  }
   {
     LaunchScope ls(MQ_PROF_GEMM1, st);
     err = launch_gemm1_tc(a, plan, xs, xinv, st);

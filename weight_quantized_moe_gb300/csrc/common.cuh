@@ -116,15 +116,18 @@ MQ_HIDDEN cudaError_t launch_route_align(const float* logits, int renorm, float*
                                          int32_t* sorted, int32_t* block_expert,
                                          int32_t* offsets, int32_t* num_padded, unsigned* status,
                                          cudaStream_t st, int chunk, int32_t* chunk_expert,
-                                         int32_t* chunk_start, int32_t* counts);
+                                         int32_t* chunk_start, int32_t* counts,
+                                         int32_t* dep = nullptr);
 // chunk > 0 also writes the chunk table of the expert GEMMs' token tiles
-// (chunk_expert [cap / bm], chunk_start [E + 1]); counts != null the number
-// of token-slots of each expert [E].
+// (chunk_expert [cap / bm], chunk_start [E + 1]) and, with dep != null,
+// zeroes each chunk's dependency counter of the fused layer kernel [cap / bm];
+// counts != null the number of token-slots of each expert [E].
 MQ_HIDDEN cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int bm,
                                    int32_t* sorted, int32_t* block_expert, int32_t* offsets,
                                    int32_t* num_padded, unsigned* status, cudaStream_t st,
                                    int chunk = 0, int32_t* chunk_expert = nullptr,
-                                   int32_t* chunk_start = nullptr, int32_t* counts = nullptr);
+                                   int32_t* chunk_start = nullptr, int32_t* counts = nullptr,
+                                   int32_t* dep = nullptr);
 
 struct MoeArgs {
   const void* x;          // bf16, or f16 with MQ_FWD_ACT_F16
@@ -149,6 +152,7 @@ struct MoeArgs {
   int32_t* chunk_expert;  // [cap / bm]: expert of each token tile (chunk)
   int32_t* chunk_start;   // [E + 1]: first chunk of each expert; [E] = number of chunks
   int32_t* counts;        // [E]: token-slots of each expert
+  int32_t* dep;           // [cap / bm]: fused layer, gate/up warps done per token tile
   __nv_bfloat16* act;     // [cap, I]
   float* y;               // [S, H]
   int bm;
@@ -161,6 +165,7 @@ struct TcPlan {
   int splits;  // K splits of the down GEMM
   bool sync1;  // gate/up GEMM: warp-MMA consumers (few tokens per expert), not tcgen05
   bool sync2;  // down GEMM: the same
+  bool layer;  // 8-bit, tcgen05: both GEMMs in one launch (moe_layer_tc)
 };
 MQ_HIDDEN TcPlan tc_plan(int T, int H, int I, int E, int k, int bits);
 MQ_HIDDEN int tc_num_sms();
@@ -172,6 +177,10 @@ MQ_HIDDEN cudaError_t launch_gemm2_tc(const MoeArgs& a, const TcPlan& pl, const 
                                       float* ypart, cudaStream_t st);
 MQ_HIDDEN cudaError_t launch_combine_splits(const MoeArgs& a, const float* ypart, int splits,
                                             cudaStream_t st);
+// Both expert GEMMs of an 8-bit layer in one launch (token tiles of 64 or 128
+// rows): act and the down GEMM's partial sums as the two launches write them.
+MQ_HIDDEN cudaError_t launch_layer_tc(const MoeArgs& a, const TcPlan& pl, const void* xs,
+                                      const float* xinv, float* ypart, cudaStream_t st);
 
 // Warp-MMA ("decode") mode of the expert GEMMs: the formats it takes, and
 // the K splits of its down GEMM.

@@ -32,6 +32,7 @@
 
 #include <cmath>
 #include <mutex>
+#include <type_traits>
 
 namespace {
 
@@ -179,6 +180,11 @@ struct TcParams {
   __nv_bfloat16* act;     // gate/up output [cap, I]
   float* ypart;           // down output [splits, S, H]
   const float* xinv;      // gate/up: per activation row, 1 / (its power-of-two scale)
+  // fused layer: per token tile, the count of gate/up epilogue warps done
+  // with its act columns (zeroed by the align kernel); the down GEMM waits
+  // for dep_target of them
+  int* dep;
+  int dep_target;
   unsigned* status;
 };
 
@@ -187,6 +193,7 @@ struct TcParams {
 // and K split.
 struct Unit {
   int e, row0, n, mt, split;
+  int ch;  // token tile (chunk) index
 };
 
 template <int N>
@@ -214,6 +221,7 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
   const int v = g * kRasterGroup + (r - bl * gsz);
   Unit out;
   out.e = e;
+  out.ch = cs + bl;
   out.row0 = p.offsets[e] + bl * BN;
   out.n = min(BN, p.offsets[e + 1] - out.row0);
   out.mt = v % p.MT;
@@ -222,21 +230,24 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
 }
 
 __device__ __forceinline__ int4 pack_unit(const Unit& w) {
-  return make_int4(w.e, w.row0, w.mt | (w.split << 20), w.n);
+  return make_int4(w.e, w.row0, w.mt | (w.split << 20), w.n | (w.ch << 8));
 }
 
-// Unit number i of this CTA (u = blockIdx.x + i * gridDim.x): from the list
-// decoded in the prologue, or decoded on the spot past its end.
+// Unit number i of this CTA (u = first unit + i * gridDim.x): from the list
+// decoded in the prologue (`len` entries), or decoded on the spot past its
+// end.
 template <int BN>
-__device__ __forceinline__ Unit cta_unit(const TcParams& p, const int4* ulist, int i, int u) {
-  if (i < kUnitList) {
+__device__ __forceinline__ Unit cta_unit(const TcParams& p, const int4* ulist, int i, int u,
+                                         int len = kUnitList) {
+  if (i < len) {
     const int4 v = ulist[i];
     Unit w;
     w.e = v.x;
     w.row0 = v.y;
     w.mt = v.z & 0xfffff;
     w.split = v.z >> 20;
-    w.n = v.w;
+    w.n = v.w & 255;
+    w.ch = v.w >> 8;
     return w;
   }
   return decode_unit<BN>(p, u);
@@ -307,6 +318,46 @@ __device__ __forceinline__ bool warp_wait_sleepy(uint64_t* bar, uint32_t parity,
       }
       __nanosleep(256);
     }
+  }
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// Fused layer, producer side: after this warp's act stores, make them
+// visible at GPU scope (and to the tensor-memory-access proxy that loads
+// them) before adding 1 to the token tile's counter.
+__device__ __forceinline__ void dep_signal(int* cnt, int lane) {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  __syncwarp();
+  if (lane == 0) {
+    __threadfence();
+    atomicAdd(cnt, 1);
+  }
+  __syncwarp();
+}
+
+// Fused layer, consumer side (warp-uniform): lane 0 polls the counter with
+// acquire loads until it reaches target, bounded like every other wait.
+__device__ __forceinline__ bool dep_wait(const int* cnt, int target, SharedCtl* ctl,
+                                         unsigned* status, int lane) {
+  int ok = 0;
+  if (lane == 0) {
+    const unsigned long long t0 = mq::global_timer_ns();
+    for (uint32_t n = 0;; ++n) {
+      int v;
+      asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
+      if (v >= target) {
+        ok = 1;
+        break;
+      }
+      if (ctl->abort_flag) break;
+      if ((n & 15u) == 15u && mq::global_timer_ns() - t0 > kWaitNs) {
+        ctl->abort_flag = 1;
+        mq::flag(status, MQ_DEV_WAIT_TIMEOUT);
+        break;
+      }
+      __nanosleep(64);
+    }
+    if (ok) asm volatile("fence.proxy.async.global;" ::: "memory");
   }
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
@@ -764,11 +815,29 @@ __device__ __forceinline__ void epi_sync(const TcParams& p, const int4* ulist, i
 // converter group, each with its own count of weight stages (one sequential
 // consumer per slot); a converter waits for its step's activations only
 // after it has seen the MMAs of the slot's previous use complete.
-template <int MODE, int BITS, int BN, bool SYNC>
-__global__ void __launch_bounds__(CfgOf<MODE, BITS, BN, SYNC>::kThreads, 1)
-    moe_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const TcParams p) {
+//
+// FUSED: the whole expert MLP of an 8-bit layer in one persistent launch.
+// Phase 1 is the gate/up GEMM (p, tmA, tmB), phase 2 the down GEMM (p2,
+// tmA2, tmB2) on the same rings and tensor memory; every role walks its
+// phase-1 units, then its phase-2 units, so the weight stream runs on
+// across the boundary.  A down unit's activation tile (act rows of one
+// token tile) is loaded only once all gate/up units of that tile have
+// stored their act columns: each of the 4 epilogue warps of a gate/up unit
+// adds 1 to the tile's counter (release), and the activation producer of a
+// down unit waits (acquire, bounded) until the counter reaches 4 x the
+// gate/up tiles per expert.  Phase 2 continues the round-robin over the
+// concatenated unit list, and every CTA finishes its gate/up units before
+// its down units: a down unit only waits for gate/up units, which wait for
+// nothing outside their CTA, so every wait ends once all CTAs are resident
+// (one CTA per SM, grid <= SMs).
+template <int MODE, int BITS, int BN, bool SYNC, bool FUSED>
+__device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                          const TcParams& p, const CUtensorMap& tmA2,
+                                          const CUtensorMap& tmB2, const TcParams& p2) {
   using C = CfgOf<MODE, BITS, BN, SYNC>;
+  static_assert(!FUSED || (MODE == 1 && BITS == 8 && !SYNC &&
+                           std::is_same<CfgOf<1, 8, BN>, CfgOf<2, 8, BN>>::value),
+                "fused layer: 8-bit, tensor-core consumers, one tile shape for both GEMMs");
   // one weight stage = 128 rows x 128 bytes: 128 K of int8 or 256 K of uint4
   constexpr int kEntryK = BITS == 8 ? 128 : 256;
   constexpr int kGA = 256 / kEntryK;  // weight stages per MMA step (256 K)
@@ -784,12 +853,11 @@ __global__ void __launch_bounds__(CfgOf<MODE, BITS, BN, SYNC>::kThreads, 1)
   // tiles (or are zero fill), and the accumulator columns they produce are
   // never read.  A compile-time descriptor keeps the issue loop short.
   // The 8-bit down GEMM reads act as written, in bf16 (weights converted to
-  // bf16, exactly); every other GEMM runs f16 operands.
+  // bf16, exactly); every other GEMM runs f16 operands (kBf16M, kIdescM per
+  // GEMM phase below).
   // In warp-MMA mode both down GEMMs read act as written (bf16); uint4
   // weights enter as the exact q - z and their group scale multiplies each
   // group's float32 partial sum.
-  constexpr bool kBf16 = MODE == 2 && (BITS == 8 || SYNC);
-  constexpr uint32_t kIdesc = kBf16 ? idesc_bf16_f32(kTileM, BN) : idesc_f16_f32(kTileM, BN);
   static_assert(NA <= 16, "ring sizes");
 
   extern __shared__ uint8_t smem_raw[];
@@ -804,6 +872,13 @@ __global__ void __launch_bounds__(CfgOf<MODE, BITS, BN, SYNC>::kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
+  // The first TMA of each map waits for its descriptor (a kernel parameter
+  // in global memory): start both fetches before the set-up below, so that
+  // they overlap it.
+  if (threadIdx.x == 32) tma_prefetch_desc(&tmA);
+  if (threadIdx.x == 64) tma_prefetch_desc(&tmB);
+  if (FUSED && threadIdx.x == 96) tma_prefetch_desc(&tmA2);
+  if (FUSED && threadIdx.x == 128) tma_prefetch_desc(&tmB2);
   if (threadIdx.x == 0) {
     for (int s = 0; s < NA; ++s) {
       mbar_init(&ctl->fullA[s], 1);
@@ -831,15 +906,34 @@ __global__ void __launch_bounds__(CfgOf<MODE, BITS, BN, SYNC>::kThreads, 1)
     tmem_relinquish();
   }
   // Decode this CTA's work units once, all threads in parallel, so that no
-  // role waits on the schedule's global loads at a unit boundary.
+  // role waits on the schedule's global loads at a unit boundary (the fused
+  // layer: half of the list for each GEMM).
+  constexpr int kUL = FUSED ? kUnitList / 2 : kUnitList;
   const int total = p.chunk_start[p.E] * p.MT * p.splits;
+  const int total2 = FUSED ? p2.chunk_start[p2.E] * p2.MT * p2.splits : 0;
+  // the fused layer's down units continue the round-robin after the gate/up
+  // units: unit u2 is item total + u2 of the concatenated list
+  const int u02 = FUSED ? (int)((blockIdx.x + gridDim.x - (unsigned)total % gridDim.x) % gridDim.x) : 0;
   int4* ulist = reinterpret_cast<int4*>(ctl + 1);
+  int4* ulist2 = ulist + kUL;
   uint8_t* sS = reinterpret_cast<uint8_t*>(ulist + kUnitList);  // uint4 staging, 2 buffers
-  for (int i = threadIdx.x; i < kUnitList; i += C::kThreads) {
+  for (int i = threadIdx.x; i < kUL; i += C::kThreads) {
     const int u = blockIdx.x + i * gridDim.x;
     if (u >= total) break;
     ulist[i] = pack_unit(decode_unit<BN>(p, u));
   }
+  if constexpr (FUSED)
+    for (int i = threadIdx.x; i < kUL; i += C::kThreads) {
+      const int u = u02 + i * gridDim.x;
+      if (u >= total2) break;
+      ulist2[i] = pack_unit(decode_unit<BN>(p2, u));
+    }
+  // Runs fn once per GEMM phase with that phase's parameters, tensor maps,
+  // unit list, unit count and this CTA's first unit.
+  auto phases = [&](auto&& fn) {
+    fn(IC<MODE>{}, p, tmA, tmB, static_cast<const int4*>(ulist), total, (int)blockIdx.x);
+    if constexpr (FUSED) fn(IC<2>{}, p2, tmA2, tmB2, static_cast<const int4*>(ulist2), total2, u02);
+  };
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -854,68 +948,71 @@ __global__ void __launch_bounds__(CfgOf<MODE, BITS, BN, SYNC>::kThreads, 1)
     // ------------------------------------------ A producer (int8 weights) ----
     // The whole warp walks the schedule (so it stays converged); lane 0
     // issues the copies.
-    if (lane == 0) tma_prefetch_desc(&tmA);
     int st = 0;
     int lit0 = 0, lit1 = 0;  // weight stages issued into each group's half of the ring
     bool ok = true;
     int nstaged = 0;  // units whose scales were staged
-    for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
-      const Unit w = cta_unit<BN>(p, ulist, ui, u);
-      const int ks0 = w.split * p.ksteps / p.splits;
-      const int ks1 = (w.split + 1) * p.ksteps / p.splits;
-      if (BITS == 4 && p.stage) {
-        // the unit's group scales (and zero points): one contiguous block per
-        // 64 (gate/up) or 128 (down) weight rows, 16-byte aligned because
-        // tiles start at multiples of 64 rows
-        const int b = ui & 1;
-        ok = warp_wait(&ctl->emptyS[b], ((ui >> 1) & 1) ^ 1, ctl, p.status, lane);
-        if (!ok) break;
-        if (lane == 0) {
-          uint8_t* dst = sS + b * kStageBytes;
-          const uint32_t sbytes = 128u * p.G * 2u;
-          const uint32_t zbytes = p.has_zp ? 64u * p.G : 0u;
-          mbar_arrive_expect_tx(&ctl->fullS[b], sbytes + zbytes);
-          if (MODE == 1) {
-            const int64_t r0 = (int64_t)w.e * 2 * p.I + w.mt * 64;  // gate rows; up rows + I
-            bulk_load(dst, p.gscale + r0 * p.G, sbytes / 2, &ctl->fullS[b]);
-            bulk_load(dst + sbytes / 2, p.gscale + (r0 + p.I) * p.G, sbytes / 2, &ctl->fullS[b]);
-            if (p.has_zp) {
-              bulk_load(dst + sbytes, p.gzero + (r0 >> 1) * p.G, zbytes / 2, &ctl->fullS[b]);
-              bulk_load(dst + sbytes + zbytes / 2, p.gzero + ((r0 + p.I) >> 1) * p.G, zbytes / 2,
-                        &ctl->fullS[b]);
-            }
-          } else {
-            const int64_t r0 = (int64_t)w.e * p.H + w.mt * kTileM;
-            bulk_load(dst, p.gscale + r0 * p.G, sbytes, &ctl->fullS[b]);
-            if (p.has_zp) bulk_load(dst + sbytes, p.gzero + (r0 >> 1) * p.G, zbytes, &ctl->fullS[b]);
-          }
-        }
-        __syncwarp();
-        ++nstaged;
-      }
-      for (int ks = ks0; ks < ks1 && ok; ks += kGA, ++st) {
-        const int g = st % kConvGroups;
-        const int nk = min(kGA, ks1 - ks);
-        for (int j = 0; j < nk; ++j) {
-          const int n = g ? lit1 : lit0;
-          const int s = g * NAG + n % NAG;
-          ok = warp_wait(&ctl->emptyA[s], ((n / NAG) & 1) ^ 1, ctl, p.status, lane);
+    phases([&](auto ph_tag, const TcParams& prm, const CUtensorMap& mA, const CUtensorMap& mB,
+               const int4* ul, int tot, int u0) {
+      constexpr int M = decltype(ph_tag)::value;
+      for (int u = u0, ui = 0; u < tot && ok; u += gridDim.x, ++ui) {
+        const Unit w = cta_unit<BN>(prm, ul, ui, u, kUL);
+        const int ks0 = w.split * prm.ksteps / prm.splits;
+        const int ks1 = (w.split + 1) * prm.ksteps / prm.splits;
+        if (BITS == 4 && prm.stage) {
+          // the unit's group scales (and zero points): one contiguous block per
+          // 64 (gate/up) or 128 (down) weight rows, 16-byte aligned because
+          // tiles start at multiples of 64 rows
+          const int b = ui & 1;
+          ok = warp_wait(&ctl->emptyS[b], ((ui >> 1) & 1) ^ 1, ctl, prm.status, lane);
           if (!ok) break;
           if (lane == 0) {
-            mbar_arrive_expect_tx(&ctl->fullA[s], kABytes);
-            uint8_t* a = sA + s * kABytes;
-            if (MODE == 1) {
-              // {K, row in half, gate/up half, expert}: 64 gate rows then 64 up rows
-              tma_load_4d(a, &tmA, &ctl->fullA[s], (ks + j) * 128, w.mt * 64, 0, w.e);
+            uint8_t* dst = sS + b * kStageBytes;
+            const uint32_t sbytes = 128u * prm.G * 2u;
+            const uint32_t zbytes = prm.has_zp ? 64u * prm.G : 0u;
+            mbar_arrive_expect_tx(&ctl->fullS[b], sbytes + zbytes);
+            if (M == 1) {
+              const int64_t r0 = (int64_t)w.e * 2 * prm.I + w.mt * 64;  // gate rows; up rows + I
+              bulk_load(dst, prm.gscale + r0 * prm.G, sbytes / 2, &ctl->fullS[b]);
+              bulk_load(dst + sbytes / 2, prm.gscale + (r0 + prm.I) * prm.G, sbytes / 2, &ctl->fullS[b]);
+              if (prm.has_zp) {
+                bulk_load(dst + sbytes, prm.gzero + (r0 >> 1) * prm.G, zbytes / 2, &ctl->fullS[b]);
+                bulk_load(dst + sbytes + zbytes / 2, prm.gzero + ((r0 + prm.I) >> 1) * prm.G, zbytes / 2,
+                          &ctl->fullS[b]);
+              }
             } else {
-              tma_load_2d(a, &tmA, &ctl->fullA[s], (ks + j) * 128, w.e * p.H + w.mt * kTileM);
+              const int64_t r0 = (int64_t)w.e * prm.H + w.mt * kTileM;
+              bulk_load(dst, prm.gscale + r0 * prm.G, sbytes, &ctl->fullS[b]);
+              if (prm.has_zp) bulk_load(dst + sbytes, prm.gzero + (r0 >> 1) * prm.G, zbytes, &ctl->fullS[b]);
             }
           }
           __syncwarp();
-          if (g) ++lit1; else ++lit0;
+          ++nstaged;
+        }
+        for (int ks = ks0; ks < ks1 && ok; ks += kGA, ++st) {
+          const int g = st % kConvGroups;
+          const int nk = min(kGA, ks1 - ks);
+          for (int j = 0; j < nk; ++j) {
+            const int n = g ? lit1 : lit0;
+            const int s = g * NAG + n % NAG;
+            ok = warp_wait(&ctl->emptyA[s], ((n / NAG) & 1) ^ 1, ctl, prm.status, lane);
+            if (!ok) break;
+            if (lane == 0) {
+              mbar_arrive_expect_tx(&ctl->fullA[s], kABytes);
+              uint8_t* a = sA + s * kABytes;
+              if (M == 1) {
+                // {K, row in half, gate/up half, expert}: 64 gate rows then 64 up rows
+                tma_load_4d(a, &mA, &ctl->fullA[s], (ks + j) * 128, w.mt * 64, 0, w.e);
+              } else {
+                tma_load_2d(a, &mA, &ctl->fullA[s], (ks + j) * 128, w.e * prm.H + w.mt * kTileM);
+              }
+            }
+            __syncwarp();
+            if (g) ++lit1; else ++lit0;
+          }
         }
       }
-    }
+    });
     // Never leave with copies in flight: wait for the last load issued into
     // each slot of both halves, and for the last staged scales.
     if (lane == 0) {
@@ -934,29 +1031,41 @@ __global__ void __launch_bounds__(CfgOf<MODE, BITS, BN, SYNC>::kThreads, 1)
     __syncwarp();
   } else if (warp == 2) {
     // ------------------------------------------ B producer (activations) ----
-    if (lane == 0) tma_prefetch_desc(&tmB);
     mq::pdl_wait();
     int st = 0;
     bool ok = true;
-    for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
-      const Unit w = cta_unit<BN>(p, ulist, ui, u);
-      const int ks0 = w.split * p.ksteps / p.splits;
-      const int ks1 = (w.split + 1) * p.ksteps / p.splits;
-      for (int ks = ks0; ks < ks1; ks += kGA, ++st) {
-        const int nboxes = min(kGA, ks1 - ks) * kEntryK / 64;  // 64-K activation boxes
-        const int d = st % ND;
-        ok = warp_wait(&ctl->stepfree[d], ((st / ND) & 1) ^ 1, ctl, p.status, lane);
-        if (!ok) break;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&ctl->fullB[d], nboxes * (kBBytesK / 2));
-          uint8_t* b = sB + d * kBBytes;
-          for (int j = 0; j < nboxes; ++j)  // past K the box reads the fill value 0
-            tma_load_2d(b + j * (kBBytesK / 2), &tmB, &ctl->fullB[d], ks * kEntryK + 64 * j,
-                        w.row0);
+    phases([&](auto ph_tag, const TcParams& prm, const CUtensorMap& mA, const CUtensorMap& mB,
+               const int4* ul, int tot, int u0) {
+      constexpr int M = decltype(ph_tag)::value;
+      int dep_ch = -1;  // fused layer: the last token tile whose gate/up outputs were waited for
+      for (int u = u0, ui = 0; u < tot && ok; u += gridDim.x, ++ui) {
+        const Unit w = cta_unit<BN>(prm, ul, ui, u, kUL);
+        const int ks0 = w.split * prm.ksteps / prm.splits;
+        const int ks1 = (w.split + 1) * prm.ksteps / prm.splits;
+        if constexpr (FUSED && M == 2) {
+          // the token tile's act rows: every gate/up unit of the tile is done
+          if (w.ch != dep_ch) {
+            ok = dep_wait(prm.dep + w.ch, prm.dep_target, ctl, prm.status, lane);
+            if (!ok) break;
+            dep_ch = w.ch;
+          }
         }
-        __syncwarp();
+        for (int ks = ks0; ks < ks1; ks += kGA, ++st) {
+          const int nboxes = min(kGA, ks1 - ks) * kEntryK / 64;  // 64-K activation boxes
+          const int d = st % ND;
+          ok = warp_wait(&ctl->stepfree[d], ((st / ND) & 1) ^ 1, ctl, prm.status, lane);
+          if (!ok) break;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&ctl->fullB[d], nboxes * (kBBytesK / 2));
+            uint8_t* b = sB + d * kBBytes;
+            for (int j = 0; j < nboxes; ++j)  // past K the box reads the fill value 0
+              tma_load_2d(b + j * (kBBytesK / 2), &mB, &ctl->fullB[d], ks * kEntryK + 64 * j,
+                          w.row0);
+          }
+          __syncwarp();
+        }
       }
-    }
+    });
     if (lane == 0) {
       const int n = st < ND ? st : ND;
       for (int dd = 1; dd <= n; ++dd) {
@@ -986,46 +1095,51 @@ __global__ void __launch_bounds__(CfgOf<MODE, BITS, BN, SYNC>::kThreads, 1)
       int d = 0;         // stage of step st (st % ND), advanced without a division
       uint32_t ph = 0;   // its barrier parity ((st / ND) & 1)
       bool ok = true;
-      for (int u = blockIdx.x; u < total && ok; u += gridDim.x, ++t) {
-        const Unit w = cta_unit<BN>(p, ulist, t, u);
-        const int ks0 = w.split * p.ksteps / p.splits;
-        const int ks1 = (w.split + 1) * p.ksteps / p.splits;
-        const int buf = t & 1;
-        ok = wait_bounded(&ctl->accempty[buf], ((t >> 1) & 1) ^ 1, ctl, p.status);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem + (buf * C::kNI + ip) * BN;
-        uint32_t acc = 0;  // the first step of this issuer in the unit overwrites
-        for (int ks = ks0; ks < ks1; ks += kGA, ++st) {
-          const int dc = d;
-          const uint32_t phc = ph;
-          if (++d == ND) {
-            d = 0;
-            ph ^= 1u;
-          }
-          if (C::kNI == 2 && (st & 1) != ip) continue;
-          const int nmma = min(kGA, ks1 - ks) * kEntryK / 16;  // K = 16 per MMA
-          ok = wait_bounded(&ctl->afull[dc], phc, ctl, p.status);
+      phases([&](auto ph_tag, const TcParams& prm, const CUtensorMap& mA, const CUtensorMap& mB,
+               const int4* ul, int tot, int u0) {
+        constexpr int M = decltype(ph_tag)::value;
+        constexpr uint32_t kIdescM = (M == 2 && (BITS == 8 || SYNC)) ? idesc_bf16_f32(kTileM, BN) : idesc_f16_f32(kTileM, BN);
+        for (int u = u0, ui = 0; u < tot && ok; u += gridDim.x, ++t, ++ui) {
+          const Unit w = cta_unit<BN>(prm, ul, ui, u, kUL);
+          const int ks0 = w.split * prm.ksteps / prm.splits;
+          const int ks1 = (w.split + 1) * prm.ksteps / prm.splits;
+          const int buf = t & 1;
+          ok = wait_bounded(&ctl->accempty[buf], ((t >> 1) & 1) ^ 1, ctl, prm.status);
           if (!ok) break;
           tc_fence_after();
-          // four K slices of 16 (32 bytes) per 64-K activation box
-          const uint64_t b_desc = b_desc0 + (uint64_t)(dc * kStageD);
-          const uint32_t a_tmem = tmem + kACol0 + dc * kAColsPerStep;
-          if (nmma == 16) {
-            mma_ts_x16<2, 4, 6, kBoxD, kBoxD + 2, kBoxD + 4, kBoxD + 6, 2 * kBoxD, 2 * kBoxD + 2,
-                       2 * kBoxD + 4, 2 * kBoxD + 6, 3 * kBoxD, 3 * kBoxD + 2, 3 * kBoxD + 4,
-                       3 * kBoxD + 6>(d_tmem, a_tmem, b_desc, kIdesc, acc);
-          } else {
-            for (int kk = 0; kk < nmma; ++kk)
-              mma_ts(d_tmem, a_tmem + kk * 8, b_desc + (uint64_t)((kk >> 2) * kBoxD + (kk & 3) * 2),
-                     kIdesc, kk > 0 ? 1u : acc);
+          const uint32_t d_tmem = tmem + (buf * C::kNI + ip) * BN;
+          uint32_t acc = 0;  // the first step of this issuer in the unit overwrites
+          for (int ks = ks0; ks < ks1; ks += kGA, ++st) {
+            const int dc = d;
+            const uint32_t phc = ph;
+            if (++d == ND) {
+              d = 0;
+              ph ^= 1u;
+            }
+            if (C::kNI == 2 && (st & 1) != ip) continue;
+            const int nmma = min(kGA, ks1 - ks) * kEntryK / 16;  // K = 16 per MMA
+            ok = wait_bounded(&ctl->afull[dc], phc, ctl, prm.status);
+            if (!ok) break;
+            tc_fence_after();
+            // four K slices of 16 (32 bytes) per 64-K activation box
+            const uint64_t b_desc = b_desc0 + (uint64_t)(dc * kStageD);
+            const uint32_t a_tmem = tmem + kACol0 + dc * kAColsPerStep;
+            if (nmma == 16) {
+              mma_ts_x16<2, 4, 6, kBoxD, kBoxD + 2, kBoxD + 4, kBoxD + 6, 2 * kBoxD, 2 * kBoxD + 2,
+                         2 * kBoxD + 4, 2 * kBoxD + 6, 3 * kBoxD, 3 * kBoxD + 2, 3 * kBoxD + 4,
+                         3 * kBoxD + 6>(d_tmem, a_tmem, b_desc, kIdescM, acc);
+            } else {
+              for (int kk = 0; kk < nmma; ++kk)
+                mma_ts(d_tmem, a_tmem + kk * 8, b_desc + (uint64_t)((kk >> 2) * kBoxD + (kk & 3) * 2),
+                       kIdescM, kk > 0 ? 1u : acc);
+            }
+            acc = 1;
+            mma_commit(&ctl->stepfree[dc]);
           }
-          acc = 1;
-          mma_commit(&ctl->stepfree[dc]);
+          if (!ok) break;
+          mma_commit(&ctl->accfull[buf]);
         }
-        if (!ok) break;
-        mma_commit(&ctl->accfull[buf]);
-      }
+      });
       // every MMA issued here must finish before tensor memory is freed
       mma_commit(&ctl->drain);
       wait_drain(&ctl->drain, 0);
@@ -1046,141 +1160,142 @@ __global__ void __launch_bounds__(CfgOf<MODE, BITS, BN, SYNC>::kThreads, 1)
     const int grp = (warp - kConvWarp0) >> 2;  // takes the steps with st % kConvGroups == grp
     const int q = warp & 3;                    // tensor-memory lane quarter of this warp
     const int r = q * 32 + lane;
-    int srow;
-    int rot = 0;
-    if (MODE == 1) {
-      // lanes (2i, 2i+1) hold gate row i and up row i of this tile
-      const int i = q * 16 + (lane >> 1);
-      srow = (lane & 1) ? 64 + i : i;
-      rot = (lane & 1) ? 4 : 0;  // rotated read order keeps the pair on distinct banks
-    } else {
-      srow = r;
-    }
-    const uint32_t sw = srow & 7;  // 128-byte swizzle phase of this row
     const uint32_t tcol = ((uint32_t)(q * 32) << 16) + kACol0;
-    const bool rt = rot != 0;
     int lit = 0, st = 0;  // lit: weight stages consumed by this group
     bool ok = true;
-    for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
-      const Unit w = cta_unit<BN>(p, ulist, ui, u);
-      const int ks0 = w.split * p.ksteps / p.splits;
-      const int ks1 = (w.split + 1) * p.ksteps / p.splits;
-      // this thread's weight row (uint4 group scales and zero points)
-      const int wrow = MODE == 1 ? w.e * 2 * p.I + ((lane & 1) ? p.I : 0) + w.mt * 64 + q * 16 + (lane >> 1)
-                                 : w.e * p.H + w.mt * kTileM + r;
-      // 8-bit: 1024 + zero point of this row (128 unless uint8 codes carry zeros)
-      const uint32_t zz8 = (BITS == 8 && p.zrow) ? (0x6400u | p.zrow[wrow]) * 0x00010001u : 0x64806480u;
-      const float zf8 = 8388608.0f + (float)((BITS == 8 && p.zrow) ? p.zrow[wrow] : 128u);
-      // uint4: the unit's staged group scales (every converter warp waits for
-      // every unit's buffer, so that its parity waits stay exact)
-      const uint8_t* stg = sS + (ui & 1) * kStageBytes;
-      // this row's staged scales and zero points (row srow of the tile)
-      const uint16_t* srow16 = reinterpret_cast<const uint16_t*>(stg) + srow * p.G;
-      const uint8_t* zrow8 = stg + 256 * p.G + (srow >> 1) * p.G;
-      const int zsh = 4 * (srow & 1);
-      if (BITS == 4 && p.stage) {
-        ok = warp_wait(&ctl->fullS[ui & 1], (ui >> 1) & 1, ctl, p.status, lane);
-        if (!ok) break;
-      }
-      for (int ks = ks0; ks < ks1; ks += kGA, ++st) {
-        const int nk = min(kGA, ks1 - ks);
-        if (st % kConvGroups != grp) continue;
-        const int d = st % ND;
-        for (int j = 0; j < nk && ok; ++j, ++lit) {
-          const int sa = grp * NAG + lit % NAG;
-          uint32_t zz[8], ss[8];  // uint4: per 32-K chunk, issued before the tile wait
-          if constexpr (BITS == 4) {
-            if (p.stage) {
-              // chunk c of this 256-K stage lies in group g0 + (32 c >> log2 gs):
-              // one staged lookup per distinct group (gs is a power of two)
-              const int g0 = ((ks + j) * kEntryK) >> p.gs_log2;
-              const int csh = p.gs_log2 - 5;  // chunks per group = 2^csh
+    phases([&](auto ph_tag, const TcParams& prm, const CUtensorMap& mA, const CUtensorMap& mB,
+               const int4* ul, int tot, int u0) {
+      constexpr int M = decltype(ph_tag)::value;
+      constexpr bool kBf16M = M == 2 && (BITS == 8 || SYNC);
+      // this thread's row of the weight tile: gate/up lanes (2i, 2i+1) hold
+      // gate row i and up row i (rotated read order keeps the pair on
+      // distinct banks); down: row r
+      const int i_gu = q * 16 + (lane >> 1);
+      const int srow = M == 1 ? ((lane & 1) ? 64 + i_gu : i_gu) : r;
+      const int rot = (M == 1 && (lane & 1)) ? 4 : 0;
+      const uint32_t sw = srow & 7;  // 128-byte swizzle phase of this row
+      const bool rt = rot != 0;
+      for (int u = u0, ui = 0; u < tot && ok; u += gridDim.x, ++ui) {
+        const Unit w = cta_unit<BN>(prm, ul, ui, u, kUL);
+        const int ks0 = w.split * prm.ksteps / prm.splits;
+        const int ks1 = (w.split + 1) * prm.ksteps / prm.splits;
+        // this thread's weight row (uint4 group scales and zero points)
+        const int wrow = M == 1 ? w.e * 2 * prm.I + ((lane & 1) ? prm.I : 0) + w.mt * 64 + q * 16 + (lane >> 1)
+                                   : w.e * prm.H + w.mt * kTileM + r;
+        // 8-bit: 1024 + zero point of this row (128 unless uint8 codes carry zeros)
+        const uint32_t zz8 = (BITS == 8 && prm.zrow) ? (0x6400u | prm.zrow[wrow]) * 0x00010001u : 0x64806480u;
+        const float zf8 = 8388608.0f + (float)((BITS == 8 && prm.zrow) ? prm.zrow[wrow] : 128u);
+        // uint4: the unit's staged group scales (every converter warp waits for
+        // every unit's buffer, so that its parity waits stay exact)
+        const uint8_t* stg = sS + (ui & 1) * kStageBytes;
+        // this row's staged scales and zero points (row srow of the tile)
+        const uint16_t* srow16 = reinterpret_cast<const uint16_t*>(stg) + srow * prm.G;
+        const uint8_t* zrow8 = stg + 256 * prm.G + (srow >> 1) * prm.G;
+        const int zsh = 4 * (srow & 1);
+        if (BITS == 4 && prm.stage) {
+          ok = warp_wait(&ctl->fullS[ui & 1], (ui >> 1) & 1, ctl, prm.status, lane);
+          if (!ok) break;
+        }
+        for (int ks = ks0; ks < ks1; ks += kGA, ++st) {
+          const int nk = min(kGA, ks1 - ks);
+          if (st % kConvGroups != grp) continue;
+          const int d = st % ND;
+          for (int j = 0; j < nk && ok; ++j, ++lit) {
+            const int sa = grp * NAG + lit % NAG;
+            uint32_t zz[8], ss[8];  // uint4: per 32-K chunk, issued before the tile wait
+            if constexpr (BITS == 4) {
+              if (prm.stage) {
+                // chunk c of this 256-K stage lies in group g0 + (32 c >> log2 gs):
+                // one staged lookup per distinct group (gs is a power of two)
+                const int g0 = ((ks + j) * kEntryK) >> prm.gs_log2;
+                const int csh = prm.gs_log2 - 5;  // chunks per group = 2^csh
 #pragma unroll
-              for (int c = 0; c < 8; ++c) {
-                if ((c & ((1 << csh) - 1)) == 0) {
-                  const int g = g0 + (c >> csh);
-                  uint32_t z = 8, sb = 0;  // past the row's end: scale 0
-                  if (g < p.G) {
-                    sb = srow16[g];
-                    if (p.has_zp) z = (zrow8[g] >> zsh) & 15u;
+                for (int c = 0; c < 8; ++c) {
+                  if ((c & ((1 << csh) - 1)) == 0) {
+                    const int g = g0 + (c >> csh);
+                    uint32_t z = 8, sb = 0;  // past the row's end: scale 0
+                    if (g < prm.G) {
+                      sb = srow16[g];
+                      if (prm.has_zp) z = (zrow8[g] >> zsh) & 15u;
+                    }
+                    zz[c] = (0x6400u | z) * 0x00010001u;
+                    ss[c] = sb * 0x00010001u;
+                  } else {
+                    zz[c] = zz[c - 1];
+                    ss[c] = ss[c - 1];
                   }
-                  zz[c] = (0x6400u | z) * 0x00010001u;
-                  ss[c] = sb * 0x00010001u;
-                } else {
-                  zz[c] = zz[c - 1];
-                  ss[c] = ss[c - 1];
                 }
+              } else {
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                  group_words(prm, wrow, (ks + j) * kEntryK + 32 * c, zz[c], ss[c]);
+              }
+            }
+            ok = warp_wait(&ctl->fullA[sa], (lit / NAG) & 1, ctl, prm.status, lane);
+            if (!ok) break;
+            const uint8_t* row = sA + sa * kABytes + srow * 128;
+            uint4 x[8];  // x[c] holds logical chunk (c + rot) & 7
+#pragma unroll
+            for (int c = 0; c < 8; ++c) x[c] = ld_chunk(row, (c + rot) & 7, sw);
+            if (j == 0) {
+              // the MMAs that last read this tensor-memory stage must be done
+              ok = warp_wait(&ctl->stepfree[d], ((st / ND) & 1) ^ 1, ctl, prm.status, lane);
+              if (!ok) break;
+              tc_fence_after();
+            }
+            const uint32_t tbase = tmem + tcol + d * kAColsPerStep + j * kEntryCols;
+            if constexpr (BITS == 8) {
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                uint32_t words[32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                  // logical chunk 4h + c sits in x[4h + c] (rot 0) or x[(4h + c + 4) & 7] (rot 4)
+                  const uint4 cv = sel4(rt, x[(4 * h + c + 4) & 7], x[4 * h + c]);
+                  if constexpr (kBf16M) convert16_bf16(cv, prm.xmask, zf8, &words[c * 8]);
+                  else convert16(cv, prm.xmask, zz8, &words[c * 8]);
+                }
+                tmem_st32(tbase + h * 32, words);
               }
             } else {
 #pragma unroll
-              for (int c = 0; c < 8; ++c)
-                group_words(p, wrow, (ks + j) * kEntryK + 32 * c, zz[c], ss[c]);
+              for (int h = 0; h < 4; ++h) {
+                uint32_t words[32];
+#pragma unroll
+                for (int c2 = 0; c2 < 2; ++c2) {
+                  const int c = 2 * h + c2;  // logical 16-byte chunk = 32 codes
+                  const uint4 v = sel4(rt, x[(c + 4) & 7], x[c]);
+                  uint4x8_to_f16(v.x, zz[c], ss[c], &words[c2 * 16 + 0]);
+                  uint4x8_to_f16(v.y, zz[c], ss[c], &words[c2 * 16 + 4]);
+                  uint4x8_to_f16(v.z, zz[c], ss[c], &words[c2 * 16 + 8]);
+                  uint4x8_to_f16(v.w, zz[c], ss[c], &words[c2 * 16 + 12]);
+                }
+                tmem_st32(tbase + h * 32, words);
+              }
             }
+            // The slot goes back only now that the loaded registers have been
+            // consumed: a shared-memory load that has issued may still be
+            // reading, and the next fill of the slot (TMA) would overtake it.
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->emptyA[sa]);
           }
-          ok = warp_wait(&ctl->fullA[sa], (lit / NAG) & 1, ctl, p.status, lane);
           if (!ok) break;
-          const uint8_t* row = sA + sa * kABytes + srow * 128;
-          uint4 x[8];  // x[c] holds logical chunk (c + rot) & 7
-#pragma unroll
-          for (int c = 0; c < 8; ++c) x[c] = ld_chunk(row, (c + rot) & 7, sw);
-          if (j == 0) {
-            // the MMAs that last read this tensor-memory stage must be done
-            ok = warp_wait(&ctl->stepfree[d], ((st / ND) & 1) ^ 1, ctl, p.status, lane);
-            if (!ok) break;
-            tc_fence_after();
-          }
-          const uint32_t tbase = tmem + tcol + d * kAColsPerStep + j * kEntryCols;
-          if constexpr (BITS == 8) {
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              uint32_t words[32];
-#pragma unroll
-              for (int c = 0; c < 4; ++c) {
-                // logical chunk 4h + c sits in x[4h + c] (rot 0) or x[(4h + c + 4) & 7] (rot 4)
-                const uint4 cv = sel4(rt, x[(4 * h + c + 4) & 7], x[4 * h + c]);
-                if constexpr (kBf16) convert16_bf16(cv, p.xmask, zf8, &words[c * 8]);
-                else convert16(cv, p.xmask, zz8, &words[c * 8]);
-              }
-              tmem_st32(tbase + h * 32, words);
-            }
-          } else {
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              uint32_t words[32];
-#pragma unroll
-              for (int c2 = 0; c2 < 2; ++c2) {
-                const int c = 2 * h + c2;  // logical 16-byte chunk = 32 codes
-                const uint4 v = sel4(rt, x[(c + 4) & 7], x[c]);
-                uint4x8_to_f16(v.x, zz[c], ss[c], &words[c2 * 16 + 0]);
-                uint4x8_to_f16(v.y, zz[c], ss[c], &words[c2 * 16 + 4]);
-                uint4x8_to_f16(v.z, zz[c], ss[c], &words[c2 * 16 + 8]);
-                uint4x8_to_f16(v.w, zz[c], ss[c], &words[c2 * 16 + 12]);
-              }
-              tmem_st32(tbase + h * 32, words);
-            }
-          }
-          // The slot goes back only now that the loaded registers have been
-          // consumed: a shared-memory load that has issued may still be
-          // reading, and the next fill of the slot (TMA) would overtake it.
+          // the step's activations (exact: the MMAs that read this slot's
+          // previous fill are done, so its barrier is at most this phase behind)
+          ok = warp_wait(&ctl->fullB[d], (st / ND) & 1, ctl, prm.status, lane);
+          if (!ok) break;
+          tmem_st_wait();
+          tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&ctl->emptyA[sa]);
+          if (lane == 0) mbar_arrive(&ctl->afull[d]);
         }
         if (!ok) break;
-        // the step's activations (exact: the MMAs that read this slot's
-        // previous fill are done, so its barrier is at most this phase behind)
-        ok = warp_wait(&ctl->fullB[d], (st / ND) & 1, ctl, p.status, lane);
-        if (!ok) break;
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl->afull[d]);
+        if (BITS == 4 && prm.stage) {  // done with the unit's staged scales
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl->emptyS[ui & 1]);
+        }
       }
-      if (!ok) break;
-      if (BITS == 4 && p.stage) {  // done with the unit's staged scales
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl->emptyS[ui & 1]);
-      }
-    }
+    });
   } else {
     // ---------------------------------------------------- epilogue ----
     const int q = warp & 3;
@@ -1191,149 +1306,167 @@ __global__ void __launch_bounds__(CfgOf<MODE, BITS, BN, SYNC>::kThreads, 1)
     mq::pdl_wait();
     int t = 0;
     int est = 0;  // schedule index of the unit's first MMA step
-    for (int u = blockIdx.x; u < total; u += gridDim.x, ++t) {
-      const Unit w = cta_unit<BN>(p, ulist, t, u);
-      const int buf = t & 1;
-      const int nsteps = ((w.split + 1) * p.ksteps / p.splits - w.split * p.ksteps / p.splits + kGA - 1) / kGA;
-      // two issuers: both halves hold partial sums when the unit has two or
-      // more steps; with one step only half (first step % 2) was written
-      const bool both = C::kNI == 2 && nsteps >= 2;
-      const int half0 = (C::kNI == 2 && !both) ? (est & 1) : 0;
-      est += nsteps;
-      // Per-column values of the tile, loaded while its MMAs still run (a
-      // unit of a few MMA steps would otherwise wait on these dependent
-      // loads): column i * 32 + lane in element i.  MODE 1: the activation
-      // row scale; MODE 2: the token-slot (S for padding) and its factor
-      // (activation row scale x router weight).
-      constexpr int NP = (BN + 31) / 32;
-      float colf[NP];
-      int colslot[NP];
+    bool ok = true;
+    phases([&](auto ph_tag, const TcParams& prm, const CUtensorMap& mA, const CUtensorMap& mB,
+               const int4* ul, int tot, int u0) {
+      constexpr int M = decltype(ph_tag)::value;
+      constexpr bool kBf16M = M == 2 && (BITS == 8 || SYNC);
+      for (int u = u0, ui = 0; u < tot && ok; u += gridDim.x, ++t, ++ui) {
+        const Unit w = cta_unit<BN>(prm, ul, ui, u, kUL);
+        const int buf = t & 1;
+        const int nsteps = ((w.split + 1) * prm.ksteps / prm.splits - w.split * prm.ksteps / prm.splits + kGA - 1) / kGA;
+        // two issuers: both halves hold partial sums when the unit has two or
+        // more steps; with one step only half (first step % 2) was written
+        const bool both = C::kNI == 2 && nsteps >= 2;
+        const int half0 = (C::kNI == 2 && !both) ? (est & 1) : 0;
+        est += nsteps;
+        // Per-column values of the tile, loaded while its MMAs still run (a
+        // unit of a few MMA steps would otherwise wait on these dependent
+        // loads): column i * 32 + lane in element i.  M 1: the activation
+        // row scale; M 2: the token-slot (S for padding) and its factor
+        // (activation row scale x router weight).
+        constexpr int NP = (BN + 31) / 32;
+        float colf[NP];
+        int colslot[NP];
 #pragma unroll
-      for (int i = 0; i < NP; ++i) {
-        const int cc = i * 32 + lane;
-        colf[i] = MODE == 1 ? 1.0f : 0.0f;
-        colslot[i] = p.S;
-        if (cc < w.n) {
-          if (MODE == 1) colf[i] = p.xinv[w.row0 + cc];
-          if (MODE == 2 || p.rw_on_input) colslot[i] = p.sorted[w.row0 + cc];
+        for (int i = 0; i < NP; ++i) {
+          const int cc = i * 32 + lane;
+          colf[i] = M == 1 ? 1.0f : 0.0f;
+          colslot[i] = prm.S;
+          if (cc < w.n) {
+            if (M == 1) colf[i] = prm.xinv[w.row0 + cc];
+            if (M == 2 || prm.rw_on_input) colslot[i] = prm.sorted[w.row0 + cc];
+          }
         }
-      }
-      if (MODE == 1 && p.rw_on_input) {
-        // router weight on the input: W13 . (w x) = w (W13 . x), applied to
-        // the float32 accumulators with the row scale
+        if (M == 1 && prm.rw_on_input) {
+          // router weight on the input: W13 . (w x) = w (W13 . x), applied to
+          // the float32 accumulators with the row scale
 #pragma unroll
-        for (int i = 0; i < NP; ++i) colf[i] *= colslot[i] < p.S ? p.topk_w[colslot[i]] : 0.0f;
-      }
-      if (MODE == 2) {
-#pragma unroll
-        for (int i = 0; i < NP; ++i)
-          if (colslot[i] < p.S)
-            colf[i] = (kBf16 ? 1.0f : p.xinv[w.row0 + i * 32 + lane]) *
-                      (p.rw_on_input ? 1.0f : p.topk_w[colslot[i]]);
-      }
-      if (!warp_wait_sleepy(&ctl->accfull[buf], (t >> 1) & 1, ctl, p.status, lane)) break;
-      tc_fence_after();
-      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (buf * C::kNI + half0) * BN;
-      // accumulator columns [c0, c0 + W) into v: half 0 (+ half 1), in that order
-      auto load_acc = [&](auto wtag, int c0, auto& v) {
-        constexpr int W = decltype(wtag)::value;
-        tmem_ld_cols_sync<W>(taddr + c0, v);
-        if (C::kNI == 2 && both) {
-          uint32_t v2[W];
-          tmem_ld_cols_sync<W>(taddr + BN + c0, v2);
-#pragma unroll
-          for (int j = 0; j < W; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(v2[j]));
+          for (int i = 0; i < NP; ++i) colf[i] *= colslot[i] < prm.S ? prm.topk_w[colslot[i]] : 0.0f;
         }
-      };
-      if (MODE == 1) {
-        // lanes (2i, 2i+1) hold gate row i and up row i; per pair of
-        // columns (jj, jj + HALF) the even lane finishes column jj and the
-        // odd lane column jj + HALF, after one exchange
-        const int i = q * 16 + (lane >> 1);
-        const int wrow = w.e * 2 * p.I + (odd ? p.I : 0) + w.mt * 64 + i;
-        // int8: per-channel scale here; uint4: group scales were applied to A
-        const float sc = BITS == 8 ? load_scale(p, p.scale_per_tensor ? w.e : wrow) : 1.0f;
-        // uint4 runs the down GEMM in the K order [0,4,1,5,2,6,3,7] per octet
-        const int col = w.mt * 64 + q * 16 + (BITS == 8 ? (lane >> 1) : permute_octet(lane >> 1));
-        // xv: element c0 / 32 of colf (column c0 + cj on lane (c0 & 31) + cj)
-        auto body = [&](auto wtag, int c0, float xv) {
+        if (M == 2) {
+#pragma unroll
+          for (int i = 0; i < NP; ++i)
+            if (colslot[i] < prm.S)
+              colf[i] = (kBf16M ? 1.0f : prm.xinv[w.row0 + i * 32 + lane]) *
+                        (prm.rw_on_input ? 1.0f : prm.topk_w[colslot[i]]);
+        }
+        // this thread's per-channel scale (8-bit), likewise loaded before the wait
+        float sc_pre = 1.0f;
+        if (BITS == 8) {
+          int64_t srow_g;
+          if (M == 1)
+            srow_g = (int64_t)w.e * 2 * prm.I + (odd ? prm.I : 0) + w.mt * 64 + q * 16 + (lane >> 1);
+          else
+            srow_g = (int64_t)w.e * prm.H + w.mt * kTileM + r;
+          sc_pre = load_scale(prm, prm.scale_per_tensor ? w.e : srow_g);
+        }
+        if (!warp_wait_sleepy(&ctl->accfull[buf], (t >> 1) & 1, ctl, prm.status, lane)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (buf * C::kNI + half0) * BN;
+        // accumulator columns [c0, c0 + W) into v: half 0 (+ half 1), in that order
+        auto load_acc = [&](auto wtag, int c0, auto& v) {
           constexpr int W = decltype(wtag)::value;
-          constexpr int HW = W / 2;
-          uint32_t v[W];
-          load_acc(wtag, c0, v);
+          tmem_ld_cols_sync<W>(taddr + c0, v);
+          if (C::kNI == 2 && both) {
+            uint32_t v2[W];
+            tmem_ld_cols_sync<W>(taddr + BN + c0, v2);
 #pragma unroll
-          for (int jj = 0; jj < HW; ++jj) {
-            const float lo = __uint_as_float(v[jj]) * sc;       // own row, column jj
-            const float hi = __uint_as_float(v[jj + HW]) * sc;  // own row, column jj + HW
-            const float got = __shfl_xor_sync(0xffffffffu, odd ? lo : hi, 1);
-            const int cj = odd ? jj + HW : jj;
-            const float xs = __shfl_sync(0xffffffffu, xv, (c0 & 31) + cj);
-            const float g = (odd ? got : lo) * xs;
-            const float up = (odd ? hi : got) * xs;
-            const float a = __fdividef(g * up, 1.0f + __expf(-g));  // silu(g) * up
-            p.act[(int64_t)(w.row0 + c0 + cj) * p.I + col] = __float2bfloat16_rn(a);
+            for (int j = 0; j < W; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(v2[j]));
           }
         };
-        int c0 = 0;
-        for (; c0 + CH <= w.n; c0 += CH) {
-          float xv = colf[0];
+        if (M == 1) {
+          // lanes (2i, 2i+1) hold gate row i and up row i; per pair of
+          // columns (jj, jj + HALF) the even lane finishes column jj and the
+          // odd lane column jj + HALF, after one exchange
+          // int8: per-channel scale here; uint4: group scales were applied to A
+          const float sc = sc_pre;
+          // uint4 runs the down GEMM in the K order [0,4,1,5,2,6,3,7] per octet
+          const int col = w.mt * 64 + q * 16 + (BITS == 8 ? (lane >> 1) : permute_octet(lane >> 1));
+          // xv: element c0 / 32 of colf (column c0 + cj on lane (c0 & 31) + cj)
+          auto body = [&](auto wtag, int c0, float xv) {
+            constexpr int W = decltype(wtag)::value;
+            constexpr int HW = W / 2;
+            uint32_t v[W];
+            load_acc(wtag, c0, v);
 #pragma unroll
-          for (int i = 1; i < NP; ++i)
-            if ((c0 >> 5) == i) xv = colf[i];
-          body(IC<CH>{}, c0, xv);
-        }
-        if (CH > 16 && c0 < w.n) {  // n is a multiple of 16
-          float xv = colf[0];
+            for (int jj = 0; jj < HW; ++jj) {
+              const float lo = __uint_as_float(v[jj]) * sc;       // own row, column jj
+              const float hi = __uint_as_float(v[jj + HW]) * sc;  // own row, column jj + HW
+              const float got = __shfl_xor_sync(0xffffffffu, odd ? lo : hi, 1);
+              const int cj = odd ? jj + HW : jj;
+              const float xs = __shfl_sync(0xffffffffu, xv, (c0 & 31) + cj);
+              const float g = (odd ? got : lo) * xs;
+              const float up = (odd ? hi : got) * xs;
+              const float a = __fdividef(g * up, 1.0f + __expf(-g));  // silu(g) * up
+              prm.act[(int64_t)(w.row0 + c0 + cj) * prm.I + col] = __float2bfloat16_rn(a);
+            }
+          };
+          int c0 = 0;
+          for (; c0 + CH <= w.n; c0 += CH) {
+            float xv = colf[0];
 #pragma unroll
-          for (int i = 1; i < NP; ++i)
-            if ((c0 >> 5) == i) xv = colf[i];
-          body(IC<16>{}, c0, xv);
-        }
-      } else {
-        const int h = w.mt * kTileM + r;
-        const float sc =
-            BITS == 8 ? load_scale(p, p.scale_per_tensor ? w.e : (int64_t)w.e * p.H + h) : 1.0f;
-        float* yp = p.ypart + (int64_t)w.split * p.S * p.H;
-        // slot, f: element c0 / 32 of colslot, colf (column c0 + jj on lane (c0 & 31) + jj)
-        auto body = [&](auto wtag, int c0, int slot, float f) {
-          constexpr int W = decltype(wtag)::value;
-          uint32_t v[W];
-          load_acc(wtag, c0, v);
-#pragma unroll
-          for (int jj = 0; jj < W; ++jj) {
-            const int sj = __shfl_sync(0xffffffffu, slot, (c0 & 31) + jj);
-            const float fj = __shfl_sync(0xffffffffu, f, (c0 & 31) + jj);
-            if (sj < p.S) yp[(int64_t)sj * p.H + h] = __uint_as_float(v[jj]) * sc * fj;
+            for (int i = 1; i < NP; ++i)
+              if ((c0 >> 5) == i) xv = colf[i];
+            body(IC<CH>{}, c0, xv);
           }
-        };
-        int c0 = 0;
-        for (; c0 + CH <= w.n; c0 += CH) {
-          int sl = colslot[0];
-          float fc = colf[0];
+          if (CH > 16 && c0 < w.n) {  // n is a multiple of 16
+            float xv = colf[0];
 #pragma unroll
-          for (int i = 1; i < NP; ++i)
-            if ((c0 >> 5) == i) {
-              sl = colslot[i];
-              fc = colf[i];
-            }
-          body(IC<CH>{}, c0, sl, fc);
-        }
-        if (CH > 16 && c0 < w.n) {  // n is a multiple of 16
-          int sl = colslot[0];
-          float fc = colf[0];
+            for (int i = 1; i < NP; ++i)
+              if ((c0 >> 5) == i) xv = colf[i];
+            body(IC<16>{}, c0, xv);
+          }
+        } else {
+          const int h = w.mt * kTileM + r;
+          const float sc = sc_pre;
+          float* yp = prm.ypart + (int64_t)w.split * prm.S * prm.H;
+          // slot, f: element c0 / 32 of colslot, colf (column c0 + jj on lane (c0 & 31) + jj)
+          auto body = [&](auto wtag, int c0, int slot, float f) {
+            constexpr int W = decltype(wtag)::value;
+            uint32_t v[W];
+            load_acc(wtag, c0, v);
 #pragma unroll
-          for (int i = 1; i < NP; ++i)
-            if ((c0 >> 5) == i) {
-              sl = colslot[i];
-              fc = colf[i];
+            for (int jj = 0; jj < W; ++jj) {
+              const int sj = __shfl_sync(0xffffffffu, slot, (c0 & 31) + jj);
+              const float fj = __shfl_sync(0xffffffffu, f, (c0 & 31) + jj);
+              if (sj < prm.S) yp[(int64_t)sj * prm.H + h] = __uint_as_float(v[jj]) * sc * fj;
             }
-          body(IC<16>{}, c0, sl, fc);
+          };
+          int c0 = 0;
+          for (; c0 + CH <= w.n; c0 += CH) {
+            int sl = colslot[0];
+            float fc = colf[0];
+#pragma unroll
+            for (int i = 1; i < NP; ++i)
+              if ((c0 >> 5) == i) {
+                sl = colslot[i];
+                fc = colf[i];
+              }
+            body(IC<CH>{}, c0, sl, fc);
+          }
+          if (CH > 16 && c0 < w.n) {  // n is a multiple of 16
+            int sl = colslot[0];
+            float fc = colf[0];
+#pragma unroll
+            for (int i = 1; i < NP; ++i)
+              if ((c0 >> 5) == i) {
+                sl = colslot[i];
+                fc = colf[i];
+              }
+            body(IC<16>{}, c0, sl, fc);
+          }
         }
+        // fused layer: this warp's act columns of the token tile are stored
+        if constexpr (FUSED && M == 1) dep_signal(prm.dep + w.ch, lane);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->accempty[buf]);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl->accempty[buf]);
-    }
+    });
   }
 
   tc_fence_before();
@@ -1342,6 +1475,23 @@ __global__ void __launch_bounds__(CfgOf<MODE, BITS, BN, SYNC>::kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+}
+
+// One expert GEMM (MODE 1 gate/up, 2 down).
+template <int MODE, int BITS, int BN, bool SYNC>
+__global__ void __launch_bounds__(CfgOf<MODE, BITS, BN, SYNC>::kThreads, 1)
+    moe_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ TcParams p) {
+  gemm_body<MODE, BITS, BN, SYNC, false>(tmA, tmB, p, tmA, tmB, p);
+}
+
+// Both expert GEMMs of an 8-bit layer in one launch (FUSED above).
+template <int BN>
+__global__ void __launch_bounds__(CfgOf<1, 8, BN, false>::kThreads, 1)
+    moe_layer_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap tmA2,
+                 const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ TcParams p2) {
+  gemm_body<1, 8, BN, false, true>(tmA, tmB, p, tmA2, tmB2, p2);
 }
 
 // Rows of x gathered into expert-sorted order as f16, each scaled by a power
@@ -1627,6 +1777,7 @@ inline int entries(int K, int bits) { return (K + entry_k(bits) - 1) / entry_k(b
 TcPlan tc_plan(int T, int H, int I, int E, int k, int bits) {
   TcPlan pl;
   pl.sync1 = pl.sync2 = false;
+  pl.layer = false;
   const int64_t S = (int64_t)T * k;
   // Token-slots per tile at most (the MMA's N).  A tile is cut from one
   // expert's segment with the rows it has, so a larger bound costs shared
@@ -1702,6 +1853,8 @@ void common_params(TcParams& p, const MoeArgs& a) {
   p.zrow = nullptr;
   p.rw_on_input = (a.flags & MQ_FWD_ROUTER_WEIGHT_ON_INPUT) ? 1 : 0;
   p.xinv = nullptr;
+  p.dep = nullptr;
+  p.dep_target = 0;
   p.scale = nullptr;
   p.gscale = nullptr;
   p.gzero = nullptr;
@@ -1710,13 +1863,15 @@ void common_params(TcParams& p, const MoeArgs& a) {
 
 }  // namespace
 
-cudaError_t launch_gemm1_tc(const MoeArgs& a, const TcPlan& pl, const void* xs,
-                            const float* xinv, cudaStream_t st) {
+namespace {
+
+// Tensor maps and parameters of the gate/up GEMM; mu bounds its work units.
+cudaError_t prep_gemm1(const MoeArgs& a, const TcPlan& pl, const void* xs, const float* xinv,
+                       CUtensorMap& ta, CUtensorMap& tb, TcParams& p, int& mu) {
   cudaError_t err = get_encoder();
   if (err != cudaSuccess) return err;
   // weight rows in bytes: H int8 codes or H/2 bytes of packed uint4 codes
   const uint64_t rb = a.bits == 8 ? (uint64_t)a.H : (uint64_t)a.H / 2;
-  CUtensorMap ta, tb;
   {
     // w13 [E, 2, I, rb] viewed as {rb, I, 2, E}: one box = 64 gate rows + 64 up rows
     const cuuint64_t dims[4] = {rb, (cuuint64_t)a.I, 2, (cuuint64_t)a.E};
@@ -1734,7 +1889,6 @@ cudaError_t launch_gemm1_tc(const MoeArgs& a, const TcPlan& pl, const void* xs,
                    CU_TENSOR_MAP_SWIZZLE_128B);
     if (err != cudaSuccess) return err;
   }
-  TcParams p;
   common_params(p, a);
   p.ksteps = entries(a.H, a.bits);
   p.MT = a.I / 64;
@@ -1751,7 +1905,19 @@ cudaError_t launch_gemm1_tc(const MoeArgs& a, const TcPlan& pl, const void* xs,
   p.act = a.act;
   p.xinv = xinv;
   const int64_t units = (a.cap / a.bm) * (int64_t)p.MT;  // token tiles <= 16-slot blocks
-  const int mu = (int)(units < (1 << 30) ? units : (1 << 30));
+  mu = (int)(units < (1 << 30) ? units : (1 << 30));
+  return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm1_tc(const MoeArgs& a, const TcPlan& pl, const void* xs,
+                            const float* xinv, cudaStream_t st) {
+  CUtensorMap ta, tb;
+  TcParams p;
+  int mu = 0;
+  const cudaError_t err = prep_gemm1(a, pl, xs, xinv, ta, tb, p, mu);
+  if (err != cudaSuccess) return err;
   return a.bits == 8 ? launch_gemm_bn<1, 8>(pl.bn, pl.sync1, ta, tb, p, mu, st)
                      : launch_gemm_bn<1, 4>(pl.bn, pl.sync1, ta, tb, p, mu, st);
 }
@@ -1764,12 +1930,14 @@ cudaError_t launch_act_to_f16(const MoeArgs& a, float* act_inv, cudaStream_t st)
   return err != cudaSuccess ? err : cudaGetLastError();
 }
 
-cudaError_t launch_gemm2_tc(const MoeArgs& a, const TcPlan& pl, const float* act_inv,
-                            float* ypart, cudaStream_t st) {
+namespace {
+
+// Tensor maps and parameters of the down GEMM; mu bounds its work units.
+cudaError_t prep_gemm2(const MoeArgs& a, const TcPlan& pl, const float* act_inv, float* ypart,
+                       CUtensorMap& ta, CUtensorMap& tb, TcParams& p, int& mu) {
   cudaError_t err = get_encoder();
   if (err != cudaSuccess) return err;
   const uint64_t rb = a.bits == 8 ? (uint64_t)a.I : (uint64_t)a.I / 2;
-  CUtensorMap ta, tb;
   {
     const cuuint64_t dims[2] = {rb, (cuuint64_t)a.E * a.H};
     const cuuint64_t strides[1] = {rb};
@@ -1790,7 +1958,6 @@ cudaError_t launch_gemm2_tc(const MoeArgs& a, const TcPlan& pl, const float* act
                    CU_TENSOR_MAP_SWIZZLE_128B);
     if (err != cudaSuccess) return err;
   }
-  TcParams p;
   common_params(p, a);
   p.ksteps = entries(a.I, a.bits);
   p.MT = a.H / kTileM;
@@ -1807,9 +1974,64 @@ cudaError_t launch_gemm2_tc(const MoeArgs& a, const TcPlan& pl, const float* act
   p.ypart = ypart;
   p.xinv = act_inv;
   const int64_t units = (a.cap / a.bm) * (int64_t)p.MT * p.splits;
-  const int mu = (int)(units < (1 << 30) ? units : (1 << 30));
+  mu = (int)(units < (1 << 30) ? units : (1 << 30));
+  return cudaSuccess;
+}
+
+template <int BN>
+cudaError_t launch_layer(const CUtensorMap& ta, const CUtensorMap& tb, const TcParams& p,
+                         const CUtensorMap& ta2, const CUtensorMap& tb2, const TcParams& p2,
+                         int max_units, cudaStream_t st) {
+  constexpr size_t smem = smem_for<1, 8, BN, false>();
+  static_assert(smem <= 227 * 1024, "shared memory");
+  auto kern = moe_layer_tc<BN>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  // at most one CTA per SM (shared memory and all tensor-memory columns):
+  // with grid <= SMs every CTA becomes resident, which the down units'
+  // waits for other CTAs' gate/up units rely on
+  const int sms = tc_num_sms();
+  const int grid = max_units < sms ? max_units : sms;
+  if (grid <= 0) return cudaSuccess;
+  err = launch_pdl(kern, dim3(grid), dim3(CfgOf<1, 8, BN, false>::kThreads), smem, st, ta, tb, p,
+                   ta2, tb2, p2);
+  return err != cudaSuccess ? err : cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm2_tc(const MoeArgs& a, const TcPlan& pl, const float* act_inv,
+                            float* ypart, cudaStream_t st) {
+  CUtensorMap ta, tb;
+  TcParams p;
+  int mu = 0;
+  const cudaError_t err = prep_gemm2(a, pl, act_inv, ypart, ta, tb, p, mu);
+  if (err != cudaSuccess) return err;
   return a.bits == 8 ? launch_gemm_bn<2, 8>(pl.bn, pl.sync2, ta, tb, p, mu, st)
                      : launch_gemm_bn<2, 4>(pl.bn, pl.sync2, ta, tb, p, mu, st);
+}
+
+cudaError_t launch_layer_tc(const MoeArgs& a, const TcPlan& pl, const void* xs,
+                            const float* xinv, float* ypart, cudaStream_t st) {
+  if (a.bits != 8 || pl.sync1 || pl.sync2 || a.dep == nullptr) return cudaErrorInvalidValue;
+  CUtensorMap ta, tb, ta2, tb2;
+  TcParams p, p2;
+  int mu1 = 0, mu2 = 0;
+  cudaError_t err = prep_gemm1(a, pl, xs, xinv, ta, tb, p, mu1);
+  if (err != cudaSuccess) return err;
+  err = prep_gemm2(a, pl, nullptr, ypart, ta2, tb2, p2, mu2);
+  if (err != cudaSuccess) return err;
+  // each gate/up unit's 4 epilogue warps count once per token tile
+  p.dep = a.dep;
+  p2.dep = a.dep;
+  p2.dep_target = 4 * p.MT;
+  const int64_t mu = (int64_t)mu1 + mu2;
+  const int m = (int)(mu < (1 << 30) ? mu : (1 << 30));
+  switch (pl.bn) {
+    case 64: return launch_layer<64>(ta, tb, p, ta2, tb2, p2, m, st);
+    case 128: return launch_layer<128>(ta, tb, p, ta2, tb2, p2, m, st);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_combine_splits(const MoeArgs& a, const float* ypart, int splits,
