@@ -271,9 +271,8 @@ int moe_quant_forward(const void* x, int T, int H, int I, int E, int k,
  * them exactly; the products run either on tcgen05 (a single issuing thread
  * per SM, accumulators in tensor memory) or, for experts holding a few
  * token-slots, on warp-level MMAs issued by the converter warps themselves.
- * By default the gate/up GEMM of 8-bit batches of up to 32 tokens takes the
- * warp-level MMAs and everything else tcgen05 (the faster choice measured
- * on GB300 for each GEMM and batch size).
+ * By default both GEMMs run on tcgen05 (the faster choice measured on GB300
+ * for every GEMM and batch size); the warp-level MMAs run when forced.
  * For 8-bit layers of many small experts both GEMMs can run in one
  * persistent launch on tcgen05 (token tiles of 64 or 128 rows): each SM
  * streams its gate/up weight tiles and then its down weight tiles without a

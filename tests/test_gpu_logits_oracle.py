@@ -11,9 +11,9 @@ of every sampled token is compared.  The sizes span the kernels' plans:
 (Mixtral-shaped T = 1, 8, 32), 64-token tiles (T = 64), the fused router in
 the align kernel (small T·k·ceil(E/32)) and the separate router kernel
 (fine-grained T = 512), and the uint4 path at T = 1 -- each with the
-default consumers (warp-level MMAs in the 8-bit gate/up GEMM up to 32
-tokens, tcgen05 elsewhere), with tcgen05 forced for both GEMMs in two
-launches, and (8-bit) with both GEMMs forced into one launch.
+default kernels (tcgen05 consumers; one launch for both GEMMs of the
+fine-grained layer at T = 512), with the warp-level-MMA consumers forced
+for both GEMMs, and (8-bit) with both GEMMs forced into one launch.
 """
 
 import numpy as np
@@ -75,20 +75,20 @@ def mixtral():
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("path", ["auto", "tc", "layer"])
+@pytest.mark.parametrize("path", ["auto", "decode", "layer"])
 @pytest.mark.parametrize("T", [1, 8, 32, 64])
 def test_logits_forward_mixtral_decode(mixtral, T, path):
     _logits_case(mixtral, T, seed=20 + T, path=path)
 
 
-@pytest.mark.parametrize("path", ["auto", "tc", "layer"])
+@pytest.mark.parametrize("path", ["auto", "tc", "decode", "layer"])
 @pytest.mark.parametrize("T", [1, 64, 512])
 def test_logits_forward_fine_grained(T, path):
     layer = Layer(W["fine"], seed=0)
     _logits_case(layer, T, seed=30 + T, path=path)
 
 
-@pytest.mark.parametrize("path", ["auto", "tc"])
+@pytest.mark.parametrize("path", ["auto", "decode"])
 @pytest.mark.parametrize("T", [1, 32])
 def test_logits_forward_w4a16(T, path):
     layer = Layer(W["w4a16"], seed=0)

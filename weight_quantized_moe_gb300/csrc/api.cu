@@ -109,15 +109,15 @@ constexpr int kAlignBlock = 16;
 // Which consumers the expert GEMMs run.  With a few token-slots per expert
 // the converter warps can multiply with warp-level MMAs themselves
 // (TcPlan::sync1 / sync2; token tiles of 16 or 32 rows) instead of feeding
-// one tcgen05.mma issuer.  Measured on GB300 (kernel times per
-// launch): the warp-MMA gate/up GEMM is faster for batches of up to
-// kSyncGateUpMaxT tokens of 8-bit codes (Mixtral-shaped T=1: 49 vs 56 us,
-// T=8: 150 vs 163, T=32: 171 vs 179); the down GEMM (bf16 conversion,
-// heavier) and uint4 are faster on the tcgen05 consumers.  On GB300 each
-// mma.sync takes about 8 cycles of its scheduler's issue that dequant
-// instructions cannot overlap, so the warp MMAs pay off only where the
-// conversion is cheap and few 8-token groups run.
-constexpr int kSyncGateUpMaxT = 32;
+// the tcgen05.mma issuers.  That mode was the faster gate/up GEMM for 8-bit
+// batches of up to 32 tokens while each converter group had one
+// tensor-memory stage (Mixtral-shaped T=8: 150 vs 163 us per launch).  With
+// three stages shared by two issuers, tcgen05 is faster at every size
+// measured (Mixtral-shaped gate/up T=1: 56.4 vs 57.8 us, T=8: 148.6 vs
+// 158.3, T=32: 161.7 vs 174.0; fine-grained T=8: 25.1 vs 26.0), so the
+// default takes tcgen05 and the warp-MMA mode runs when forced
+// (MQ_FWD_PATH_DECODE).  Each mma.sync takes about 8 cycles of its
+// scheduler's issue that dequant instructions cannot overlap.
 
 // The one-launch layer by default where it measured faster than two
 // launches (fine-grained E=128, k=8, H=2048, I=768 with Zipf routing, step
@@ -149,12 +149,10 @@ TcPlan fwd_plan(int T, int H, int I, int E, int k, int bits, int group_size, uns
     if (T <= 64) pl.splits = dec_splits(T, H, I, E, k, bits);
     return pl;
   }
-  // default: warp-MMA gate/up GEMM for small 8-bit batches (the tcgen05 plan
-  // uses 16-row tiles up to 32 tokens too, so both GEMMs share the chunk
-  // table)
-  if (ok && bits == 8 && T <= kSyncGateUpMaxT) pl.sync1 = true;
-  // one launch for both GEMMs of 8-bit layers of many experts (measured rule above)
-  if (bits == 8 && !pl.sync1 && pl.bn >= 64 && layer_default(T, E)) pl.layer = true;
+  // default: tcgen05 for both GEMMs; one launch for both GEMMs of 8-bit
+  // layers of many experts (measured rule above)
+  (void)ok;
+  if (bits == 8 && pl.bn >= 64 && layer_default(T, E)) pl.layer = true;
   return pl;
 }
 

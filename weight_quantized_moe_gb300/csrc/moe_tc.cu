@@ -54,6 +54,7 @@ constexpr int kRasterGroup = 8;           // weight tiles per raster group
 constexpr uint32_t kTmemCols = 512;
 constexpr int kSmemBudget = 212 * 1024;   // A ring + B ring
 constexpr int kMaxSteps = 4;              // MMA-step ring depth (max)
+constexpr int kMaxVirt = 6;               // barrier slots of the MMA-step ring (max)
 constexpr int kUnitList = 512;            // work units per CTA decoded once into shared memory
 // uint4: a work unit's group scales ([128 tile rows][G] f16) and zero points
 // ([64 row pairs][G] bytes) are staged in shared memory, double-buffered
@@ -73,21 +74,32 @@ inline bool stage_fits(int G) { return 128 * G * 2 + 64 * G <= kStageBytes; }
 //   one MMA commit per step frees both.
 // * One tcgen05.mma takes about 80 cycles to issue whatever N is, and the
 //   issuing thread's wait and commit around each 16-MMA step add about a
-//   third to that.  For 16- and 32-token tiles a second issuer thread takes
-//   every other step, so that one thread's wait and commit overlap the
-//   other's MMAs; each issuer accumulates its steps into its own half of the
-//   accumulator (kNI = 2 halves, added in a fixed order by the epilogue),
-//   and step st uses tensor-memory stage st % 2 (kSteps = 2).  Not for the
-//   8-bit down GEMM: its bf16 conversion needs the third stage of overlap
-//   more than the issuers need each other (measured on Mixtral shapes: the
-//   launch takes 104 us with one issuer and three stages, 118 us with two
-//   issuers and two).
+//   third to that; two threads issuing at once reach twice the rate.  For
+//   16- and 32-token tiles a second issuer thread takes every other step;
+//   each issuer accumulates its steps into its own half of the accumulator
+//   (kNI = 2 halves, added in a fixed order by the epilogue).  Step st uses
+//   tensor-memory stage st % 3: a converter group converts its next step
+//   while its issuer's MMAs still read the previous one.  With one stage
+//   per issuer (st % 2) the two alternated, and the Mixtral-shaped gate/up
+//   launch at T=64 took 184 us against 163 us with three; the 8-bit down
+//   GEMM kept one issuer then (its bf16 conversion needed a third stage),
+//   and with three stages two issuers serve it too (T=64: 106 -> 99 us).
 template <int BN, int NI, int SB = 0>
 struct TileCfg {
   static constexpr int kNI = NI;                // MMA issuer threads
   static constexpr int kACol0 = 2 * kNI * BN;   // two accumulator buffers of kNI halves
   static constexpr int kStepFit = ((int)kTmemCols - kACol0) / kAColsPerStep;
-  static constexpr int kSteps = kNI == 2 ? 2 : (kStepFit > kMaxSteps ? kMaxSteps : kStepFit);
+  // one issuer: as many stages as fit (at most kMaxSteps); two issuers:
+  // three where they fit, so that a converter group's next step can be
+  // converted while its issuer's MMAs of the previous one still read their
+  // stage (with two stages, one per issuer, conversion and MMAs alternated)
+  static constexpr int kSteps =
+      kNI == 2 ? (kStepFit >= 3 ? 3 : 2) : (kStepFit > kMaxSteps ? kMaxSteps : kStepFit);
+  // barrier slots of the step ring: step st uses stage st % kSteps and the
+  // barriers of slot st % kVirt.  Two issuers with three stages: six slots,
+  // so that each slot serves one issuer and one converter group only (st % 6
+  // fixes st % 2 and st % 3) and every parity wait is exact
+  static constexpr int kVirt = (kNI == 2 && kSteps == 3) ? 6 : kSteps;
   static constexpr int kThreads = (kEpiWarp0 + 4 + (kNI - 1)) * 32;
   static constexpr int kBBytesK = BN * kBK * 2;     // activations per weight stage
   static constexpr int kBBytes = kG * kBBytesK;     // activations per MMA step
@@ -95,7 +107,8 @@ struct TileCfg {
   static constexpr int kAStagesSmem = kAFit > 12 ? 12 : kAFit;
   static_assert(kACol0 + kSteps * kAColsPerStep <= (int)kTmemCols, "tensor memory budget");
   static_assert(kSteps >= 2, "MMA-step depth");
-  static_assert(kNI == 1 || (kSteps == 2 && kStepFit >= 2), "two issuers: one stage each");
+  static_assert(kNI == 1 || kStepFit >= 2, "two issuers: at least one stage each");
+  static_assert(kVirt <= kMaxVirt, "barrier slots");
   static_assert(kAStagesSmem >= 3, "weight ring depth");
 };
 
@@ -115,6 +128,7 @@ struct SyncCfg {
   static constexpr int kNI = 1;
   static constexpr int kThreads = (kEpiWarp0 + 4) * 32;
   static constexpr int kSteps = 4;
+  static constexpr int kVirt = kSteps;
   static_assert(kSteps % 2 == 0, "one converter group per activation slot");
   static constexpr int kACol0 = 0;
   static constexpr int kBBytesK = BN * kBK * 2;
@@ -130,7 +144,7 @@ struct SyncCfg {
 
 template <int MODE, int BITS, int BN, bool SYNC>
 struct CfgSel {
-  using type = TileCfg<BN, (BN <= 32 && !(MODE == 2 && BITS == 8)) ? 2 : 1,
+  using type = TileCfg<BN, BN <= 32 ? 2 : 1,
                        BITS == 4 ? 2 * kStageBytes : 0>;
 };
 template <int MODE, int BITS, int BN>
@@ -256,9 +270,9 @@ __device__ __forceinline__ Unit cta_unit(const TcParams& p, const int4* ulist, i
 struct alignas(16) SharedCtl {
   uint64_t fullA[16];
   uint64_t emptyA[16];
-  uint64_t fullB[kMaxSteps];
-  uint64_t afull[kMaxSteps];     // converted A (and its activations) ready for the MMA
-  uint64_t stepfree[kMaxSteps];  // MMAs of the step done: TMEM A stage and B stage free
+  uint64_t fullB[kMaxVirt];
+  uint64_t afull[kMaxVirt];     // converted A (and its activations) ready for the MMA
+  uint64_t stepfree[kMaxVirt];  // MMAs of the step done: TMEM A stage and B stage free
   uint64_t accfull[2];
   uint64_t accempty[2];
   uint64_t fullS[2];    // uint4 staging: a unit's scales and zeros landed
@@ -846,6 +860,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
   constexpr int NAG = NA / kConvGroups;  // weight-ring slots per converter group
   static_assert(kConvGroups == 2 && NAG >= 2, "two converter groups, two slots each");
   constexpr int ND = C::kSteps;
+  constexpr int NV = C::kVirt;  // barrier slots of the step ring (stage st % ND, slot st % NV)
   constexpr int kBBytesK = C::kBBytesK;
   constexpr int kBBytes = C::kBBytes;
   constexpr int kACol0 = C::kACol0;
@@ -884,7 +899,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
       mbar_init(&ctl->fullA[s], 1);
       mbar_init(&ctl->emptyA[s], 4);  // the 4 warps of the converter group
     }
-    for (int s = 0; s < ND; ++s) {
+    for (int s = 0; s < NV; ++s) {
       mbar_init(&ctl->fullB[s], 1);
       mbar_init(&ctl->afull[s], 4);
       // MMA commit; warp-MMA mode: the 4 warps of the step's converter group
@@ -1052,14 +1067,18 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
         }
         for (int ks = ks0; ks < ks1; ks += kGA, ++st) {
           const int nboxes = min(kGA, ks1 - ks) * kEntryK / 64;  // 64-K activation boxes
-          const int d = st % ND;
-          ok = warp_wait(&ctl->stepfree[d], ((st / ND) & 1) ^ 1, ctl, prm.status, lane);
-          if (!ok) break;
+          const int d = st % ND;  // activation slot
+          const int v = st % NV;  // its barriers
+          if (st >= ND) {  // the MMAs of the slot's previous fill (step st - ND) are done
+            ok = warp_wait(&ctl->stepfree[(st - ND) % NV], ((st - ND) / NV) & 1, ctl, prm.status,
+                           lane);
+            if (!ok) break;
+          }
           if (lane == 0) {
-            mbar_arrive_expect_tx(&ctl->fullB[d], nboxes * (kBBytesK / 2));
+            mbar_arrive_expect_tx(&ctl->fullB[v], nboxes * (kBBytesK / 2));
             uint8_t* b = sB + d * kBBytes;
             for (int j = 0; j < nboxes; ++j)  // past K the box reads the fill value 0
-              tma_load_2d(b + j * (kBBytesK / 2), &mB, &ctl->fullB[d], ks * kEntryK + 64 * j,
+              tma_load_2d(b + j * (kBBytesK / 2), &mB, &ctl->fullB[v], ks * kEntryK + 64 * j,
                           w.row0);
           }
           __syncwarp();
@@ -1070,7 +1089,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
       const int n = st < ND ? st : ND;
       for (int dd = 1; dd <= n; ++dd) {
         const int j = st - dd;
-        wait_drain(&ctl->fullB[j % ND], (j / ND) & 1);
+        wait_drain(&ctl->fullB[j % NV], (j / NV) & 1);
       }
     }
     __syncwarp();
@@ -1092,8 +1111,6 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
       const uint64_t b_desc0 = smem_desc_k_sw128(smem_addr(sB));
       const int ip = warp == 1 ? 0 : 1;
       int st = 0, t = 0;
-      int d = 0;         // stage of step st (st % ND), advanced without a division
-      uint32_t ph = 0;   // its barrier parity ((st / ND) & 1)
       bool ok = true;
       phases([&](auto ph_tag, const TcParams& prm, const CUtensorMap& mA, const CUtensorMap& mB,
                const int4* ul, int tot, int u0) {
@@ -1110,15 +1127,12 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
           const uint32_t d_tmem = tmem + (buf * C::kNI + ip) * BN;
           uint32_t acc = 0;  // the first step of this issuer in the unit overwrites
           for (int ks = ks0; ks < ks1; ks += kGA, ++st) {
-            const int dc = d;
-            const uint32_t phc = ph;
-            if (++d == ND) {
-              d = 0;
-              ph ^= 1u;
-            }
             if (C::kNI == 2 && (st & 1) != ip) continue;
+            const int dc = st % ND;                          // A stage and activation slot
+            const int vc = st % NV;                          // their barriers
+            const uint32_t phc = (uint32_t)(st / NV) & 1u;  // parity of this use
             const int nmma = min(kGA, ks1 - ks) * kEntryK / 16;  // K = 16 per MMA
-            ok = wait_bounded(&ctl->afull[dc], phc, ctl, prm.status);
+            ok = wait_bounded(&ctl->afull[vc], phc, ctl, prm.status);
             if (!ok) break;
             tc_fence_after();
             // four K slices of 16 (32 bytes) per 64-K activation box
@@ -1134,7 +1148,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
                        kIdescM, kk > 0 ? 1u : acc);
             }
             acc = 1;
-            mma_commit(&ctl->stepfree[dc]);
+            mma_commit(&ctl->stepfree[vc]);
           }
           if (!ok) break;
           mma_commit(&ctl->accfull[buf]);
@@ -1199,7 +1213,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
         for (int ks = ks0; ks < ks1; ks += kGA, ++st) {
           const int nk = min(kGA, ks1 - ks);
           if (st % kConvGroups != grp) continue;
-          const int d = st % ND;
+          const int d = st % ND;  // tensor-memory A stage and activation slot
+          const int v = st % NV;  // their barriers
           for (int j = 0; j < nk && ok; ++j, ++lit) {
             const int sa = grp * NAG + lit % NAG;
             uint32_t zz[8], ss[8];  // uint4: per 32-K chunk, issued before the tile wait
@@ -1238,9 +1253,13 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
 #pragma unroll
             for (int c = 0; c < 8; ++c) x[c] = ld_chunk(row, (c + rot) & 7, sw);
             if (j == 0) {
-              // the MMAs that last read this tensor-memory stage must be done
-              ok = warp_wait(&ctl->stepfree[d], ((st / ND) & 1) ^ 1, ctl, prm.status, lane);
-              if (!ok) break;
+              // the MMAs that last read this tensor-memory stage (step st - ND)
+              // must be done
+              if (st >= ND) {
+                ok = warp_wait(&ctl->stepfree[(st - ND) % NV], ((st - ND) / NV) & 1, ctl,
+                               prm.status, lane);
+                if (!ok) break;
+              }
               tc_fence_after();
             }
             const uint32_t tbase = tmem + tcol + d * kAColsPerStep + j * kEntryCols;
@@ -1282,12 +1301,12 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
           if (!ok) break;
           // the step's activations (exact: the MMAs that read this slot's
           // previous fill are done, so its barrier is at most this phase behind)
-          ok = warp_wait(&ctl->fullB[d], (st / ND) & 1, ctl, prm.status, lane);
+          ok = warp_wait(&ctl->fullB[v], (st / NV) & 1, ctl, prm.status, lane);
           if (!ok) break;
           tmem_st_wait();
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&ctl->afull[d]);
+          if (lane == 0) mbar_arrive(&ctl->afull[v]);
         }
         if (!ok) break;
         if (BITS == 4 && prm.stage) {  // done with the unit's staged scales
