@@ -100,15 +100,21 @@ struct TileCfg {
   // so that each slot serves one issuer and one converter group only (st % 6
   // fixes st % 2 and st % 3) and every parity wait is exact
   static constexpr int kVirt = (kNI == 2 && kSteps == 3) ? 6 : kSteps;
+  // activation ring slots (step st in slot st % kBSlots): as many as the
+  // stages, or, for 16-token tiles with six barrier slots, six (8 KB each),
+  // so that a step's activation tile is requested six steps ahead and its
+  // L2 latency stays off the converters' path
+  static constexpr int kBSlots = (kVirt == 6 && BN == 16) ? 6 : kSteps;
   static constexpr int kThreads = (kEpiWarp0 + 4 + (kNI - 1)) * 32;
   static constexpr int kBBytesK = BN * kBK * 2;     // activations per weight stage
   static constexpr int kBBytes = kG * kBBytesK;     // activations per MMA step
-  static constexpr int kAFit = (kSmemBudget - SB - kSteps * kBBytes) / kABytes;
+  static constexpr int kAFit = (kSmemBudget - SB - kBSlots * kBBytes) / kABytes;
   static constexpr int kAStagesSmem = kAFit > 12 ? 12 : kAFit;
   static_assert(kACol0 + kSteps * kAColsPerStep <= (int)kTmemCols, "tensor memory budget");
   static_assert(kSteps >= 2, "MMA-step depth");
   static_assert(kNI == 1 || kStepFit >= 2, "two issuers: at least one stage each");
   static_assert(kVirt <= kMaxVirt, "barrier slots");
+  static_assert(kBSlots == kSteps || kBSlots == kVirt, "activation slots");
   static_assert(kAStagesSmem >= 3, "weight ring depth");
 };
 
@@ -129,6 +135,7 @@ struct SyncCfg {
   static constexpr int kThreads = (kEpiWarp0 + 4) * 32;
   static constexpr int kSteps = 4;
   static constexpr int kVirt = kSteps;
+  static constexpr int kBSlots = kSteps;
   static_assert(kSteps % 2 == 0, "one converter group per activation slot");
   static constexpr int kACol0 = 0;
   static constexpr int kBBytesK = BN * kBK * 2;
@@ -861,6 +868,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
   static_assert(kConvGroups == 2 && NAG >= 2, "two converter groups, two slots each");
   constexpr int ND = C::kSteps;
   constexpr int NV = C::kVirt;  // barrier slots of the step ring (stage st % ND, slot st % NV)
+  constexpr int NB = C::kBSlots;  // activation ring slots (st % NB)
   constexpr int kBBytesK = C::kBBytesK;
   constexpr int kBBytes = C::kBBytes;
   constexpr int kACol0 = C::kACol0;
@@ -879,10 +887,10 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* sA = smem;                 // NA x 16 KB (int8 codes, 128-byte swizzle)
-  uint8_t* sB = smem + NA * kABytes;  // ND x kG x 2 x BN x 128 B (16-bit, 128-byte swizzle)
-  float* partials = reinterpret_cast<float*>(sB + ND * kBBytes);  // warp-MMA mode only
+  uint8_t* sB = smem + NA * kABytes;  // NB x kG x 2 x BN x 128 B (16-bit, 128-byte swizzle)
+  float* partials = reinterpret_cast<float*>(sB + NB * kBBytes);  // warp-MMA mode only
   constexpr int kPartBytes = partial_bytes<SYNC, BN>();
-  SharedCtl* ctl = reinterpret_cast<SharedCtl*>(sB + ND * kBBytes + kPartBytes);
+  SharedCtl* ctl = reinterpret_cast<SharedCtl*>(sB + NB * kBBytes + kPartBytes);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -966,7 +974,6 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
     int st = 0;
     int lit0 = 0, lit1 = 0;  // weight stages issued into each group's half of the ring
     bool ok = true;
-    int nstaged = 0;  // units whose scales were staged
     phases([&](auto ph_tag, const TcParams& prm, const CUtensorMap& mA, const CUtensorMap& mB,
                const int4* ul, int tot, int u0) {
       constexpr int M = decltype(ph_tag)::value;
@@ -974,10 +981,63 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
         const Unit w = cta_unit<BN>(prm, ul, ui, u, kUL);
         const int ks0 = w.split * prm.ksteps / prm.splits;
         const int ks1 = (w.split + 1) * prm.ksteps / prm.splits;
+        for (int ks = ks0; ks < ks1 && ok; ks += kGA, ++st) {
+          const int g = st % kConvGroups;
+          const int nk = min(kGA, ks1 - ks);
+          for (int j = 0; j < nk; ++j) {
+            const int n = g ? lit1 : lit0;
+            const int s = g * NAG + n % NAG;
+            ok = warp_wait(&ctl->emptyA[s], ((n / NAG) & 1) ^ 1, ctl, prm.status, lane);
+            if (!ok) break;
+            if (lane == 0) {
+              mbar_arrive_expect_tx(&ctl->fullA[s], kABytes);
+              uint8_t* a = sA + s * kABytes;
+              if (M == 1) {
+                // {K, row in half, gate/up half, expert}: 64 gate rows then 64 up rows
+                tma_load_4d(a, &mA, &ctl->fullA[s], (ks + j) * 128, w.mt * 64, 0, w.e);
+              } else {
+                tma_load_2d(a, &mA, &ctl->fullA[s], (ks + j) * 128, w.e * prm.H + w.mt * kTileM);
+              }
+            }
+            __syncwarp();
+            if (g) ++lit1; else ++lit0;
+          }
+        }
+      }
+    });
+    // Never leave with copies in flight: wait for the last load issued into
+    // each slot of both halves.
+    if (lane == 0) {
+      for (int g = 0; g < kConvGroups; ++g) {
+        const int n = g ? lit1 : lit0;
+        for (int d = 1; d <= (n < NAG ? n : NAG); ++d) {
+          const int j = n - d;
+          wait_drain(&ctl->fullA[g * NAG + j % NAG], (j / NAG) & 1);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ------------------------------------------ B producer (activations) ----
+    mq::pdl_wait();
+    int st = 0;
+    bool ok = true;
+    int nstaged = 0;  // units whose uint4 scales were staged
+    phases([&](auto ph_tag, const TcParams& prm, const CUtensorMap& mA, const CUtensorMap& mB,
+               const int4* ul, int tot, int u0) {
+      constexpr int M = decltype(ph_tag)::value;
+      int dep_ch = -1;  // fused layer: the last token tile whose gate/up outputs were waited for
+      for (int u = u0, ui = 0; u < tot && ok; u += gridDim.x, ++ui) {
+        const Unit w = cta_unit<BN>(prm, ul, ui, u, kUL);
+        const int ks0 = w.split * prm.ksteps / prm.splits;
+        const int ks1 = (w.split + 1) * prm.ksteps / prm.splits;
         if (BITS == 4 && prm.stage) {
           // the unit's group scales (and zero points): one contiguous block per
           // 64 (gate/up) or 128 (down) weight rows, 16-byte aligned because
-          // tiles start at multiples of 64 rows
+          // tiles start at multiples of 64 rows.  Staged here rather than by
+          // the weight producer, whose stream would otherwise stall until the
+          // converters have finished the unit two back (this producer runs at
+          // most ND steps ahead of the MMAs, so it seldom waits here)
           const int b = ui & 1;
           ok = warp_wait(&ctl->emptyS[b], ((ui >> 1) & 1) ^ 1, ctl, prm.status, lane);
           if (!ok) break;
@@ -1004,59 +1064,6 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
           __syncwarp();
           ++nstaged;
         }
-        for (int ks = ks0; ks < ks1 && ok; ks += kGA, ++st) {
-          const int g = st % kConvGroups;
-          const int nk = min(kGA, ks1 - ks);
-          for (int j = 0; j < nk; ++j) {
-            const int n = g ? lit1 : lit0;
-            const int s = g * NAG + n % NAG;
-            ok = warp_wait(&ctl->emptyA[s], ((n / NAG) & 1) ^ 1, ctl, prm.status, lane);
-            if (!ok) break;
-            if (lane == 0) {
-              mbar_arrive_expect_tx(&ctl->fullA[s], kABytes);
-              uint8_t* a = sA + s * kABytes;
-              if (M == 1) {
-                // {K, row in half, gate/up half, expert}: 64 gate rows then 64 up rows
-                tma_load_4d(a, &mA, &ctl->fullA[s], (ks + j) * 128, w.mt * 64, 0, w.e);
-              } else {
-                tma_load_2d(a, &mA, &ctl->fullA[s], (ks + j) * 128, w.e * prm.H + w.mt * kTileM);
-              }
-            }
-            __syncwarp();
-            if (g) ++lit1; else ++lit0;
-          }
-        }
-      }
-    });
-    // Never leave with copies in flight: wait for the last load issued into
-    // each slot of both halves, and for the last staged scales.
-    if (lane == 0) {
-      for (int g = 0; g < kConvGroups; ++g) {
-        const int n = g ? lit1 : lit0;
-        for (int d = 1; d <= (n < NAG ? n : NAG); ++d) {
-          const int j = n - d;
-          wait_drain(&ctl->fullA[g * NAG + j % NAG], (j / NAG) & 1);
-        }
-      }
-      for (int d = 1; d <= (nstaged < 2 ? nstaged : 2); ++d) {
-        const int j = nstaged - d;
-        wait_drain(&ctl->fullS[j & 1], (j >> 1) & 1);
-      }
-    }
-    __syncwarp();
-  } else if (warp == 2) {
-    // ------------------------------------------ B producer (activations) ----
-    mq::pdl_wait();
-    int st = 0;
-    bool ok = true;
-    phases([&](auto ph_tag, const TcParams& prm, const CUtensorMap& mA, const CUtensorMap& mB,
-               const int4* ul, int tot, int u0) {
-      constexpr int M = decltype(ph_tag)::value;
-      int dep_ch = -1;  // fused layer: the last token tile whose gate/up outputs were waited for
-      for (int u = u0, ui = 0; u < tot && ok; u += gridDim.x, ++ui) {
-        const Unit w = cta_unit<BN>(prm, ul, ui, u, kUL);
-        const int ks0 = w.split * prm.ksteps / prm.splits;
-        const int ks1 = (w.split + 1) * prm.ksteps / prm.splits;
         if constexpr (FUSED && M == 2) {
           // the token tile's act rows: every gate/up unit of the tile is done
           if (w.ch != dep_ch) {
@@ -1067,10 +1074,10 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
         }
         for (int ks = ks0; ks < ks1; ks += kGA, ++st) {
           const int nboxes = min(kGA, ks1 - ks) * kEntryK / 64;  // 64-K activation boxes
-          const int d = st % ND;  // activation slot
-          const int v = st % NV;  // its barriers
-          if (st >= ND) {  // the MMAs of the slot's previous fill (step st - ND) are done
-            ok = warp_wait(&ctl->stepfree[(st - ND) % NV], ((st - ND) / NV) & 1, ctl, prm.status,
+          const int d = st % NB;  // activation slot
+          const int v = st % NV;  // the step's barriers
+          if (st >= NB) {  // the MMAs of the slot's previous fill (step st - NB) are done
+            ok = warp_wait(&ctl->stepfree[(st - NB) % NV], ((st - NB) / NV) & 1, ctl, prm.status,
                            lane);
             if (!ok) break;
           }
@@ -1086,10 +1093,14 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
       }
     });
     if (lane == 0) {
-      const int n = st < ND ? st : ND;
+      const int n = st < NB ? st : NB;
       for (int dd = 1; dd <= n; ++dd) {
         const int j = st - dd;
         wait_drain(&ctl->fullB[j % NV], (j / NV) & 1);
+      }
+      for (int d = 1; d <= (nstaged < 2 ? nstaged : 2); ++d) {
+        const int j = nstaged - d;
+        wait_drain(&ctl->fullS[j & 1], (j >> 1) & 1);
       }
     }
     __syncwarp();
@@ -1136,7 +1147,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
             if (!ok) break;
             tc_fence_after();
             // four K slices of 16 (32 bytes) per 64-K activation box
-            const uint64_t b_desc = b_desc0 + (uint64_t)(dc * kStageD);
+            const uint64_t b_desc = b_desc0 + (uint64_t)((st % NB) * kStageD);
             const uint32_t a_tmem = tmem + kACol0 + dc * kAColsPerStep;
             if (nmma == 16) {
               mma_ts_x16<2, 4, 6, kBoxD, kBoxD + 2, kBoxD + 4, kBoxD + 6, 2 * kBoxD, 2 * kBoxD + 2,
@@ -1752,7 +1763,7 @@ template <int MODE, int BITS, int BN, bool SYNC>
 constexpr size_t smem_for() {
   using C = CfgOf<MODE, BITS, BN, SYNC>;
   const size_t part = (size_t)partial_bytes<SYNC, BN>();
-  const size_t need = 1024 + (size_t)C::kAStagesSmem * kABytes + (size_t)C::kSteps * C::kBBytes +
+  const size_t need = 1024 + (size_t)C::kAStagesSmem * kABytes + (size_t)C::kBSlots * C::kBBytes +
                       part + sizeof(SharedCtl) + kUnitList * sizeof(int4) +
                       (size_t)stage_bytes<BITS>();
   return need < 120 * 1024 ? 120 * 1024 : need;
