@@ -134,7 +134,6 @@ TcPlan fwd_plan(int T, int H, int I, int E, int k, int bits, int group_size, uns
   if (flags & MQ_FWD_PATH_TENSOR_CORE) return pl;
   if (flags & MQ_FWD_PATH_LAYER) {  // 8-bit only (checked by the caller)
     pl.layer = true;
-    if (pl.bn < 64) pl.bn = 64;
     return pl;
   }
   if (flags & MQ_FWD_PATH_DECODE) {
