@@ -82,7 +82,7 @@ def test_logits_forward_mixtral_decode(mixtral, T, path):
 
 
 @pytest.mark.parametrize("path", ["auto", "tc", "decode", "layer"])
-@pytest.mark.parametrize("T", [1, 64, 512])
+@pytest.mark.parametrize("T", [1, 24, 64, 512])
 def test_logits_forward_fine_grained(T, path):
     layer = Layer(W["fine"], seed=0)
     _logits_case(layer, T, seed=30 + T, path=path)

@@ -1834,14 +1834,19 @@ TcPlan tc_plan(int T, int H, int I, int E, int k, int bits) {
   // memory for the activation ring (a shallower weight ring) and activation
   // traffic, while a smaller one streams an expert's weights once per tile
   // (the tiles of one expert run side by side, so the second pass mostly
-  // hits L2).  Up to 32 tokens: 16.  Up to 64 tokens: 32 for layers of a
+  // hits L2).  Up to 32 tokens: 16 (32 from 17 tokens in 8-bit layers of
+  // many experts, below).  Up to 64 tokens: 32 for layers of a
   // few large experts, whose loads are near-uniform (measured on the
   // Mixtral-shaped layer, E=8, at T=64: gate/up 186.3 us with 64-row tiles,
   // 178.3 us with 32-row tiles and two MMA issuers), 64 for layers of many
   // small experts, where a few experts take most tokens (fine-grained E=128
   // with Zipf routing at T=64: step 66.9 us with 64-row tiles, 69.2 us with
   // 32-row ones).  Beyond 64 tokens, 128.
-  const int bn = T > 64 ? 128 : (T > 32 ? (E <= 16 ? 32 : 64) : 16);
+  // 8-bit layers of many experts take 32-row tiles from 17 tokens (Zipf
+  // routing puts most tokens on a few experts: fine-grained T=32 step 51.5
+  // -> 46.4 us; W4A16 and the Mixtral-shaped layer lose 0.3-1 % with them).
+  const int bn = T > 64 ? 128
+                        : (T > 32 ? (E <= 16 ? 32 : 64) : (T > 16 && E > 16 && bits == 8 ? 32 : 16));
   pl.bn = bn;
   // K splits of the down GEMM.  Decode batches: the split count whose units
   // (live experts x H / 128 x splits) fill the SMs most evenly (dec_splits;
