@@ -105,7 +105,15 @@ struct TileCfg {
   // so that a step's activation tile is requested six steps ahead and its
   // L2 latency stays off the converters' path
   static constexpr int kBSlots = (kVirt == 6 && BN == 16) ? 6 : kSteps;
-  static constexpr int kThreads = (kEpiWarp0 + 4 + (kNI - 1)) * 32;
+  // converter warps per group: one per tensor-memory lane quarter, or for
+  // uint4 (SB > 0) two, each converting half of a stage's K: uint4 -> f16
+  // with the group scale costs about twice the instructions of int8 per
+  // weight, and one warp per quarter left the converters the bottleneck
+  static constexpr int kWPG = SB > 0 ? 8 : 4;
+  static constexpr int kConvW0 = kConvWarp0;
+  static constexpr int kEpiW0 = kConvW0 + kWPG * kConvGroups;  // first epilogue warp
+  static constexpr int kIss2W = kEpiW0 + 4;                    // second MMA issuer
+  static constexpr int kThreads = (kEpiW0 + 4 + (kNI - 1)) * 32;
   static constexpr int kBBytesK = BN * kBK * 2;     // activations per weight stage
   static constexpr int kBBytes = kG * kBBytesK;     // activations per MMA step
   static constexpr int kAFit = (kSmemBudget - SB - kBSlots * kBBytes) / kABytes;
@@ -132,6 +140,10 @@ struct TileCfg {
 template <int BN, int SB = 0>
 struct SyncCfg {
   static constexpr int kNI = 1;
+  static constexpr int kWPG = 4;
+  static constexpr int kConvW0 = kConvWarp0;
+  static constexpr int kEpiW0 = kEpiWarp0;
+  static constexpr int kIss2W = kIssuer2Warp;
   static constexpr int kThreads = (kEpiWarp0 + 4) * 32;
   static constexpr int kSteps = 4;
   static constexpr int kVirt = kSteps;
@@ -908,11 +920,11 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
   if (threadIdx.x == 0) {
     for (int s = 0; s < NA; ++s) {
       mbar_init(&ctl->fullA[s], 1);
-      mbar_init(&ctl->emptyA[s], 4);  // the 4 warps of the converter group
+      mbar_init(&ctl->emptyA[s], C::kWPG);  // the warps of the converter group
     }
     for (int s = 0; s < NV; ++s) {
       mbar_init(&ctl->fullB[s], 1);
-      mbar_init(&ctl->afull[s], 4);
+      mbar_init(&ctl->afull[s], C::kWPG);
       // MMA commit; warp-MMA mode: the 4 warps of the step's converter group
       mbar_init(&ctl->stepfree[s], SYNC ? 4 : 1);
     }
@@ -921,7 +933,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
       mbar_init(&ctl->accfull[s], SYNC ? 4 * kConvGroups : C::kNI);
       mbar_init(&ctl->accempty[s], 4);
       mbar_init(&ctl->fullS[s], 1);
-      mbar_init(&ctl->emptyS[s], 4 * kConvGroups);
+      mbar_init(&ctl->emptyS[s], C::kWPG * kConvGroups);
     }
     mbar_init(&ctl->drain, C::kNI);
     ctl->abort_flag = 0;
@@ -1121,7 +1133,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
     __syncwarp();
   } else if (SYNC && warp == 1) {
     // warp-MMA mode: no MMA issuer
-  } else if (warp == 1 || (C::kNI == 2 && warp == kIssuer2Warp)) {
+  } else if (warp == 1 || (C::kNI == 2 && warp == C::kIss2W)) {
     // ------------------------------------------------- MMA issuer ----
     // One thread runs this loop: it alone waits, issues and commits, so the
     // rest of the warp has nothing to agree on.  Per 256-K step: one wait
@@ -1185,21 +1197,26 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
       wait_drain(&ctl->drain, 0);
     }
     __syncwarp();
-  } else if (SYNC && warp < kEpiWarp0) {
+  } else if (SYNC && warp < C::kEpiW0) {
     if constexpr (SYNC)
       conv_sync<MODE, BITS, BN, C>(p, ulist, total, sA, sB, partials, sS, ctl, warp, lane);
   } else if (SYNC) {
     if constexpr (SYNC) epi_sync<MODE, BITS, BN, C>(p, ulist, total, partials, ctl, warp, lane);
-  } else if (warp < kEpiWarp0) {
+  } else if (warp < C::kEpiW0) {
     // -------------------------------------------------- converters ----
     // Per MMA step of this group: for each weight stage, wait for the tile
     // in this group's half of the ring, read this thread's row into
     // registers, convert it (int8: exact; uint4: (q - z) * s per group),
     // write it into the step's tensor-memory A stage and hand the slot back.
     // Then wait for the step's activations and tell the MMA issuer.
-    const int grp = (warp - kConvWarp0) >> 2;  // takes the steps with st % kConvGroups == grp
-    const int q = warp & 3;                    // tensor-memory lane quarter of this warp
+    const int cw = warp - C::kConvW0;
+    const int grp = cw / C::kWPG;  // takes the steps with st % kConvGroups == grp
+    const int q = warp & 3;        // tensor-memory lane quarter of this warp
     const int r = q * 32 + lane;
+    // uint4 with two warps per quarter: this warp's half of each stage's K
+    constexpr int NH = C::kWPG / 4;   // parts of a stage's row (1 or 2)
+    constexpr int NCH = 8 / NH;       // 16-byte chunks of its row per thread
+    const int khalf = (cw % C::kWPG) >> 2;
     const uint32_t tcol = ((uint32_t)(q * 32) << 16) + kACol0;
     int lit = 0, st = 0;  // lit: weight stages consumed by this group
     bool ok = true;
@@ -1212,7 +1229,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
       // distinct banks); down: row r
       const int i_gu = q * 16 + (lane >> 1);
       const int srow = M == 1 ? ((lane & 1) ? 64 + i_gu : i_gu) : r;
-      const int rot = (M == 1 && (lane & 1)) ? 4 : 0;
+      const int rot = (M == 1 && (lane & 1)) ? NCH / 2 : 0;
       const uint32_t sw = srow & 7;  // 128-byte swizzle phase of this row
       const bool rt = rot != 0;
       for (int u = u0, ui = 0; u < tot && ok; u += gridDim.x, ++ui) {
@@ -1243,15 +1260,16 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
           const int v = st % NV;  // their barriers
           for (int j = 0; j < nk && ok; ++j, ++lit) {
             const int sa = grp * NAG + lit % NAG;
-            uint32_t zz[8], ss[8];  // uint4: per 32-K chunk, issued before the tile wait
+            uint32_t zz[NCH], ss[NCH];  // uint4: per 32-K chunk, issued before the tile wait
             if constexpr (BITS == 4) {
               if (prm.stage) {
-                // chunk c of this 256-K stage lies in group g0 + (32 c >> log2 gs):
-                // one staged lookup per distinct group (gs is a power of two)
-                const int g0 = ((ks + j) * kEntryK) >> prm.gs_log2;
+                // chunk c of this thread's part of the 256-K stage lies in group
+                // g0 + (32 c >> log2 gs): one staged lookup per distinct group
+                // (gs is a power of two, at least 32)
+                const int g0 = ((ks + j) * kEntryK + khalf * 32 * NCH) >> prm.gs_log2;
                 const int csh = prm.gs_log2 - 5;  // chunks per group = 2^csh
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
+                for (int c = 0; c < NCH; ++c) {
                   if ((c & ((1 << csh) - 1)) == 0) {
                     const int g = g0 + (c >> csh);
                     uint32_t z = 8, sb = 0;  // past the row's end: scale 0
@@ -1268,16 +1286,18 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
                 }
               } else {
 #pragma unroll
-                for (int c = 0; c < 8; ++c)
-                  group_words(prm, wrow, (ks + j) * kEntryK + 32 * c, zz[c], ss[c]);
+                for (int c = 0; c < NCH; ++c)
+                  group_words(prm, wrow, (ks + j) * kEntryK + 32 * (khalf * NCH + c), zz[c], ss[c]);
               }
             }
             ok = warp_wait(&ctl->fullA[sa], (lit / NAG) & 1, ctl, prm.status, lane);
             if (!ok) break;
             const uint8_t* row = sA + sa * kABytes + srow * 128;
-            uint4 x[8];  // x[c] holds logical chunk (c + rot) & 7
+            // x[c] holds chunk khalf * NCH + ((c + rot) % NCH) of the row
+            uint4 x[NCH];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) x[c] = ld_chunk(row, (c + rot) & 7, sw);
+            for (int c = 0; c < NCH; ++c)
+              x[c] = ld_chunk(row, (uint32_t)(khalf * NCH + ((c + rot) & (NCH - 1))), sw);
             if (j == 0) {
               // the MMAs that last read this tensor-memory stage (step st - ND)
               // must be done
@@ -1288,7 +1308,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
               }
               tc_fence_after();
             }
-            const uint32_t tbase = tmem + tcol + d * kAColsPerStep + j * kEntryCols;
+            const uint32_t tbase = tmem + tcol + d * kAColsPerStep + j * kEntryCols + khalf * (kEntryCols / NH);
             if constexpr (BITS == 8) {
 #pragma unroll
               for (int h = 0; h < 2; ++h) {
@@ -1304,12 +1324,12 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
               }
             } else {
 #pragma unroll
-              for (int h = 0; h < 4; ++h) {
+              for (int h = 0; h < NCH / 2; ++h) {
                 uint32_t words[32];
 #pragma unroll
                 for (int c2 = 0; c2 < 2; ++c2) {
-                  const int c = 2 * h + c2;  // logical 16-byte chunk = 32 codes
-                  const uint4 v = sel4(rt, x[(c + 4) & 7], x[c]);
+                  const int c = 2 * h + c2;  // chunk of this part: 32 codes
+                  const uint4 v = sel4(rt, x[(c + NCH / 2) & (NCH - 1)], x[c]);
                   uint4x8_to_f16(v.x, zz[c], ss[c], &words[c2 * 16 + 0]);
                   uint4x8_to_f16(v.y, zz[c], ss[c], &words[c2 * 16 + 4]);
                   uint4x8_to_f16(v.z, zz[c], ss[c], &words[c2 * 16 + 8]);
