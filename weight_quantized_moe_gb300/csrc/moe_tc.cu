@@ -1311,12 +1311,14 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
             const uint32_t tbase = tmem + tcol + d * kAColsPerStep + j * kEntryCols + khalf * (kEntryCols / NH);
             if constexpr (BITS == 8) {
 #pragma unroll
-              for (int h = 0; h < 2; ++h) {
+              for (int h = 0; h < NCH / 4; ++h) {
                 uint32_t words[32];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                  // logical chunk 4h + c sits in x[4h + c] (rot 0) or x[(4h + c + 4) & 7] (rot 4)
-                  const uint4 cv = sel4(rt, x[(4 * h + c + 4) & 7], x[4 * h + c]);
+                  // chunk 4h + c of this part sits in x[4h + c] (rot 0) or
+                  // x[(4h + c + NCH / 2) % NCH] (rotated)
+                  const int cl = 4 * h + c;
+                  const uint4 cv = sel4(rt, x[(cl + NCH / 2) & (NCH - 1)], x[cl]);
                   if constexpr (kBf16M) convert16_bf16(cv, prm.xmask, zf8, &words[c * 8]);
                   else convert16(cv, prm.xmask, zz8, &words[c * 8]);
                 }
