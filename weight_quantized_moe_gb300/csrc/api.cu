@@ -152,6 +152,13 @@ TcPlan fwd_plan(int T, int H, int I, int E, int k, int bits, int group_size, uns
   // layers of many experts (measured rule above)
   (void)ok;
   if (bits == 8 && pl.bn >= 64 && layer_default(T, E)) pl.layer = true;
+  // 8-bit down GEMM on f16 operands after the in-place act -> f16 pass, for
+  // layers of a few experts at 8-64 tokens: the f16 conversion of the codes
+  // takes about half the instructions of bf16, which outweighs the pass
+  // (Mixtral-shaped step T=64 248.3 -> 240.7 us, T=8 218.7 -> 213.1 us; T=1
+  // 79.5 -> 81.9, fine-grained T=64 51.9 -> 57.4, prefill T=4096 2456 ->
+  // 2556 us, where the pass costs more than it saves)
+  if (bits == 8 && !pl.layer && E <= 16 && T >= 8 && T <= 64) pl.f16down = true;
   return pl;
 }
 
@@ -555,9 +562,10 @@ static int forward_impl(const void* x, int T, int H, int I, int E, int k, int bi
   }
   if (err != cudaSuccess) return cuda_fail(err, "forward: gate/up GEMM launch");
   float* act_inv = reinterpret_cast<float*>(ws + L.act_inv);
-  if (bits == 4 && !plan.sync2) {
-    // the tcgen05 uint4 down GEMM runs f16 operands; the 8-bit one and the
-    // warp-MMA mode read bf16 act
+  if ((bits == 4 && !plan.sync2) || plan.f16down) {
+    // the tcgen05 uint4 down GEMM runs f16 operands (and the 8-bit one where
+    // the plan says so); otherwise the 8-bit one and the warp-MMA mode read
+    // bf16 act
     LaunchScope ls(MQ_PROF_ACTF16, st);
     err = launch_act_to_f16(a, act_inv, st);
     if (err != cudaSuccess) return cuda_fail(err, "forward: act conversion launch");

@@ -166,6 +166,7 @@ struct TcPlan {
   bool sync1;  // gate/up GEMM: warp-MMA consumers (few tokens per expert), not tcgen05
   bool sync2;  // down GEMM: the same
   bool layer;  // 8-bit, tcgen05: both GEMMs in one launch (moe_layer_tc)
+  bool f16down;  // 8-bit, two launches: act to f16 in place, f16 down GEMM
 };
 MQ_HIDDEN TcPlan tc_plan(int T, int H, int I, int E, int k, int bits);
 MQ_HIDDEN int tc_num_sms();

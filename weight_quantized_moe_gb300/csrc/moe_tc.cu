@@ -218,6 +218,9 @@ struct TcParams {
   // for dep_target of them
   int* dep;
   int dep_target;
+  // 8-bit down GEMM: act was converted to f16 in place (exact, with the row
+  // scales in xinv), so the weights are converted to f16 as well
+  int down_f16;
   unsigned* status;
 };
 
@@ -866,7 +869,7 @@ __device__ __forceinline__ void epi_sync(const TcParams& p, const int4* ulist, i
 // its down units: a down unit only waits for gate/up units, which wait for
 // nothing outside their CTA, so every wait ends once all CTAs are resident
 // (one CTA per SM, grid <= SMs).
-template <int MODE, int BITS, int BN, bool SYNC, bool FUSED>
+template <int MODE, int BITS, int BN, bool SYNC, bool FUSED, bool F16D>
 __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensorMap& tmB,
                                           const TcParams& p, const CUtensorMap& tmA2,
                                           const CUtensorMap& tmB2, const TcParams& p2) {
@@ -1153,7 +1156,11 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
       phases([&](auto ph_tag, const TcParams& prm, const CUtensorMap& mA, const CUtensorMap& mB,
                const int4* ul, int tot, int u0) {
         constexpr int M = decltype(ph_tag)::value;
-        constexpr uint32_t kIdescM = (M == 2 && (BITS == 8 || SYNC)) ? idesc_bf16_f32(kTileM, BN) : idesc_f16_f32(kTileM, BN);
+        // operand type: bf16 in the 8-bit down GEMM (unless act was converted
+        // to f16 in place: F16D) and in the warp-MMA mode, else f16
+        constexpr uint32_t kIdescM = (M == 2 && (BITS == 8 || SYNC) && !F16D)
+                                         ? idesc_bf16_f32(kTileM, BN)
+                                         : idesc_f16_f32(kTileM, BN);
         for (int u = u0, ui = 0; u < tot && ok; u += gridDim.x, ++t, ++ui) {
           const Unit w = cta_unit<BN>(prm, ul, ui, u, kUL);
           const int ks0 = w.split * prm.ksteps / prm.splits;
@@ -1223,7 +1230,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
     phases([&](auto ph_tag, const TcParams& prm, const CUtensorMap& mA, const CUtensorMap& mB,
                const int4* ul, int tot, int u0) {
       constexpr int M = decltype(ph_tag)::value;
-      constexpr bool kBf16M = M == 2 && (BITS == 8 || SYNC);
+      constexpr bool kBf16M = M == 2 && (BITS == 8 || SYNC) && !F16D;
       // this thread's row of the weight tile: gate/up lanes (2i, 2i+1) hold
       // gate row i and up row i (rotated read order keeps the pair on
       // distinct banks); down: row r
@@ -1310,20 +1317,25 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
             }
             const uint32_t tbase = tmem + tcol + d * kAColsPerStep + j * kEntryCols + khalf * (kEntryCols / NH);
             if constexpr (BITS == 8) {
+              // the stage's codes as 16-bit words (bf16 or f16), into tensor memory
+              auto conv8 = [&](auto bf) {
+                constexpr bool kB = decltype(bf)::value;
 #pragma unroll
-              for (int h = 0; h < NCH / 4; ++h) {
-                uint32_t words[32];
+                for (int h = 0; h < NCH / 4; ++h) {
+                  uint32_t words[32];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                  // chunk 4h + c of this part sits in x[4h + c] (rot 0) or
-                  // x[(4h + c + NCH / 2) % NCH] (rotated)
-                  const int cl = 4 * h + c;
-                  const uint4 cv = sel4(rt, x[(cl + NCH / 2) & (NCH - 1)], x[cl]);
-                  if constexpr (kBf16M) convert16_bf16(cv, prm.xmask, zf8, &words[c * 8]);
-                  else convert16(cv, prm.xmask, zz8, &words[c * 8]);
+                  for (int c = 0; c < 4; ++c) {
+                    // chunk 4h + c of this part sits in x[4h + c] (rot 0) or
+                    // x[(4h + c + NCH / 2) % NCH] (rotated)
+                    const int cl = 4 * h + c;
+                    const uint4 cv = sel4(rt, x[(cl + NCH / 2) & (NCH - 1)], x[cl]);
+                    if constexpr (kB) convert16_bf16(cv, prm.xmask, zf8, &words[c * 8]);
+                    else convert16(cv, prm.xmask, zz8, &words[c * 8]);
+                  }
+                  tmem_st32(tbase + h * 32, words);
                 }
-                tmem_st32(tbase + h * 32, words);
-              }
+              };
+              conv8(std::integral_constant<bool, kBf16M>{});
             } else {
 #pragma unroll
               for (int h = 0; h < NCH / 2; ++h) {
@@ -1382,7 +1394,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
                const int4* ul, int tot, int u0) {
       constexpr int M = decltype(ph_tag)::value;
       constexpr int CHM = M == 1 ? 16 : CH;
-      constexpr bool kBf16M = M == 2 && (BITS == 8 || SYNC);
+      constexpr bool kBf16M = M == 2 && (BITS == 8 || SYNC) && !F16D;
       for (int u = u0, ui = 0; u < tot && ok; u += gridDim.x, ++t, ++ui) {
         const Unit w = cta_unit<BN>(prm, ul, ui, u, kUL);
         const int buf = t & 1;
@@ -1549,12 +1561,13 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
   }
 }
 
-// One expert GEMM (MODE 1 gate/up, 2 down).
-template <int MODE, int BITS, int BN, bool SYNC>
+// One expert GEMM (MODE 1 gate/up, 2 down).  F16D: the 8-bit down GEMM on
+// f16 operands (act converted to f16 in place beforehand).
+template <int MODE, int BITS, int BN, bool SYNC, bool F16D = false>
 __global__ void __launch_bounds__(CfgOf<MODE, BITS, BN, SYNC>::kThreads, 1)
     moe_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ TcParams p) {
-  gemm_body<MODE, BITS, BN, SYNC, false>(tmA, tmB, p, tmA, tmB, p);
+  gemm_body<MODE, BITS, BN, SYNC, false, F16D>(tmA, tmB, p, tmA, tmB, p);
 }
 
 // Both expert GEMMs of an 8-bit layer in one launch (FUSED above).
@@ -1563,7 +1576,7 @@ __global__ void __launch_bounds__(CfgOf<1, 8, BN, false>::kThreads, 1)
     moe_layer_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap tmA2,
                  const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ TcParams p2) {
-  gemm_body<1, 8, BN, false, true>(tmA, tmB, p, tmA2, tmB2, p2);
+  gemm_body<1, 8, BN, false, true, false>(tmA, tmB, p, tmA2, tmB2, p2);
 }
 
 // Rows of x gathered into expert-sorted order as f16, each scaled by a power
@@ -1806,12 +1819,12 @@ constexpr size_t smem_for() {
   return need < 120 * 1024 ? 120 * 1024 : need;
 }
 
-template <int MODE, int BITS, int BN, bool SYNC>
+template <int MODE, int BITS, int BN, bool SYNC, bool F16D = false>
 cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const TcParams& p,
                         int max_units, cudaStream_t st) {
   constexpr size_t smem = smem_for<MODE, BITS, BN, SYNC>();
   static_assert(smem <= 227 * 1024, "shared memory");
-  auto kern = moe_gemm_tc<MODE, BITS, BN, SYNC>;
+  auto kern = moe_gemm_tc<MODE, BITS, BN, SYNC, F16D>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   const int sms = tc_num_sms();
@@ -1830,6 +1843,13 @@ cudaError_t launch_gemm_bn(int bn, bool sync, const CUtensorMap& ta, const CUten
     if constexpr (BITS == 8)
       if (bn == 32) return launch_gemm<MODE, BITS, 32, true>(ta, tb, p, max_units, st);
     return cudaErrorInvalidValue;
+  }
+  if constexpr (MODE == 2 && BITS == 8) {
+    if (p.down_f16) {  // f16 operands: 16- and 32-row tiles (batches of 8-64 tokens)
+      if (bn == 16) return launch_gemm<2, 8, 16, false, true>(ta, tb, p, max_units, st);
+      if (bn == 32) return launch_gemm<2, 8, 32, false, true>(ta, tb, p, max_units, st);
+      return cudaErrorInvalidValue;
+    }
   }
   switch (bn) {
     case 16: return launch_gemm<MODE, BITS, 16, false>(ta, tb, p, max_units, st);
@@ -1850,6 +1870,7 @@ TcPlan tc_plan(int T, int H, int I, int E, int k, int bits) {
   TcPlan pl;
   pl.sync1 = pl.sync2 = false;
   pl.layer = false;
+  pl.f16down = false;
   const int64_t S = (int64_t)T * k;
   // Token-slots per tile at most (the MMA's N).  A tile is cut from one
   // expert's segment with the rows it has, so a larger bound costs shared
@@ -1932,6 +1953,7 @@ void common_params(TcParams& p, const MoeArgs& a) {
   p.xinv = nullptr;
   p.dep = nullptr;
   p.dep_target = 0;
+  p.down_f16 = 0;
   p.scale = nullptr;
   p.gscale = nullptr;
   p.gzero = nullptr;
@@ -2029,8 +2051,8 @@ cudaError_t prep_gemm2(const MoeArgs& a, const TcPlan& pl, const float* act_inv,
     const cuuint32_t box[2] = {64, (cuuint32_t)pl.bn};
     // act: bf16 as written by the gate/up GEMM (8-bit, and uint4 in warp-MMA
     // mode), or f16 after the in-place conversion (uint4, tensor cores)
-    err = make_map(&tb, (a.bits == 8 || pl.sync2) ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                                 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+    err = make_map(&tb, ((a.bits == 8 && !pl.f16down) || pl.sync2) ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                    2, a.act, dims, strides, box,
                    CU_TENSOR_MAP_SWIZZLE_128B);
     if (err != cudaSuccess) return err;
@@ -2050,6 +2072,7 @@ cudaError_t prep_gemm2(const MoeArgs& a, const TcPlan& pl, const float* act_inv,
   }
   p.ypart = ypart;
   p.xinv = act_inv;
+  p.down_f16 = (a.bits == 8 && pl.f16down && !pl.sync2) ? 1 : 0;
   const int64_t units = (a.cap / a.bm) * (int64_t)p.MT * p.splits;
   mu = (int)(units < (1 << 30) ? units : (1 << 30));
   return cudaSuccess;
@@ -2090,7 +2113,8 @@ cudaError_t launch_gemm2_tc(const MoeArgs& a, const TcPlan& pl, const float* act
 
 cudaError_t launch_layer_tc(const MoeArgs& a, const TcPlan& pl, const void* xs,
                             const float* xinv, float* ypart, cudaStream_t st) {
-  if (a.bits != 8 || pl.sync1 || pl.sync2 || a.dep == nullptr) return cudaErrorInvalidValue;
+  if (a.bits != 8 || pl.sync1 || pl.sync2 || pl.f16down || a.dep == nullptr)
+    return cudaErrorInvalidValue;
   CUtensorMap ta, tb, ta2, tb2;
   TcParams p, p2;
   int mu1 = 0, mu2 = 0;
