@@ -278,7 +278,8 @@ int moe_quant_forward(const void* x, int T, int H, int I, int E, int k,
  * streams its gate/up weight tiles and then its down weight tiles without a
  * kernel boundary, and the down GEMM of a token tile starts as soon as all
  * gate/up tiles of that token tile are done.  By default that launch serves
- * 8-bit batches of 65 to 2048 tokens in layers of more than 16 experts.  It relies on all of its CTAs (one per SM, at most the
+ * 8-bit batches of 65 to 2048 tokens in layers of more than 16 experts, and
+ * of one or two tokens in layers of up to 16 experts.  It relies on all of its CTAs (one per SM, at most the
  * SM count) becoming resident together, as they do unless kernels of other
  * streams hold SMs for longer than a second; its waits on other CTAs give
  * up after a second with MQ_DEV_WAIT_TIMEOUT.

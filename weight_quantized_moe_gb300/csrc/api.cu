@@ -125,8 +125,12 @@ constexpr int kAlignBlock = 16;
 // of many small experts with 128-row token tiles, where each GEMM alone runs
 // few MMA steps per SM.  At T=64 (64-row tiles) both take 59-60 us, at
 // T=4096 both 574 us; Mixtral-shaped layers (E=8) lose with it (T=64: 291 ->
-// 305 us, as 64-row tiles replace the 32-row ones).
-bool layer_default(int T, int E) { return E > 16 && T > 64 && T <= 2048; }
+// 305 us, as 64-row tiles replace the 32-row ones).  For one or two tokens
+// in layers of a few experts the down GEMM's start-up hides behind the
+// gate/up GEMM's tail: Mixtral-shaped T=1 step 79.6 -> 76.5 us (L2 flushed:
+// 90.7 -> 85.3), T=2 80.1 -> 77.7 us; from T=4 on two launches are as fast
+// or faster.
+bool layer_default(int T, int E) { return E > 16 ? (T > 64 && T <= 2048) : T <= 2; }
 
 TcPlan fwd_plan(int T, int H, int I, int E, int k, int bits, int group_size, unsigned flags) {
   TcPlan pl = tc_plan(T, H, I, E, k, bits);
@@ -151,7 +155,7 @@ TcPlan fwd_plan(int T, int H, int I, int E, int k, int bits, int group_size, uns
   // default: tcgen05 for both GEMMs; one launch for both GEMMs of 8-bit
   // layers of many experts (measured rule above)
   (void)ok;
-  if (bits == 8 && pl.bn >= 64 && layer_default(T, E)) pl.layer = true;
+  if (bits == 8 && layer_default(T, E)) pl.layer = true;
   // 8-bit down GEMM on f16 operands after the in-place act -> f16 pass, for
   // layers of a few experts at 8-64 tokens: the f16 conversion of the codes
   // takes about half the instructions of bf16, which outweighs the pass
