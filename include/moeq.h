@@ -414,6 +414,20 @@ long long mq_kernel_launch_count(void);
 int mq_profile_enable(int on);
 int mq_profile_read(double* total_ms, long long* launches, int n_slots);
 
+/*
+ * Testing aid for the bounded waits (no counterpart on the pages).
+ * mq_test_layer_wait_extra(extra): adds `extra` (>= 0) to the number of
+ *   gate/up completions that each down unit of the one-launch layer
+ *   (MQ_FWD_PATH_LAYER) waits for, in later launches.  With extra > 0 those
+ *   waits cannot end: after their limit of about a second the kernel stops
+ *   its CTAs cleanly, the forward's output is invalid and
+ *   mq_device_status reports MQ_DEV_WAIT_TIMEOUT; later forwards run
+ *   normally.  0 restores normal operation.  Returns MQ_OK, or
+ *   MQ_ERR_INVALID_ARG for extra < 0.  Process-wide; not for concurrent
+ *   forwards.
+ */
+int mq_test_layer_wait_extra(int extra);
+
 #ifdef __cplusplus
 }
 #endif

@@ -101,6 +101,9 @@ def test_host_side_rejections(lib):
     assert lib.moe_align_block(fake, 4, 2, 8, 16, fake, fake, fake, fake, 8, None) == 1
     assert lib.moe_quant_forward_workspace(4, 128, 128, 8, 2, 8, -1) > 0
     assert lib.moe_quant_forward_workspace(4, 128, 128, 8, 2, 3, -1) == 0
+    # the bounded-wait testing hook takes extra >= 0 (0 restores)
+    assert lib.mq_test_layer_wait_extra(-1) == 1
+    assert lib.mq_test_layer_wait_extra(0) == 0
 
 
 def test_route_options_rejections(lib):

@@ -11,6 +11,7 @@ from .binding import (  # noqa: F401
     mq_device_status,
     mq_kernel_launch_count,
     mq_profile_enable,
+    mq_test_layer_wait_extra,
     mq_profile_read,
     mq_status_string,
     moe_align_block,

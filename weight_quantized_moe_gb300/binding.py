@@ -74,6 +74,7 @@ _SIGNATURES = {
     "moe_quant_forward_noalloc": (_i32, [_vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
                                          _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "mq_kernel_launch_count": (ctypes.c_longlong, []),
+    "mq_test_layer_wait_extra": (_i32, [_i32]),
     "mq_profile_enable": (_i32, [_i32]),
     "mq_profile_read": (_i32, [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_longlong), _i32]),
 }
@@ -139,6 +140,13 @@ def _need(t, dtype, name, ndim=None):
 def mq_kernel_launch_count() -> int:
     """Kernels launched by the library in this process so far."""
     return int(lib().mq_kernel_launch_count())
+
+
+def mq_test_layer_wait_extra(extra: int) -> None:
+    """Testing aid (moeq.h): with extra > 0 the one-launch layer's down
+    units wait for gate/up completions that never come, and their bounded
+    waits run out; 0 restores normal operation."""
+    _check(lib().mq_test_layer_wait_extra(int(extra)))
 
 
 def mq_profile_enable(on: bool) -> None:

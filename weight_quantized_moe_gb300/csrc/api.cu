@@ -234,6 +234,12 @@ MQ_EXPORT const char* mq_last_error_message(void) { return g_msg; }
 
 MQ_EXPORT long long mq_kernel_launch_count(void) { return g_launches.load(); }
 
+MQ_EXPORT int mq_test_layer_wait_extra(int extra) {
+  if (extra < 0) return fail(MQ_ERR_INVALID_ARG, "extra must be >= 0");
+  set_layer_wait_extra(extra);
+  return MQ_OK;
+}
+
 MQ_EXPORT int mq_profile_enable(int on) {
   g_prof_on.store(on ? 1 : 0);
   return MQ_OK;

@@ -182,6 +182,9 @@ MQ_HIDDEN cudaError_t launch_combine_splits(const MoeArgs& a, const float* ypart
 // rows): act and the down GEMM's partial sums as the two launches write them.
 MQ_HIDDEN cudaError_t launch_layer_tc(const MoeArgs& a, const TcPlan& pl, const void* xs,
                                       const float* xinv, float* ypart, cudaStream_t st);
+// Testing aid: extra gate/up completions the layer's down units wait for
+// (their waits then run out); returns the previous value.
+MQ_HIDDEN int set_layer_wait_extra(int extra);
 
 // Warp-MMA ("decode") mode of the expert GEMMs: the formats it takes, and
 // the K splits of its down GEMM.

@@ -30,6 +30,7 @@
 
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cmath>
 #include <mutex>
 #include <type_traits>
@@ -2111,6 +2112,12 @@ cudaError_t launch_gemm2_tc(const MoeArgs& a, const TcPlan& pl, const float* act
                      : launch_gemm_bn<2, 4>(pl.bn, pl.sync2, ta, tb, p, mu, st);
 }
 
+namespace {
+std::atomic<int> g_layer_wait_extra{0};
+}  // namespace
+
+int set_layer_wait_extra(int extra) { return g_layer_wait_extra.exchange(extra); }
+
 cudaError_t launch_layer_tc(const MoeArgs& a, const TcPlan& pl, const void* xs,
                             const float* xinv, float* ypart, cudaStream_t st) {
   if (a.bits != 8 || pl.sync1 || pl.sync2 || pl.f16down || a.dep == nullptr)
@@ -2125,7 +2132,7 @@ cudaError_t launch_layer_tc(const MoeArgs& a, const TcPlan& pl, const void* xs,
   // each gate/up unit's 4 epilogue warps count once per token tile
   p.dep = a.dep;
   p2.dep = a.dep;
-  p2.dep_target = 4 * p.MT;
+  p2.dep_target = 4 * p.MT + g_layer_wait_extra.load();
   const int64_t mu = (int64_t)mu1 + mu2;
   const int m = (int)(mu < (1 << 30) ? mu : (1 << 30));
   switch (pl.bn) {
