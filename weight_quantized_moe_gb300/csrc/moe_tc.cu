@@ -19,8 +19,11 @@
 // * Accumulators live in tensor memory, double-buffered across work units.
 // * One persistent CTA per SM walks the work units (expert block, weight
 //   tile, K split).  Warp roles: 0 weight producer (TMA), 1 MMA issuer,
-//   2 activation producer (TMA), 3-10 two converter warpgroups taking
-//   alternate MMA steps, 11-14 epilogue.
+//   2 activation producer (TMA, and the uint4 scale staging), then two
+//   converter groups taking alternate MMA steps (3-10; uint4: 3-18, two
+//   warps per tensor-memory lane quarter), then 4 epilogue warps, then the
+//   second MMA issuer of 16- and 32-token tiles.  The one-launch layer
+//   (moe_layer_tc) runs the gate/up and the down GEMM in one kernel.
 // * Every mbarrier wait is bounded: after kWaitNs the CTA flags
 //   MQ_DEV_WAIT_TIMEOUT, stops issuing work, drains its own copies and MMAs
 //   (with a bound again), frees its tensor memory and exits.
@@ -71,8 +74,9 @@ inline bool stage_fits(int G) { return 128 * G * 2 + 64 * G <= kStageBytes; }
 //   stages (16 MMAs): the wait and commit around a step cost several MMAs'
 //   worth of issue time, so a step batches 16 of them.
 // * Tensor memory holds two accumulator buffers and kSteps converted-A
-//   stages of kG * 64 columns; the activation ring has the same depth, and
-//   one MMA commit per step frees both.
+//   stages of kG * 64 columns; the activation ring has kBSlots slots (as
+//   many, or six for 16-token tiles), and one MMA commit per step frees a
+//   stage and a slot.
 // * One tcgen05.mma takes about 80 cycles to issue whatever N is, and the
 //   issuing thread's wait and commit around each 16-MMA step add about a
 //   third to that; two threads issuing at once reach twice the rate.  For
