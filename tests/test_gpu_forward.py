@@ -168,13 +168,17 @@ def test_forward_mixtral_decode_sampled():
     assert _run(layer, 64, seed=0, tokens=[5, 40], out_cols=cols) <= FWD_TOL
 
 
-@pytest.mark.parametrize("name,T,tokens", [("mixtral_prefill", 4096, [0, 2047, 4095]),
+@pytest.mark.parametrize("name,T,tokens", [("mixtral_prefill", 1024, [0, 511, 1023]),
+                                           ("mixtral_prefill", 4096, [0, 2047, 4095]),
+                                           ("mixtral_prefill", 8192, [0, 5000, 8191]),
                                            ("fine", 4096, [1, 3000]),
                                            ("w4a16", 2048, [5, 2047])])
 def test_forward_prefill_sizes_sampled(name, T, tokens):
-    """The prefill-sized layers in the benchmark's launch configuration
-    (128-token tiles, no K split, the eight-slot combine): sampled tokens and
-    512 sampled output columns against the oracle."""
+    """The prefill-sized layers in their default launch configuration
+    (128-token tiles; the down GEMM split over K in two at T=1024 on the
+    Mixtral-shaped layer, unsplit beyond; 16,384 token-slots sorted at
+    T=8192): sampled tokens and 512 sampled output columns against the
+    oracle."""
     layer = Layer(W[name], seed=0)
     cols = np.sort(np.random.default_rng(T).choice(layer.H, 512, replace=False))
     assert _run(layer, T, seed=5, tokens=tokens, out_cols=cols) <= FWD_TOL
