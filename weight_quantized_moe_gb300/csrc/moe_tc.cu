@@ -73,7 +73,8 @@ inline bool stage_fits(int G) { return 128 * G * 2 + 64 * G <= kStageBytes; }
 // * Synchronisation with the MMA issuer happens per MMA step of kG weight
 //   stages (16 MMAs): the wait and commit around a step cost several MMAs'
 //   worth of issue time, so a step batches 16 of them.
-// * Tensor memory holds two accumulator buffers and kSteps converted-A
+// * Tensor memory holds two accumulator buffers (one, below, for uint4
+//   64-token tiles) and kSteps converted-A
 //   stages of kG * 64 columns; the activation ring has kBSlots slots (as
 //   many, or six for 16-token tiles), and one MMA commit per step frees a
 //   stage and a slot.
@@ -89,10 +90,23 @@ inline bool stage_fits(int G) { return 128 * G * 2 + 64 * G <= kStageBytes; }
 //   launch at T=64 took 184 us against 163 us with three; the 8-bit down
 //   GEMM kept one issuer then (its bf16 conversion needed a third stage),
 //   and with three stages two issuers serve it too (T=64: 106 -> 99 us).
+// * uint4 64-token tiles take two issuers as well.  Two accumulator buffers
+//   of two halves would leave room for two stages only, so they keep one
+//   buffer and three stages: the MMAs of a unit wait for the epilogue of the
+//   previous one, which costs less than a lone issuer's wait and commit per
+//   step (W4A16 E=64 at T=64: gate/up 100.8 -> 90.2 us, down 57.5 -> 53.3
+//   us).  8-bit 64-token tiles keep one issuer and two buffers: their down
+//   GEMM in the fine-grained layer (K = 768, three steps per unit) went from
+//   22.5 to 28.5 us with one buffer.
 template <int BN, int NI, int SB = 0>
 struct TileCfg {
   static constexpr int kNI = NI;                // MMA issuer threads
-  static constexpr int kACol0 = 2 * kNI * BN;   // two accumulator buffers of kNI halves
+  // accumulator buffers of kNI halves: two (the epilogue of a unit overlaps
+  // the next unit's MMAs), or one where two would leave two issuers fewer
+  // than three stages (64-row tiles)
+  static constexpr int kAccBufs =
+      (kNI == 2 && 2 * kNI * BN + 3 * kAColsPerStep > (int)kTmemCols) ? 1 : 2;
+  static constexpr int kACol0 = kAccBufs * kNI * BN;
   static constexpr int kStepFit = ((int)kTmemCols - kACol0) / kAColsPerStep;
   // one issuer: as many stages as fit (at most kMaxSteps); two issuers:
   // three where they fit, so that a converter group's next step can be
@@ -145,6 +159,7 @@ struct TileCfg {
 template <int BN, int SB = 0>
 struct SyncCfg {
   static constexpr int kNI = 1;
+  static constexpr int kAccBufs = 2;
   static constexpr int kWPG = 4;
   static constexpr int kConvW0 = kConvWarp0;
   static constexpr int kEpiW0 = kEpiWarp0;
@@ -168,7 +183,7 @@ struct SyncCfg {
 
 template <int MODE, int BITS, int BN, bool SYNC>
 struct CfgSel {
-  using type = TileCfg<BN, BN <= 32 ? 2 : 1,
+  using type = TileCfg<BN, (BN <= 32 || (BN == 64 && BITS == 4)) ? 2 : 1,
                        BITS == 4 ? 2 * kStageBytes : 0>;
 };
 template <int MODE, int BITS, int BN>
@@ -1170,8 +1185,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
           const Unit w = cta_unit<BN>(prm, ul, ui, u, kUL);
           const int ks0 = w.split * prm.ksteps / prm.splits;
           const int ks1 = (w.split + 1) * prm.ksteps / prm.splits;
-          const int buf = t & 1;
-          ok = wait_bounded(&ctl->accempty[buf], ((t >> 1) & 1) ^ 1, ctl, prm.status);
+          const int buf = t % C::kAccBufs;
+          ok = wait_bounded(&ctl->accempty[buf], ((t / C::kAccBufs) & 1) ^ 1, ctl, prm.status);
           if (!ok) break;
           tc_fence_after();
           const uint32_t d_tmem = tmem + (buf * C::kNI + ip) * BN;
@@ -1402,7 +1417,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
       constexpr bool kBf16M = M == 2 && (BITS == 8 || SYNC) && !F16D;
       for (int u = u0, ui = 0; u < tot && ok; u += gridDim.x, ++t, ++ui) {
         const Unit w = cta_unit<BN>(prm, ul, ui, u, kUL);
-        const int buf = t & 1;
+        const int buf = t % C::kAccBufs;
         const int nsteps = ((w.split + 1) * prm.ksteps / prm.splits - w.split * prm.ksteps / prm.splits + kGA - 1) / kGA;
         // two issuers: both halves hold partial sums when the unit has two or
         // more steps; with one step only half (first step % 2) was written
@@ -1450,7 +1465,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
             srow_g = (int64_t)w.e * prm.H + w.mt * kTileM + r;
           sc_pre = load_scale(prm, prm.scale_per_tensor ? w.e : srow_g);
         }
-        if (!warp_wait_sleepy(&ctl->accfull[buf], (t >> 1) & 1, ctl, prm.status, lane)) {
+        if (!warp_wait_sleepy(&ctl->accfull[buf], (t / C::kAccBufs) & 1, ctl, prm.status, lane)) {
           ok = false;
           break;
         }
