@@ -118,6 +118,20 @@ def test_forward_w4a16_group_sizes(gs, zp, H, I):
     assert _run(layer, 20, seed=gs) <= FWD_TOL
 
 
+@pytest.mark.parametrize("E,k,H,I,gs,zp,T", [(6, 2, 256, 384, 128, True, 48),
+                                              (20, 4, 384, 256, 64, True, 40),
+                                              (20, 3, 640, 384, 128, False, 64)])
+def test_forward_w4a16_tile_shapes(E, k, H, I, gs, zp, T):
+    """uint4 32-row tiles (up to 16 experts, 33-64 tokens) and 64-row tiles
+    (more experts): two issuers on two accumulator buffers, or on one buffer
+    with three tensor-memory stages; units of one, two and three MMA steps,
+    the last stage of a unit half-filled (K = 384, 640)."""
+    wl = synth.Workload(f"w4a16_E{E}_T{T}", E=E, k=k, H=H, I=I, Ts=(T,), bits=4, group_size=gs,
+                        has_zp=zp)
+    layer = Layer(wl, seed=E + T)
+    assert _run(layer, T, seed=T) <= FWD_TOL
+
+
 def test_forward_w4a16_full_sampled():
     """The full W4A16 layer (E=64, k=6, H=2048, I=1408, gs=128) at T=32."""
     layer = Layer(W["w4a16"], seed=0)
