@@ -132,6 +132,16 @@ def test_forward_w4a16_tile_shapes(E, k, H, I, gs, zp, T):
     assert _run(layer, T, seed=T) <= FWD_TOL
 
 
+@pytest.mark.parametrize("T", [24, 40, 100])
+def test_forward_int8_tile_shapes_many_experts(T):
+    """8-bit layer of 20 experts (more than 16) with K = 384 and 640 (a
+    half-filled last stage): 32-row tiles from 17 tokens, 64-row tiles from
+    33, 128-row tiles (one launch for both GEMMs) beyond 64."""
+    wl = synth.Workload(f"int8_E20_T{T}", E=20, k=4, H=384, I=640, Ts=(T,))
+    layer = Layer(wl, seed=T)
+    assert _run(layer, T, seed=T + 1) <= FWD_TOL
+
+
 def test_forward_w4a16_full_sampled():
     """The full W4A16 layer (E=64, k=6, H=2048, I=1408, gs=128) at T=32."""
     layer = Layer(W["w4a16"], seed=0)
