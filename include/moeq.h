@@ -273,16 +273,17 @@ int moe_quant_forward(const void* x, int T, int H, int I, int E, int k,
  * token-slots, on warp-level MMAs issued by the converter warps themselves.
  * By default both GEMMs run on tcgen05 (the faster choice measured on GB300
  * for every GEMM and batch size); the warp-level MMAs run when forced.
- * For 8-bit layers of many small experts both GEMMs can run in one
- * persistent launch on tcgen05 (token tiles of 64 or 128 rows): each SM
- * streams its gate/up weight tiles and then its down weight tiles without a
- * kernel boundary, and the down GEMM of a token tile starts as soon as all
+ * For 8-bit layers both GEMMs can also run in one persistent launch on
+ * tcgen05 (token tiles of 16, 32, 64 or 128 rows, as in two launches): each
+ * SM streams its gate/up weight tiles and then its down weight tiles without
+ * a kernel boundary, and the down GEMM of a token tile starts as soon as all
  * gate/up tiles of that token tile are done.  By default that launch serves
  * 8-bit batches of 65 to 2048 tokens in layers of more than 16 experts, and
- * of one or two tokens in layers of up to 16 experts.  It relies on all of its CTAs (one per SM, at most the
- * SM count) becoming resident together, as they do unless kernels of other
- * streams hold SMs for longer than a second; its waits on other CTAs give
- * up after a second with MQ_DEV_WAIT_TIMEOUT.
+ * of one or two tokens in layers of up to 16 experts.  It relies on all of
+ * its CTAs (one per SM, at most the SM count) becoming resident together,
+ * as they do unless kernels of other streams hold SMs for longer than a
+ * second; its waits on other CTAs give up after a second with
+ * MQ_DEV_WAIT_TIMEOUT.
  * MQ_FWD_PATH_TENSOR_CORE forces tcgen05 for both GEMMs in two launches,
  * MQ_FWD_PATH_DECODE the warp-level MMAs for both (MQ_ERR_UNSUPPORTED for
  * uint4 with group_size 32 or 64), MQ_FWD_PATH_LAYER the one-launch layer
