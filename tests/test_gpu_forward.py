@@ -94,6 +94,32 @@ def test_forward_empty_batch(tiny):
     assert tiny.forward(x, tw, tid).shape == (0, 128)
 
 
+@pytest.mark.parametrize("path", ["auto", "tc", "decode", "layer"])
+def test_logits_forward_empty_batch(tiny, path):
+    """T = 0 through the one-call forward on every path: an empty output,
+    no launch that reads a token, and a clean device status."""
+    x = torch.zeros(0, tiny.H, dtype=torch.bfloat16, device="cuda")
+    lg = torch.zeros(0, tiny.E, dtype=torch.float32, device="cuda")
+    out = mq.moe_quant_forward_logits(x, lg, tiny.q13, tiny.q2, tiny.s13, tiny.s2, tiny.k, True,
+                                      path=path)
+    torch.cuda.synchronize()
+    assert out.shape == (0, tiny.H)
+    assert mq.mq_device_status() == 0
+
+
+def test_forward_empty_batch_uint4():
+    wl = synth.Workload("w4a16_empty", E=6, k=2, H=256, I=384, Ts=(0,), bits=4, group_size=128,
+                        has_zp=True)
+    layer = Layer(wl, seed=5)
+    x = torch.zeros(0, wl.H, dtype=torch.bfloat16, device="cuda")
+    tw = torch.zeros(0, wl.k, device="cuda")
+    tid = torch.zeros(0, wl.k, dtype=torch.int32, device="cuda")
+    out = layer.forward(x, tw, tid)
+    torch.cuda.synchronize()
+    assert out.shape == (0, wl.H)
+    assert mq.mq_device_status() == 0
+
+
 def test_forward_fine_grained_full():
     """E=128, k=8, H=2048, I=768 with Zipf-skewed routing (zero-token experts)."""
     layer = Layer(W["fine"], seed=0)
