@@ -120,6 +120,16 @@ def test_forward_empty_batch_uint4():
     assert mq.mq_device_status() == 0
 
 
+@pytest.mark.parametrize("bits,T", [(8, 50), (8, 300), (4, 50)])
+def test_forward_single_expert(bits, T):
+    """E = 1, k = 1: the MoE layer is one dense MLP whose router weight is 1;
+    every token lands in the one expert's segment (several token tiles)."""
+    wl = synth.Workload(f"dense_b{bits}_T{T}", E=1, k=1, H=256, I=384, Ts=(T,), bits=bits,
+                        group_size=128 if bits == 4 else -1, has_zp=bits == 4)
+    layer = Layer(wl, seed=T + bits)
+    assert _run(layer, T, seed=T) <= FWD_TOL
+
+
 def test_forward_fine_grained_full():
     """E=128, k=8, H=2048, I=768 with Zipf-skewed routing (zero-token experts)."""
     layer = Layer(W["fine"], seed=0)
