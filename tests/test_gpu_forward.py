@@ -130,6 +130,25 @@ def test_forward_single_expert(bits, T):
     assert _run(layer, T, seed=T) <= FWD_TOL
 
 
+@pytest.mark.parametrize("T", [16, 64, 128, 256])
+def test_forward_hot_expert_fills_whole_tiles(tiny, T):
+    """Every token's first choice is expert 5, so its segment holds exactly T
+    slots: a whole number of token tiles (16, 32 or 128 rows), no ragged
+    tail, with the second choices spread over the other experts."""
+    x, _ = inputs(tiny.wl, T, seed=T + 7)
+    lg = synth.router_logits(T, tiny.E, seed=T + 7, device="cuda")
+    lg[:, 5] += 20.0
+    tw, tid = mq.moe_topk_route(lg, tiny.k, True)
+    ids = tid.cpu().numpy()
+    assert (ids[:, 0] == 5).all() and (ids[:, 1] != 5).all()
+    out = tiny.forward(x, tw, tid)
+    torch.cuda.synchronize()
+    assert mq.mq_device_status() == 0
+    ex = tiny.oracle_experts(np.unique(ids))
+    ref = oracle.moe_forward(x.float().cpu().numpy(), ex, tw.cpu().numpy(), ids)
+    check_forward(out.float().cpu().numpy(), ref, what=f"hot expert T={T}")
+
+
 def test_forward_fine_grained_full():
     """E=128, k=8, H=2048, I=768 with Zipf-skewed routing (zero-token experts)."""
     layer = Layer(W["fine"], seed=0)
