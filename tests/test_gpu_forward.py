@@ -149,6 +149,17 @@ def test_forward_hot_expert_fills_whole_tiles(tiny, T):
     check_forward(out.float().cpu().numpy(), ref, what=f"hot expert T={T}")
 
 
+@pytest.mark.parametrize("bits", [8, 4])
+def test_forward_128_row_tiles_with_k_splits(bits):
+    """Two experts, H = 512, I = 4096, T = 100: 128-row token tiles, and
+    the down GEMM split eight ways over K to fill the SMs (the split rule of
+    batches beyond 64 tokens)."""
+    wl = synth.Workload(f"split_b{bits}", E=2, k=1, H=512, I=4096, Ts=(100,), bits=bits,
+                        group_size=128 if bits == 4 else -1, has_zp=bits == 4)
+    layer = Layer(wl, seed=bits)
+    assert _run(layer, 100, seed=3) <= FWD_TOL
+
+
 def test_forward_fine_grained_full():
     """E=128, k=8, H=2048, I=768 with Zipf-skewed routing (zero-token experts)."""
     layer = Layer(W["fine"], seed=0)
