@@ -92,6 +92,20 @@ def test_layer_mixtral_split_k():
     _check(layer, x, tw, tid, "mixtral T=3")
 
 
+def test_layer_128_row_tiles_with_k_splits():
+    """Two experts, H = 512, I = 4096, T = 100: 128-row tiles and the down
+    units split eight ways over K, every split waiting for its token tile;
+    bitwise equal to the two-launch path with the same tiles."""
+    wl = synth.Workload("layer_split", E=2, k=1, H=512, I=4096, Ts=(100,))
+    layer = Layer(wl, seed=12)
+    x, lg = inputs(wl, 100, seed=12)
+    tw, tid = mq.moe_topk_route(lg, wl.k, True)
+    out = _check(layer, x, tw, tid, "two experts, K splits")
+    two = layer.forward(x, tw, tid, path="tc")
+    torch.cuda.synchronize()
+    assert torch.equal(out, two)
+
+
 def test_layer_in_place(tiny):
     """out == x (fused_experts' inplace): x is gathered before any output is
     written, also when one launch runs both GEMMs."""
