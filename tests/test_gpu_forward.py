@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import oracle
-from moe_helpers import FWD_TOL, Layer, check_forward, inputs
+from moe_helpers import FWD_TOL, Layer, check_forward, forward_error, inputs, plain_error
 from weight_quantized_moe_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -185,17 +185,42 @@ def test_forward_w4a16_group_sizes(gs, zp, H, I):
 
 
 @pytest.mark.parametrize("E,k,H,I,gs,zp,T", [(6, 2, 256, 384, 128, True, 48),
-                                              (20, 4, 384, 256, 64, True, 40),
-                                              (20, 3, 640, 384, 128, False, 64)])
+                                              (20, 3, 640, 384, 128, False, 64),
+                                              (20, 4, 384, 256, 64, True, 120),
+                                              (20, 10, 640, 384, 128, False, 64)])
 def test_forward_w4a16_tile_shapes(E, k, H, I, gs, zp, T):
-    """uint4 32-row tiles (up to 16 experts, 33-64 tokens) and 64-row tiles
-    (more experts): two issuers on two accumulator buffers, or on one buffer
-    with three tensor-memory stages; units of one, two and three MMA steps,
-    the last stage of a unit half-filled (K = 384, 640)."""
+    """uint4 tile widths: 32 rows (up to 16 experts, 33-64 tokens), 16 and
+    32 rows for layers of more experts while the mean slots per expert stay
+    below 10 and 28 (T = 64 and T = 120 here), 64 rows beyond that (k = 10
+    of 20 experts at T = 64: one accumulator buffer, three stages); units of
+    one, two and three MMA steps, the last stage of a unit half-filled
+    (K = 384, 640).
+
+    These layers are small (the down GEMM sums 256 to 384 products per
+    output), and the act intermediate's bf16 rounding alone then reaches the
+    bound at the outliers (E=20, I=256, T=120: 1.1e-2 of the RMS against the
+    exact oracle, the same with every tile width).  As for the format
+    variants, the bound is checked against the oracle with that rounding
+    modelled; the error against the exact oracle is printed beside it."""
     wl = synth.Workload(f"w4a16_E{E}_T{T}", E=E, k=k, H=H, I=I, Ts=(T,), bits=4, group_size=gs,
                         has_zp=zp)
     layer = Layer(wl, seed=E + T)
-    assert _run(layer, T, seed=T) <= FWD_TOL
+    x, lg = inputs(wl, T, T)
+    tw, tid = mq.moe_topk_route(lg, k, True)
+    out = layer.forward(x, tw, tid)
+    torch.cuda.synchronize()
+    assert mq.mq_device_status() == 0
+    ids = tid.cpu().numpy()
+    ow, oid = oracle.topk_route(lg.cpu().numpy(), k, True)
+    assert np.array_equal(ids, oid)
+    ex = layer.oracle_experts(np.unique(ids))
+    xf = x.float().cpu().numpy()
+    got = out.float().cpu().numpy()
+    exact = oracle.moe_forward(xf, ex, ow, oid)
+    ref = oracle.moe_forward(xf, ex, ow, oid, intermediate="bf16")
+    check_forward(got, ref, what=f"{wl.name} vs the bf16-intermediate oracle (forward error "
+                  f"{forward_error(got, exact):.3e}, plain {plain_error(got, exact):.3e} vs the "
+                  f"exact oracle);")
 
 
 @pytest.mark.parametrize("T", [24, 40, 100])

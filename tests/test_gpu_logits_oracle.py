@@ -10,8 +10,8 @@ of every sampled token is compared.  The sizes span the kernels' plans:
 16-token tiles with two MMA issuers and split-K 4-8 in the down GEMM
 (Mixtral-shaped T = 1, 8, 32), 64-token tiles (T = 64), the fused router in
 the align kernel (small T·k·ceil(E/32)) and the separate router kernel
-(fine-grained T = 512), and the uint4 path at T = 1, 32, 48 and 64 (16- and
-64-row tiles) -- each with the
+(fine-grained T = 512), and the uint4 path at T = 1 to 192 (16- and 32-row
+tiles) -- each with the
 default kernels (tcgen05 consumers; one launch for both GEMMs of the
 fine-grained layer at T = 512), with the warp-level-MMA consumers forced
 for both GEMMs, and (8-bit) with both GEMMs forced into one launch.
@@ -92,10 +92,15 @@ def test_logits_forward_fine_grained(T, path):
 @pytest.mark.parametrize("path", ["auto", "decode"])
 @pytest.mark.parametrize("T", [1, 32, 48, 64])
 def test_logits_forward_w4a16(T, path):
-    """T = 48 and 64 take 64-row tiles, which for uint4 weights run two
-    issuers on one accumulator buffer and three tensor-memory stages."""
     layer = Layer(W["w4a16"], seed=0)
     _logits_case(layer, T, seed=40 + T, path=path)
+
+
+@pytest.mark.parametrize("T", [128, 192])
+def test_logits_forward_w4a16_mid_batches(T):
+    """32-row uint4 tiles beyond 64 tokens (mean slots per expert 12 and 18)."""
+    layer = Layer(W["w4a16"], seed=0)
+    _logits_case(layer, T, seed=40 + T)
 
 
 def test_sample_tokens_covers_first_and_last_slot():

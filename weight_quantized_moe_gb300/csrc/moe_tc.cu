@@ -1908,8 +1908,20 @@ TcPlan tc_plan(int T, int H, int I, int E, int k, int bits) {
   // 8-bit layers of many experts take 32-row tiles from 17 tokens (Zipf
   // routing puts most tokens on a few experts: fine-grained T=32 step 51.5
   // -> 46.4 us; W4A16 and the Mixtral-shaped layer lose 0.3-1 % with them).
-  const int bn = T > 64 ? 128
-                        : (T > 32 ? (E <= 16 ? 32 : 64) : (T > 16 && E > 16 && bits == 8 ? 32 : 16));
+  int bn = T > 64 ? 128
+                  : (T > 32 ? (E <= 16 ? 32 : 64) : (T > 16 && E > 16 && bits == 8 ? 32 : 16));
+  // uint4 layers of more than 16 experts keep 16- and 32-row tiles while the
+  // mean number of slots per expert stays below 10 and 28.  A uint4 stage
+  // costs as many MMAs as an int8 step for half the bytes, and the small
+  // tiles run the deepest pipeline: two issuers, two accumulator buffers,
+  // three tensor-memory stages.  W4A16 E=64, k=6, uniform routing, step in
+  // us with the L2 flushed, tiles 16 / 32 / default:
+  // T=64 152 / 158 / 161 (64-row), T=128 161 / 159 / 186, T=192 231 / 162 /
+  // 189, T=256 268 / 171 / 191, T=384 - / 253 / 197 (128-row).
+  if (bits == 4 && E > 16) {
+    if (S <= 10 * (int64_t)E) bn = 16;
+    else if (S <= 28 * (int64_t)E) bn = 32;
+  }
   pl.bn = bn;
   // K splits of the down GEMM.  Decode batches: the split count whose units
   // (live experts x H / 128 x splits) fill the SMs most evenly (dec_splits;
